@@ -1,0 +1,6 @@
+"""fp64 CPU oracle of the eviction pass and the flat decode attention.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline legs of ``bench.py`` import it; the library never does.
+"""
+from .kvevict_oracle import *  # noqa: F401,F403
