@@ -1,0 +1,212 @@
+/*
+ * kvevict.h -- C ABI of the GB300 (sm_103a) head-adaptive KV-cache eviction pass
+ * and the flat variable-length decode attention that runs over its result.
+ *
+ * Method (cited by page title and section):
+ *   "Ada-KV: Optimizing KV Cache Eviction by Adaptive Budget Allocation for
+ *    Efficient LLM Inference": Algorithm 1 (adaptive budget allocation),
+ *    Algorithm 2 (integration with SnapKV-style observation-window scoring),
+ *    the flat cache layout with a custom cache-update kernel and variable-length
+ *    attention, and the GQA group-mean criterion.
+ *   "LAVa: Layer-wise KV Cache Eviction with Dynamic Budget Allocation":
+ *    Definition 1 (LAVa score), head-flattened layer-wise eviction,
+ *    uncertainty (entropy) based layer budgets, GQA group max.
+ *   "CriticalKV: Optimizing KV Cache Eviction from an Output Perturbation
+ *    Perspective": two-stage greedy selection with (A + eps) * ||(V W^O)_j||_1,
+ *    plugged into Ada-KV.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All tensor arguments are DEVICE pointers, contiguous, head-major, and
+ *   16-byte aligned.  `d` must be a multiple of 8.  Violations return
+ *   KV_ERR_INVALID_ARG before anything is enqueued.
+ * - The caller owns every buffer.  The library allocates nothing, frees
+ *   nothing and never synchronises implicitly: all work is enqueued on
+ *   `stream` (a cudaStream_t passed as void*; NULL is the legacy default
+ *   stream).  Inputs are read-only.
+ * - `ws` is a caller-provided device workspace of at least
+ *   kv_workspace_size(op, shape) bytes for the op it is passed to.  Its first
+ *   256 bytes hold a device error word.  Zero the whole workspace once before
+ *   its first use; the library keeps the error word sticky across calls until
+ *   kv_check_device_status() reads and clears it.  Calls that share one
+ *   workspace must be ordered on one stream.
+ * - Notation: B = batch (sequences), L = layers, Hq / Hkv = query / KV heads
+ *   (Hq a multiple of Hkv, G = Hq/Hkv, query head q uses KV head q / G),
+ *   d = head dim, n = prefix length, w = observation window (the last w
+ *   positions), C = n - w candidate positions, pool = max-pool width (odd).
+ * - Ties in every Top-k are broken by total orders: layer-wide
+ *   (score desc, head asc, position asc); per head (score desc, position asc).
+ *   Scores must be finite and >= 0 (they are, by construction).
+ */
+#ifndef KVEVICT_H_
+#define KVEVICT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KV_API __attribute__((visibility("default")))
+#else
+#define KV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KV_OK = 0,
+  KV_ERR_INVALID_ARG = 1,   /* bad shape, pointer, alignment or parameter        */
+  KV_ERR_UNSUPPORTED = 2,   /* valid but not built for this shape / dtype        */
+  KV_ERR_WORKSPACE = 3,     /* ws too small                                      */
+  KV_ERR_CAPACITY = 4,      /* flat buffer too small for what the shape implies  */
+  KV_ERR_CUDA = 5,          /* a CUDA launch or runtime call failed              */
+  KV_ERR_DEVICE_CHECK = 6   /* a device-side check fired (see kv_check_device_status) */
+} kv_status;
+
+typedef enum { KV_BF16 = 0, KV_F32 = 1 } kv_dtype;
+typedef enum { KV_SCORE_ADA = 0, KV_SCORE_LAVA = 1, KV_SCORE_CRITICAL = 2 } kv_score_mode;
+typedef enum { KV_GROUP_MEAN = 0, KV_GROUP_MAX = 1 } kv_group_reduce;
+typedef enum { KV_OP_SCORE = 0, KV_OP_ALLOCATE = 1, KV_OP_COMPACT = 2, KV_OP_DECODE = 3 } kv_op;
+
+/* Shape of one eviction problem: B sequences x L layers of one model. */
+typedef struct {
+  int32_t batch, layers, hq, hkv, d, n, w, pool;
+  int32_t dtype;            /* kv_dtype: element type of q_win, k, v, w_o, q, k_new, v_new, out */
+} kv_shape;
+
+/* Bytes of device workspace `op` needs for `shape` (0 for an invalid shape). */
+KV_API size_t kv_workspace_size(int op, const kv_shape* shape);
+
+/*
+ * kv_score -- observation-window scores of every candidate position.
+ *
+ * Ada-KV Algorithm 2 (scoring steps), LAVa Definition 1, CriticalKV's
+ * projected-value norm.  For every (b, l, KV head g):
+ *   z[q,t,j] = q_win[q,t] . k[g,j] / sqrt(d), causal: window row t sees j <= n-w+t
+ *   P[q,t,:] = softmax_j z[q,t,:]                         (over all visible keys)
+ *   a[q,j]   = (1/w) sum_t P[q,t,j]                        j < C
+ *   p[q,j]   = max over |j'-j| <= pool/2, 0 <= j' < C of a[q,j']
+ *   s[g,j]   = mean (KV_GROUP_MEAN) or max (KV_GROUP_MAX) over the G query heads
+ *   LAVA:      s[g,j] *= max_k ||v[g,k]||_1
+ *   CRITICAL:  crit_norm[g,j] = || v[g,j] W_O[l,g] ||_1  (the sum runs over D = model_dim)
+ *
+ * q_win     [B][L][Hq][w][d]    dtype
+ * k, v      [B][L][Hkv][n][d]   dtype   (v is read by LAVA and CRITICAL only; may be NULL otherwise)
+ * w_o       [L][Hkv][d][D]      dtype   CRITICAL only, else NULL; model_dim = D (multiple of 8)
+ * scores    [B][L][Hkv][C]      float32 out
+ * crit_norm [B][L][Hkv][C]      float32 out, CRITICAL only, else NULL
+ */
+KV_API kv_status kv_score(const kv_shape* shape, int mode, int group,
+                   const void* q_win, const void* k, const void* v,
+                   const void* w_o, int32_t model_dim,
+                   float* scores, float* crit_norm,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * kv_allocate -- per-head budgets (Ada-KV Algorithm 1 + safeguard; LAVa layer budgets).
+ *
+ * layer_entropy_mode = 0: budget [B][L] int64 is the layer budget B including
+ *   the w*Hkv window rows.  B' = B - w*Hkv must lie in [0, Hkv*C].
+ * layer_entropy_mode = 1: budget [B] int64 is one total over the L layers of a
+ *   sequence (including all windows).  Each layer's selectable share of
+ *   R = total - L*w*Hkv is proportional to its score entropy
+ *   e_l = -sum s^ ln s^ / (Hkv*n), s^ = s / sum s over the layer; layers capped
+ *   at Hkv*C give their overflow to the others; floors plus one unit each to
+ *   the largest fractional parts (ties to the lower layer); all-zero entropies
+ *   split uniformly.
+ * Then per layer: f_g = number of head-g entries among the layer-wide top B'
+ *   scores, and the safeguard blend with alpha = alpha_num/alpha_den, the
+ *   weight of the UNIFORM share (alpha = 1: uniform SnapKV budgets; the
+ *   Ada-KV page's own alpha' maps to alpha = 1 - alpha'):
+ *     X_g = a*B' + (b-a)*Hkv*f_g,  B_g = floor(X_g / (b*Hkv)),
+ *     the B' - sum B_g leftover units go to the largest X_g mod (b*Hkv), ties to the lower head.
+ *   sum_g B_g = B' exactly and B_g >= floor(alpha*B'/Hkv).
+ *
+ * scores       [B][L][Hkv][C] float32 (from kv_score)
+ * budget       [B][L] or [B]  int64 (device)
+ * layer_budget [B][L]         int32 out: B_l including the window rows
+ * head_budget  [B][L][Hkv]    int32 out: B_g + w, the kept length of head g
+ * An out-of-range budget sets the device error word and is clamped.
+ */
+KV_API kv_status kv_allocate(const kv_shape* shape, const float* scores, const int64_t* budget,
+                      int layer_entropy_mode, uint32_t alpha_num, uint32_t alpha_den,
+                      int32_t* layer_budget, int32_t* head_budget,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * kv_compact -- per-head Top-B_g selection and the flat cache gather
+ * (Ada-KV Algorithm 2, selection and concatenation of the window; the flat
+ * layout that concatenates every head of a layer into one tensor;
+ * CriticalKV two-stage selection when crit_norm != NULL).
+ *
+ * Head g of (b, l) keeps B_g = head_budget - w positions: the top B_g by
+ * (score desc, position asc); with crit_norm: stage 1 keeps the top
+ * floor(crit_alpha_num * B_g / crit_alpha_den) by score, stage 2 the top
+ * remaining by kappa = (score + crit_eps) * crit_norm, formed in float32.
+ * Kept positions are written in ascending order, followed by the window
+ * positions C..n-1.
+ *
+ * Flat layout: one buffer holds every (b, l, g) back to back in that order.
+ * Head (b,l,g) owns rows [cu_off[b][l][g], cu_off[b][l][g+1]), of size
+ * head_budget + reserve; its first lens = head_budget rows are filled, the
+ * reserve rows are left for decode appends.  cu_off[b][l][Hkv] ==
+ * cu_off[b][l+1][0] and the last entry is the total row count, which fits in
+ * flat_capacity_rows when that is sum over (b,l) of (B_l + Hkv*reserve).
+ *
+ * k, v        [B][L][Hkv][n][d] dtype
+ * scores      [B][L][Hkv][C] float32; crit_norm same shape or NULL
+ * head_budget [B][L][Hkv] int32 (from kv_allocate)
+ * kept_idx    [flat_capacity_rows] int32 out: source position of each flat row, -1 for reserve rows
+ * cu_off      [B][L][Hkv+1] int64 out
+ * lens        [B][L][Hkv] int32 out
+ * k_flat, v_flat [flat_capacity_rows][d] dtype out
+ * Rows past flat_capacity_rows are never written; the device error word is set instead.
+ */
+KV_API kv_status kv_compact(const kv_shape* shape, const void* k, const void* v,
+                     const float* scores, const float* crit_norm,
+                     uint32_t crit_alpha_num, uint32_t crit_alpha_den, float crit_eps,
+                     const int32_t* head_budget, int32_t reserve,
+                     int32_t* kept_idx, int64_t* cu_off, int32_t* lens,
+                     void* k_flat, void* v_flat, int64_t flat_capacity_rows,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * flat_decode_attn -- one decode step of attention over the flat cache
+ * (Ada-KV formal model: append k, v, then A = softmax(q K^T * scale), o = A V;
+ * variable-length attention over the uneven per-head lengths).
+ *
+ * If k_new/v_new are given, row cu_off[b][l][g] + lens[b][l][g] of k_flat /
+ * v_flat is written first and lens grows by one (the new token attends to
+ * itself); with no reserve row left the device error word is set and that
+ * head attends without the append.  Then for every query head q of KV head g:
+ *   out[b][l][q] = sum_{r < lens} softmax_r(q . k_flat[cu + r] * softmax_scale) v_flat[cu + r]
+ * with float32 accumulation.  A head with lens == 0 writes zeros.
+ *
+ * q            [B][L][Hq][d] dtype
+ * k_new, v_new [B][L][Hkv][d] dtype, or both NULL
+ * k_flat, v_flat, cu_off, lens as written by kv_compact (lens is updated in place)
+ * flat_capacity_rows: rows of k_flat / v_flat; rows at or past it are never read or written
+ *   (an append that would land there sets the device error word instead)
+ * out          [B][L][Hq][d] dtype
+ * `shape.n` bounds the head length (lens <= n + reserve); `w` and `pool` are unused.
+ */
+KV_API kv_status flat_decode_attn(const kv_shape* shape, const void* q,
+                           const void* k_new, const void* v_new,
+                           void* k_flat, void* v_flat, const int64_t* cu_off, int32_t* lens,
+                           int64_t flat_capacity_rows, float softmax_scale, void* out,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, reads the device error word of `ws` and clears it.
+ * Returns KV_OK or KV_ERR_DEVICE_CHECK (KV_ERR_CUDA if the copy fails).
+ * `info` (nullable) receives the first recorded check code. */
+KV_API kv_status kv_check_device_status(void* ws, void* stream, uint32_t* info);
+
+/* Static description of a status code. */
+KV_API const char* kv_status_string(kv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVEVICT_H_ */

@@ -1,0 +1,239 @@
+// Per-head selection and the flat cache gather.
+//
+// Ada-KV Algorithm 2: per-head Top-B_g eviction decision, selection of the kept
+// K/V rows, concatenation of the observation window; the flat layout that puts
+// every head of a layer into one tensor (cu_seqlens-style offsets), filled by a
+// cache-update kernel.  CriticalKV: two-stage greedy selection, stage 1 by the
+// attention score, stage 2 by (A + eps) * ||(V W^O)_j||_1.
+#include "kv_internal.cuh"
+#include "radix_select.cuh"
+
+namespace kv {
+
+namespace {
+constexpr int kScanThreads = 1024;
+constexpr int kSelThreads = 1024;
+constexpr int kGatherThreads = 256;
+}
+
+// 64-bit inclusive block scan (one value per thread).
+__device__ __forceinline__ int64_t block_incl_scan64(int64_t v, int64_t* scratch, int64_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t s = lane < nw ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < nw) scratch[lane] = s;
+  }
+  __syncthreads();
+  const int64_t base = warp > 0 ? scratch[warp - 1] : 0;
+  *total = scratch[nw - 1];
+  __syncthreads();
+  return base + x;
+}
+
+// Offsets of every head in the flat buffer and the initial lengths.
+__global__ void __launch_bounds__(kScanThreads)
+compact_offsets(const int32_t* __restrict__ head_budget, int64_t H, int Hkv, int w, int n,
+                int reserve, int64_t cap, int64_t* __restrict__ cu, int32_t* __restrict__ lens,
+                WsHeader* hdr) {
+  __shared__ int64_t scratch[32];
+  int64_t carry = 0;
+  for (int64_t t0 = 0; t0 < H; t0 += kScanThreads) {
+    const int64_t h = t0 + threadIdx.x;
+    int64_t val = 0;
+    if (h < H) {
+      int hb = head_budget[h];
+      if (hb < w || hb > n) {
+        raise_dev(hdr, DEV_HEAD_BUDGET, (unsigned)h);
+        hb = hb < w ? w : n;
+      }
+      lens[h] = hb;
+      val = (int64_t)hb + reserve;
+    }
+    int64_t tot;
+    const int64_t incl = block_incl_scan64(val, scratch, &tot);
+    if (h < H) {
+      const int64_t seg = h / Hkv;
+      const int g = (int)(h - seg * Hkv);
+      cu[seg * (Hkv + 1) + g] = carry + incl - val;
+      if (g == Hkv - 1) cu[seg * (Hkv + 1) + Hkv] = carry + incl;
+    }
+    carry += tot;
+  }
+  if (threadIdx.x == 0 && carry > cap) raise_dev(hdr, DEV_FLAT_CAPACITY, 0);
+}
+
+// One CTA per head: threshold(s), ordered kept positions, window and reserve rows.
+__global__ void __launch_bounds__(kSelThreads)
+compact_select(const float* __restrict__ scores, const float* __restrict__ crit, uint32_t can,
+               uint32_t cad, float ceps, const int32_t* __restrict__ lens,
+               const int64_t* __restrict__ cu, int Hkv, int C, int w, int reserve,
+               int32_t* __restrict__ kept, int64_t cap, uint32_t* __restrict__ flags,
+               int64_t words, WsHeader* hdr) {
+  __shared__ RadixSmem rs;
+  __shared__ uint32_t eqscr[32];
+  const int64_t h = blockIdx.x;
+  const int64_t seg = h / Hkv;
+  const int g = (int)(h - seg * Hkv);
+  const int64_t base = cu[seg * (Hkv + 1) + g];
+  const int64_t Bg = (int64_t)lens[h] - w;   // lens was clamped to [w, n]
+  const float* S = scores + h * (int64_t)C;
+  if (crit == nullptr) {
+    uint32_t tau, keq;
+    block_topk_threshold<kSelThreads>(C, Bg, [&](int64_t i) { return score_key(S[i]); }, rs, tau,
+                                      keq);
+    {
+      uint32_t carry = 0, eqc = 0;
+      for (int t0 = 0; t0 < C; t0 += kSelThreads) {
+        const int j = t0 + threadIdx.x;
+        const uint32_t key = j < C ? score_key(S[j]) : 0u;
+        const uint32_t ise = (j < C && key == tau) ? 1u : 0u;
+        uint32_t etot;
+        const uint32_t eincl = block_incl_scan(ise, eqscr, &etot);
+        const uint32_t erank = eqc + eincl - ise;
+        const uint32_t f = (j < C) && (key > tau || (ise && erank < keq)) ? 1u : 0u;
+        uint32_t tot;
+        const uint32_t incl = block_incl_scan(f, rs.scratch, &tot);
+        if (f) {
+          const int64_t row = base + carry + incl - 1;
+          if (row < cap) kept[row] = j;
+        }
+        carry += tot;
+        eqc += etot;
+      }
+      if (threadIdx.x == 0 && carry != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
+    }
+  } else {
+    const float* Cn = crit + h * (int64_t)C;
+    uint32_t* F = flags + h * words;
+    const int64_t K1 = ((int64_t)can * Bg) / cad;
+    const int64_t K2 = Bg - K1;
+    uint32_t tau1, keq1;
+    block_topk_threshold<kSelThreads>(C, K1, [&](int64_t i) { return score_key(S[i]); }, rs,
+                                      tau1, keq1);
+    // stage-1 membership bits
+    {
+      uint32_t eqc = 0;
+      for (int t0 = 0; t0 < C; t0 += kSelThreads) {
+        const int j = t0 + threadIdx.x;
+        const uint32_t key = j < C ? score_key(S[j]) : 0u;
+        const uint32_t ise = (j < C && key == tau1) ? 1u : 0u;
+        uint32_t etot;
+        const uint32_t eincl = block_incl_scan(ise, eqscr, &etot);
+        const uint32_t erank = eqc + eincl - ise;
+        const bool f = (j < C) && (key > tau1 || (ise && erank < keq1));
+        const uint32_t bits = __ballot_sync(0xffffffffu, f);
+        if ((threadIdx.x & 31) == 0 && j < C) F[j >> 5] = bits;
+        eqc += etot;
+      }
+    }
+    __syncthreads();
+    auto key2 = [&](int64_t i) -> uint32_t {
+      if ((F[i >> 5] >> (i & 31)) & 1u) return 0u;
+      const float kap = __fmul_rn(__fadd_rn(S[i], ceps), Cn[i]);
+      return score_key(kap) + 1u;
+    };
+    uint32_t tau2, keq2;
+    block_topk_threshold<kSelThreads>(C, K2, key2, rs, tau2, keq2);
+    uint32_t carry = 0, eqc = 0;
+    for (int t0 = 0; t0 < C; t0 += kSelThreads) {
+      const int j = t0 + threadIdx.x;
+      const bool in1 = j < C && ((F[j >> 5] >> (j & 31)) & 1u);
+      const uint32_t k2 = j < C ? key2(j) : 0u;
+      const uint32_t ise = (j < C && !in1 && k2 == tau2) ? 1u : 0u;
+      uint32_t etot;
+      const uint32_t eincl = block_incl_scan(ise, eqscr, &etot);
+      const uint32_t erank = eqc + eincl - ise;
+      const uint32_t f = (j < C) && (in1 || k2 > tau2 || (ise && erank < keq2)) ? 1u : 0u;
+      uint32_t tot;
+      const uint32_t incl = block_incl_scan(f, rs.scratch, &tot);
+      if (f) {
+        const int64_t row = base + carry + incl - 1;
+        if (row < cap) kept[row] = j;
+      }
+      carry += tot;
+      eqc += etot;
+    }
+    if (threadIdx.x == 0 && carry != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
+  }
+  for (int t = threadIdx.x; t < w + reserve; t += kSelThreads) {
+    const int64_t row = base + Bg + t;
+    if (row < cap) kept[row] = t < w ? C + t : -1;
+  }
+}
+
+// Copy the kept rows of K and V into the flat buffers, 16 bytes per thread.
+__global__ void __launch_bounds__(kGatherThreads)
+compact_gather(const char* __restrict__ k, const char* __restrict__ v,
+               const int32_t* __restrict__ kept, const int64_t* __restrict__ cu,
+               const int32_t* __restrict__ lens, int Hkv, int n, int row_bytes, int64_t cap,
+               char* __restrict__ kf, char* __restrict__ vf) {
+  const int64_t h = blockIdx.y;
+  const int64_t seg = h / Hkv;
+  const int g = (int)(h - seg * Hkv);
+  const int64_t base = cu[seg * (Hkv + 1) + g];
+  const int64_t len = lens[h];
+  const int vecs = row_bytes >> 4;
+  const char* Ks = k + h * (int64_t)n * row_bytes;
+  const char* Vs = v + h * (int64_t)n * row_bytes;
+  const int64_t total = len * vecs;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = idx / vecs;
+    const int c = (int)(idx - r * vecs);
+    const int64_t row = base + r;
+    if (row >= cap) continue;
+    const int64_t src = kept[row];
+    if (src < 0 || src >= n) continue;   // never read outside the source head
+    const uint4 a = reinterpret_cast<const uint4*>(Ks + src * row_bytes)[c];
+    const uint4 b = reinterpret_cast<const uint4*>(Vs + src * row_bytes)[c];
+    reinterpret_cast<uint4*>(kf + row * row_bytes)[c] = a;
+    reinterpret_cast<uint4*>(vf + row * row_bytes)[c] = b;
+  }
+}
+
+CompactPlan compact_plan(const Shape& s, bool critical) {
+  CompactPlan p{};
+  size_t off = kWsHeader;
+  p.off_flags = off;
+  p.flag_words = critical ? cdiv(s.C() > 0 ? s.C() : 1, 32) : 0;
+  off += align_up((size_t)s.units() * p.flag_words * sizeof(uint32_t), 256);
+  p.off_end = off;
+  return p;
+}
+
+cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const float* scores,
+                           const float* crit, uint32_t can, uint32_t cad, float ceps,
+                           const int32_t* head_budget, int reserve, int32_t* kept,
+                           int64_t* cu, int32_t* lens, void* kf, void* vf, int64_t cap,
+                           char* ws, const CompactPlan& p, cudaStream_t st) {
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  const int64_t H = s.units();
+  compact_offsets<<<1, kScanThreads, 0, st>>>(head_budget, H, s.Hkv, s.w, s.n, reserve, cap, cu,
+                                               lens, hdr);
+  compact_select<<<(unsigned)H, kSelThreads, 0, st>>>(
+      scores, crit, can, cad, ceps, lens, cu, s.Hkv, s.C(), s.w, reserve, kept, cap,
+      reinterpret_cast<uint32_t*>(ws + p.off_flags), p.flag_words, hdr);
+  const int row_bytes = s.d * s.esize();
+  int gx = (int)cdiv((int64_t)num_sms() * 16, H);
+  if (gx < 1) gx = 1;
+  if (gx > 64) gx = 64;
+  compact_gather<<<dim3(gx, (unsigned)H), kGatherThreads, 0, st>>>(
+      (const char*)k, (const char*)v, kept, cu, lens, s.Hkv, s.n, row_bytes, cap, (char*)kf,
+      (char*)vf);
+  return cudaGetLastError();
+}
+
+}  // namespace kv

@@ -1,0 +1,112 @@
+// Internal helpers shared by the sm_103a kernels of libkvevict.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvevict.h"
+
+namespace kv {
+
+// ---------------------------------------------------------------------------
+// Workspace header: the first 256 bytes of every workspace.
+// ---------------------------------------------------------------------------
+struct WsHeader {
+  unsigned int err;       // first device check code that fired (0 = none)
+  unsigned int info;      // optional detail of that check
+  unsigned int pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+constexpr size_t kWsHeader = 256;
+
+// Device check codes (written to WsHeader::err).
+enum DevErr : unsigned int {
+  DEV_OK = 0,
+  DEV_BUDGET_RANGE = 1,     // a budget outside [w*Hkv, n*Hkv] (clamped)
+  DEV_FLAT_CAPACITY = 2,    // the offsets exceed flat_capacity_rows (rows skipped)
+  DEV_NO_RESERVE = 3,       // decode append with no reserve row left (append skipped)
+  DEV_HEAD_BUDGET = 4,      // head_budget outside [w, n] (clamped)
+  DEV_WAIT_TIMEOUT = 5,     // a bounded wait gave up
+  DEV_SELECT = 6,           // a selection invariant failed (should never happen)
+};
+
+__device__ __forceinline__ void raise_dev(WsHeader* h, unsigned int code, unsigned int info = 0) {
+  if (atomicCAS(&h->err, 0u, code) == 0u) h->info = info;
+}
+
+// ---------------------------------------------------------------------------
+// Element access
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// Monotone key of a non-negative float: larger float <=> larger key.  Anything
+// that is not > 0 (zero, -0, negative, NaN) maps to 0.
+__device__ __forceinline__ uint32_t score_key(float x) {
+  return x > 0.0f ? __float_as_uint(x) : 0u;
+}
+
+// ---------------------------------------------------------------------------
+// Warp / block reductions
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ unsigned int warp_sum_u(unsigned int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Inclusive block-wide prefix sum of one unsigned value per thread.
+// `scratch` holds at least blockDim.x/32 entries.  Returns the inclusive prefix;
+// *total gets the block total.  All threads must call it.
+__device__ __forceinline__ unsigned int block_incl_scan(unsigned int v, unsigned int* scratch,
+                                                        unsigned int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  unsigned int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    unsigned int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned int s = lane < nw ? scratch[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      unsigned int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < nw) scratch[lane] = s;
+  }
+  __syncthreads();
+  unsigned int base = warp > 0 ? scratch[warp - 1] : 0u;
+  *total = scratch[nw - 1];
+  __syncthreads();
+  return base + x;
+}
+
+__host__ __device__ __forceinline__ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace kv

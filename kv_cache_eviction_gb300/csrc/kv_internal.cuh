@@ -1,0 +1,65 @@
+// Internal launch interface between the C ABI (kvevict_api.cu) and the kernels.
+#pragma once
+
+#include "kv_common.cuh"
+
+namespace kv {
+
+struct Shape {
+  int B, L, Hq, Hkv, d, n, w, pool, dtype;
+  __host__ __device__ int G() const { return Hq / Hkv; }
+  __host__ __device__ int C() const { return n - w; }
+  __host__ __device__ int R() const { return (Hq / Hkv) * w; }      // window rows per KV head
+  __host__ __device__ int64_t units() const { return (int64_t)B * L * Hkv; }
+  __host__ __device__ int64_t segments() const { return (int64_t)B * L; }
+  int esize() const { return dtype == KV_BF16 ? 2 : 4; }
+};
+
+// ----------------------------- scoring -------------------------------------
+struct ScorePlan {
+  int path;             // 0 = CUDA-core (SIMT), 1 = tcgen05
+  int chunk1, nchunk1;  // pass-1 keys per CTA and CTAs per unit
+  int chunk2, nchunk2;  // pass-2 candidates per CTA and CTAs per unit
+  size_t off_part, off_lse, off_vbar, off_end;
+};
+ScorePlan score_plan(const Shape& s, int mode);
+cudaError_t launch_score(const Shape& s, int mode, int group, const void* q_win, const void* k,
+                         const void* v, const void* w_o, int D, float* scores, float* crit,
+                         char* ws, const ScorePlan& p, cudaStream_t st);
+
+// ----------------------------- allocation ----------------------------------
+struct AllocPlan {
+  int nchunkE;          // entropy partial CTAs per segment
+  size_t off_bprime, off_epart, off_e, off_scratch, off_end;
+};
+AllocPlan alloc_plan(const Shape& s);
+cudaError_t launch_allocate(const Shape& s, const float* scores, const int64_t* budget,
+                            int entropy_mode, uint32_t an, uint32_t ad, int32_t* layer_budget,
+                            int32_t* head_budget, char* ws, const AllocPlan& p, cudaStream_t st);
+
+// ----------------------------- compaction ----------------------------------
+struct CompactPlan {
+  size_t off_flags, off_end;
+  int64_t flag_words;   // per head, when CriticalKV stage-1 flags are needed
+};
+CompactPlan compact_plan(const Shape& s, bool critical);
+cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const float* scores,
+                           const float* crit, uint32_t can, uint32_t cad, float ceps,
+                           const int32_t* head_budget, int reserve, int32_t* kept,
+                           int64_t* cu, int32_t* lens, void* kf, void* vf, int64_t cap,
+                           char* ws, const CompactPlan& p, cudaStream_t st);
+
+// ----------------------------- decode --------------------------------------
+struct DecodePlan {
+  int splits;
+  size_t off_part, off_end;
+};
+DecodePlan decode_plan(const Shape& s);
+cudaError_t launch_decode(const Shape& s, const void* q, const void* kn, const void* vn,
+                          void* kf, void* vf, const int64_t* cu, int32_t* lens, int64_t cap,
+                          float scale, void* out, char* ws, const DecodePlan& p,
+                          cudaStream_t st);
+
+int num_sms();
+
+}  // namespace kv

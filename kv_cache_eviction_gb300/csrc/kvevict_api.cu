@@ -1,0 +1,212 @@
+// C ABI of libkvevict: argument validation, workspace layout, dispatch.
+// Every check here runs on the host before anything is enqueued.
+#include <cmath>
+#include <cstring>
+
+#include "kv_internal.cuh"
+
+namespace kv {
+
+int num_sms() {
+  static int cached = 0;
+  if (cached == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      cached = v;
+    else
+      cached = 148;
+  }
+  return cached;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks common to every op.  Returns false on an invalid shape.
+static bool shape_ok(const kv_shape* sh, Shape* out) {
+  if (sh == nullptr) return false;
+  Shape s{sh->batch, sh->layers, sh->hq, sh->hkv, sh->d, sh->n, sh->w, sh->pool, sh->dtype};
+  if (s.B < 0 || s.L < 0 || s.Hq <= 0 || s.Hkv <= 0 || s.d <= 0 || s.n < 0 || s.w < 0) return false;
+  if (s.Hq % s.Hkv != 0) return false;
+  if (s.d % 8 != 0) return false;
+  if (s.w > s.n) return false;
+  if (s.pool < 1 || s.pool % 2 == 0) return false;
+  if (s.dtype != KV_BF16 && s.dtype != KV_F32) return false;
+  *out = s;
+  return true;
+}
+
+// Limits of the kernels as built (valid shapes outside them are KV_ERR_UNSUPPORTED).
+static bool shape_supported(const Shape& s) {
+  if (s.G() > 8) return false;
+  if (s.d > 128) return false;
+  if (s.R() > 256) return false;
+  if (s.Hkv > 256) return false;
+  if ((int64_t)s.Hkv * s.n >= (int64_t)1 << 31) return false;
+  return true;
+}
+
+static kv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KV_OK : KV_ERR_CUDA; }
+
+}  // namespace kv
+
+using namespace kv;
+
+extern "C" {
+
+size_t kv_workspace_size(int op, const kv_shape* shape) {
+  Shape s;
+  if (!shape_ok(shape, &s)) return 0;
+  switch (op) {
+    case KV_OP_SCORE: {
+      const ScorePlan a = score_plan(s, KV_SCORE_LAVA);
+      const ScorePlan b = score_plan(s, KV_SCORE_CRITICAL);
+      return a.off_end > b.off_end ? a.off_end : b.off_end;
+    }
+    case KV_OP_ALLOCATE: return alloc_plan(s).off_end;
+    case KV_OP_COMPACT: return compact_plan(s, true).off_end;
+    case KV_OP_DECODE: return decode_plan(s).off_end;
+    default: return 0;
+  }
+}
+
+kv_status kv_score(const kv_shape* shape, int mode, int group, const void* q_win, const void* k,
+                   const void* v, const void* w_o, int32_t model_dim, float* scores,
+                   float* crit_norm, void* ws, size_t ws_bytes, void* stream) {
+  Shape s;
+  if (!shape_ok(shape, &s)) return KV_ERR_INVALID_ARG;
+  if (mode < KV_SCORE_ADA || mode > KV_SCORE_CRITICAL) return KV_ERR_INVALID_ARG;
+  if (group != KV_GROUP_MEAN && group != KV_GROUP_MAX) return KV_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned16(ws)) return KV_ERR_INVALID_ARG;
+  if (s.units() == 0) return KV_OK;
+  if (s.n == 0 || s.w == 0) return KV_ERR_INVALID_ARG;
+  if (q_win == nullptr || k == nullptr || scores == nullptr) return KV_ERR_INVALID_ARG;
+  if (!aligned16(q_win) || !aligned16(k) || !aligned16(scores)) return KV_ERR_INVALID_ARG;
+  if (mode != KV_SCORE_ADA && (v == nullptr || !aligned16(v))) return KV_ERR_INVALID_ARG;
+  if (mode == KV_SCORE_CRITICAL) {
+    if (w_o == nullptr || crit_norm == nullptr || !aligned16(w_o) || !aligned16(crit_norm))
+      return KV_ERR_INVALID_ARG;
+    if (model_dim <= 0 || model_dim % 8 != 0) return KV_ERR_INVALID_ARG;
+  }
+  if (!shape_supported(s)) return KV_ERR_UNSUPPORTED;
+  const ScorePlan p = score_plan(s, mode);
+  if (ws_bytes < p.off_end) return KV_ERR_WORKSPACE;
+  return cuda_status(launch_score(s, mode, group, q_win, k, v, w_o, model_dim, scores,
+                                  crit_norm, static_cast<char*>(ws), p,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+kv_status kv_allocate(const kv_shape* shape, const float* scores, const int64_t* budget,
+                      int layer_entropy_mode, uint32_t alpha_num, uint32_t alpha_den,
+                      int32_t* layer_budget, int32_t* head_budget, void* ws, size_t ws_bytes,
+                      void* stream) {
+  Shape s;
+  if (!shape_ok(shape, &s)) return KV_ERR_INVALID_ARG;
+  if (layer_entropy_mode != 0 && layer_entropy_mode != 1) return KV_ERR_INVALID_ARG;
+  if (alpha_den == 0 || alpha_num > alpha_den || alpha_den > 65536u) return KV_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned16(ws)) return KV_ERR_INVALID_ARG;
+  if (s.units() == 0) return KV_OK;
+  if (scores == nullptr || budget == nullptr || layer_budget == nullptr || head_budget == nullptr)
+    return KV_ERR_INVALID_ARG;
+  if (!aligned16(scores) || !aligned16(budget) || !aligned16(layer_budget) ||
+      !aligned16(head_budget))
+    return KV_ERR_INVALID_ARG;
+  if (!shape_supported(s)) return KV_ERR_UNSUPPORTED;
+  const AllocPlan p = alloc_plan(s);
+  if (ws_bytes < p.off_end) return KV_ERR_WORKSPACE;
+  return cuda_status(launch_allocate(s, scores, budget, layer_entropy_mode, alpha_num, alpha_den,
+                                     layer_budget, head_budget, static_cast<char*>(ws), p,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+kv_status kv_compact(const kv_shape* shape, const void* k, const void* v, const float* scores,
+                     const float* crit_norm, uint32_t crit_alpha_num, uint32_t crit_alpha_den,
+                     float crit_eps, const int32_t* head_budget, int32_t reserve,
+                     int32_t* kept_idx, int64_t* cu_off, int32_t* lens, void* k_flat,
+                     void* v_flat, int64_t flat_capacity_rows, void* ws, size_t ws_bytes,
+                     void* stream) {
+  Shape s;
+  if (!shape_ok(shape, &s)) return KV_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned16(ws)) return KV_ERR_INVALID_ARG;
+  if (reserve < 0 || flat_capacity_rows < 0) return KV_ERR_INVALID_ARG;
+  if (s.units() == 0) return KV_OK;
+  if (k == nullptr || v == nullptr || scores == nullptr || head_budget == nullptr ||
+      kept_idx == nullptr || cu_off == nullptr || lens == nullptr || k_flat == nullptr ||
+      v_flat == nullptr)
+    return KV_ERR_INVALID_ARG;
+  const void* ptrs[] = {k, v, scores, head_budget, kept_idx, cu_off, lens, k_flat, v_flat};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return KV_ERR_INVALID_ARG;
+  if (crit_norm != nullptr) {
+    if (!aligned16(crit_norm)) return KV_ERR_INVALID_ARG;
+    if (crit_alpha_den == 0 || crit_alpha_num > crit_alpha_den || crit_alpha_den > 65536u)
+      return KV_ERR_INVALID_ARG;
+    if (!(crit_eps >= 0.0f) || std::isinf(crit_eps)) return KV_ERR_INVALID_ARG;
+  }
+  // The smallest flat buffer any valid budgets can need: every head keeps its window.
+  if (flat_capacity_rows < s.units() * (int64_t)(s.w + reserve)) return KV_ERR_CAPACITY;
+  if (!shape_supported(s)) return KV_ERR_UNSUPPORTED;
+  const CompactPlan p = compact_plan(s, crit_norm != nullptr);
+  if (ws_bytes < p.off_end) return KV_ERR_WORKSPACE;
+  return cuda_status(launch_compact(s, k, v, scores, crit_norm, crit_alpha_num, crit_alpha_den,
+                                    crit_eps, head_budget, reserve, kept_idx, cu_off, lens,
+                                    k_flat, v_flat, flat_capacity_rows, static_cast<char*>(ws),
+                                    p, static_cast<cudaStream_t>(stream)));
+}
+
+kv_status flat_decode_attn(const kv_shape* shape, const void* q, const void* k_new,
+                           const void* v_new, void* k_flat, void* v_flat, const int64_t* cu_off,
+                           int32_t* lens, int64_t flat_capacity_rows, float softmax_scale,
+                           void* out, void* ws, size_t ws_bytes, void* stream) {
+  Shape s;
+  if (!shape_ok(shape, &s)) return KV_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned16(ws)) return KV_ERR_INVALID_ARG;
+  if ((k_new == nullptr) != (v_new == nullptr)) return KV_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return KV_ERR_INVALID_ARG;
+  if (flat_capacity_rows < 0) return KV_ERR_INVALID_ARG;
+  if (s.units() == 0) return KV_OK;
+  if (q == nullptr || k_flat == nullptr || v_flat == nullptr || cu_off == nullptr ||
+      lens == nullptr || out == nullptr)
+    return KV_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k_flat, v_flat, cu_off, lens, out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return KV_ERR_INVALID_ARG;
+  if (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))) return KV_ERR_INVALID_ARG;
+  if (!shape_supported(s) || s.G() * s.d > 1024) return KV_ERR_UNSUPPORTED;
+  const DecodePlan p = decode_plan(s);
+  if (ws_bytes < p.off_end) return KV_ERR_WORKSPACE;
+  return cuda_status(launch_decode(s, q, k_new, v_new, k_flat, v_flat, cu_off, lens,
+                                   flat_capacity_rows, softmax_scale, out,
+                                   static_cast<char*>(ws), p, static_cast<cudaStream_t>(stream)));
+}
+
+kv_status kv_check_device_status(void* ws, void* stream, uint32_t* info) {
+  if (ws == nullptr || !aligned16(ws)) return KV_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WsHeader h;
+  if (cudaMemcpyAsync(&h, ws, 8, cudaMemcpyDeviceToHost, st) != cudaSuccess) return KV_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KV_ERR_CUDA;
+  if (h.err == 0) {
+    if (info) *info = 0;
+    return KV_OK;
+  }
+  if (info) *info = h.err;
+  if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return KV_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KV_ERR_CUDA;
+  return KV_ERR_DEVICE_CHECK;
+}
+
+const char* kv_status_string(kv_status status) {
+  switch (status) {
+    case KV_OK: return "ok";
+    case KV_ERR_INVALID_ARG: return "invalid argument";
+    case KV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case KV_ERR_WORKSPACE: return "workspace too small";
+    case KV_ERR_CAPACITY: return "flat buffer capacity too small";
+    case KV_ERR_CUDA: return "CUDA error";
+    case KV_ERR_DEVICE_CHECK: return "device-side check failed";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"
