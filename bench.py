@@ -1,0 +1,501 @@
+#!/usr/bin/env python3
+"""Throughput of the KV-cache eviction pass and the flat decode attention on GB300.
+
+One step = one eviction pass over every (sequence, layer) of the workload
+(kv_score -> kv_allocate -> kv_compact) followed by one decode step of
+flat_decode_attn over every layer (with the append).  The headline value is
+eviction-pass prefix tokens per second per layer: batch * n * L prefix tokens
+pass through one layer's eviction in (step time / L), i.e.
+value = batch * n * L / step_time, summed over ranks.  The second number, the
+flat varlen decode attention's HBM GB/s, is measured on its own with L2 flushed
+before every decode step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only other implementation of the
+method there is) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import os
+
+# The CPU oracle is timed single-threaded; pin the BLAS pools before numpy loads.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import json
+import math
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "eviction-pass prefix tokens/s per layer; flat varlen decode attn HBM GB/s"
+UNIT = "tokens/s/layer"
+DEFAULT_WORKLOAD = "mistral7b_128k_lava"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--decode-steps", type=int, default=-1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle sample (the cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(wl, use_cuda_inputs: bool):
+    """One KV head of (sequence 0, layer 0): its inputs as fp64 numpy arrays."""
+    import torch
+    from kv_cache_eviction_gb300 import workloads as W
+    dev = "cuda" if use_cuda_inputs else "cpu"
+    u = W.make_unit(wl, 0, 0, device=dev)
+    G = wl.hq // wl.hkv
+    to = lambda t: t.to("cpu", torch.float64).numpy()
+    out = {"q": to(u["q_win"][:G]), "k": to(u["k"][:1]), "v": to(u["v"][:1])}
+    if "w_o" in u:
+        out["w_o"] = to(u["w_o"][:1])
+    dec = W.make_decode_step(wl, 0, u["tau"], 0, 0, device=dev)
+    out["dq"], out["kn"], out["vn"] = to(dec["q"][:G]), to(dec["k_new"][:1]), to(dec["v_new"][:1])
+    del u
+    return out
+
+
+def oracle_step(wl, x):
+    """The oracle's eviction of one KV head (score, its uniform share of the layer budget,
+    selection, gather) plus one decode step of its G query heads."""
+    import numpy as np
+    import oracle as O
+    C = wl.n - wl.w
+    s, c = O.score_layer(x["q"], x["k"], x["v"], w=wl.w, pool=wl.pool, mode=wl.mode,
+                         group=wl.group, w_o=x.get("w_o"))
+    if wl.budget_kind == "layer":
+        Bl = wl.layer_budget_value()
+    else:
+        Bl = wl.total_budget_value() // wl.layers
+    Bp = (Bl - wl.w * wl.hkv) // wl.hkv
+    f, Bg = O.head_budgets(s, Bp + wl.w, wl.w, wl.alpha[0], wl.alpha[1])
+    crit = (wl.crit_alpha[0], wl.crit_alpha[1], wl.crit_eps) if wl.mode == "critical" else None
+    kept, cu, lens, Kf, Vf = O.compact_layer(x["k"], x["v"], s, Bg, wl.w, reserve=1, c=c,
+                                             crit=crit)
+    o, *_ = O.flat_decode(x["dq"], Kf, Vf, cu, lens, 1.0 / math.sqrt(wl.d), x["kn"], x["vn"])
+    return float(np.abs(o).sum())
+
+
+def sample_desc(wl):
+    return ("one KV head of one (sequence, layer) of %s (n=%d, %d query heads): window scoring, "
+            "its uniform share of the layer budget, selection, gather and one decode step; "
+            "tokens/s per layer = n / (Hkv * time)" % (wl.name, wl.n, wl.hq // wl.hkv))
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    from kv_cache_eviction_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    use_cuda = torch.cuda.is_available()
+    if use_cuda:
+        torch.cuda.set_device(local)
+    x = oracle_sample(wl, use_cuda)
+    for _ in range(args.warmup):
+        oracle_step(wl, x)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(wl, x)
+        times.append(time.perf_counter() - t0)
+    t = statistics.mean(times)
+    value = wl.n / (wl.hkv * t)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator)",
+        "config": {"workload": wl.name, "sample": "1 KV head of 1 (sequence, layer)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample_desc(wl)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def algorithmic_bytes(wl, B, L, head_budget_total_rows, decode_rows):
+    """Bytes each stage must move (see the roofline section of the design notes)."""
+    e = wl.elem_bytes
+    C = wl.n - wl.w
+    kv_bytes = B * L * wl.hkv * wl.n * wl.d * e
+    q_bytes = B * L * wl.hq * wl.w * wl.d * e
+    s_bytes = B * L * wl.hkv * C * 4
+    score = kv_bytes + q_bytes + s_bytes
+    if wl.mode in ("lava", "critical"):
+        score += kv_bytes
+    if wl.mode == "critical":
+        score += L * wl.hkv * wl.d * wl.model_dim * e + s_bytes
+    allocate = s_bytes
+    row = wl.d * e
+    compact = s_bytes + 4 * head_budget_total_rows * row + 4 * head_budget_total_rows
+    if wl.mode == "critical":
+        compact += s_bytes
+    decode = 2 * decode_rows * row + 2 * B * L * wl.hq * wl.d * e + 4 * B * L * wl.hkv * wl.d * e
+    return {"score": score, "allocate": allocate, "compact": compact, "decode": decode}
+
+
+def run_ours(args):
+    import torch
+    import kv_cache_eviction_gb300 as kv
+    from kv_cache_eviction_gb300 import workloads as W
+    import __graft_entry__
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    __graft_entry__.build()
+
+    wl = W.WORKLOADS[args.workload]
+    B, L = wl.batch, wl.layers
+    seqs = range(rank * B, (rank + 1) * B)
+    shape = kv.KvShape.from_workload(wl)
+    C = wl.n - wl.w
+    mode = {"ada": kv.KV_SCORE_ADA, "lava": kv.KV_SCORE_LAVA, "critical": kv.KV_SCORE_CRITICAL}[
+        wl.mode]
+    group = kv.KV_GROUP_MAX if wl.group == "max" else kv.KV_GROUP_MEAN
+    entropy = 1 if wl.budget_kind == "total" else 0
+
+    inp = W.make_batch(wl, device=dev, seqs=seqs)
+    budgets = wl.budgets().to(dev)
+    dec = W.make_decode_batch(wl, 0, inp["tau"], device=dev, seqs=seqs)
+    cap = wl.flat_capacity_rows()
+
+    def ws(op):
+        return torch.zeros(max(kv.kv_workspace_size(op, shape), 256), dtype=torch.uint8,
+                           device=dev)
+
+    w_s, w_a, w_c, w_d = (ws(kv.KV_OP_SCORE), ws(kv.KV_OP_ALLOCATE), ws(kv.KV_OP_COMPACT),
+                          ws(kv.KV_OP_DECODE))
+    scores = torch.empty(B, L, wl.hkv, C, dtype=torch.float32, device=dev)
+    crit = torch.empty_like(scores) if wl.mode == "critical" else None
+    lb = torch.empty(B, L, dtype=torch.int32, device=dev)
+    hb = torch.empty(B, L, wl.hkv, dtype=torch.int32, device=dev)
+    kept = torch.empty(cap, dtype=torch.int32, device=dev)
+    cu = torch.empty(B, L, wl.hkv + 1, dtype=torch.int64, device=dev)
+    lens = torch.empty(B, L, wl.hkv, dtype=torch.int32, device=dev)
+    kf = torch.empty(cap, wl.d, dtype=wl.torch_dtype, device=dev)
+    vf = torch.empty_like(kf)
+    out = torch.empty_like(dec["q"])
+    scale = 1.0 / math.sqrt(wl.d)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        kv.kv_score(shape, mode, group, inp["q_win"], inp["k"],
+                    inp["v"] if wl.mode != "ada" else None, inp["w_o"], wl.model_dim, scores,
+                    crit, w_s, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        kv.kv_allocate(shape, scores, budgets, entropy, wl.alpha[0], wl.alpha[1], lb, hb, w_a,
+                       stream)
+        if ev is not None:
+            ev[2].record(stream)
+        kv.kv_compact(shape, inp["k"], inp["v"], scores, crit, wl.crit_alpha[0],
+                      wl.crit_alpha[1], wl.crit_eps, hb, wl.reserve, kept, cu, lens, kf, vf, cap,
+                      w_c, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        kv.flat_decode_attn(shape, dec["q"], dec["k_new"], dec["v_new"], kf, vf, cu, lens, scale,
+                            out, w_d, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize(dev)
+    for w_ in (w_s, w_a, w_c, w_d):
+        code = kv.kv_check_device_status(w_, stream)
+        if code:
+            raise RuntimeError("device check %d during warm-up" % code)
+
+    input_bytes = 2 * inp["k"].numel() * inp["k"].element_size()
+    big_inputs = input_bytes > 2 * L2_BYTES
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local) if rank == 0 else None
+    launches0 = kv.kv_kernel_launches()
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for i in range(args.steps):
+        if not big_inputs and i > 0:
+            flush.zero_()
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    launches = kv.kv_kernel_launches() - launches0
+    clk = clocks.stop() if clocks is not None else None
+
+    stage_names = ["score", "allocate", "compact", "decode"]
+    stage_ms = {nm: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1])
+                                    for i in range(args.steps))
+                for j, nm in enumerate(stage_names)}
+    if big_inputs:
+        ms_per_step = t_start.elapsed_time(t_end) / args.steps
+    else:
+        ms_per_step = statistics.mean(evs[i][0].elapsed_time(evs[i][4])
+                                      for i in range(args.steps))
+    t_local = ms_per_step
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([t_local], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_local = float(tt.item())
+    value = world * B * wl.n * L / (t_local / 1e3)
+
+    for w_ in (w_s, w_a, w_c, w_d):
+        code = kv.kv_check_device_status(w_, stream)
+        if code:
+            raise RuntimeError("device check %d in the timed region" % code)
+
+    # -------------------- decode alone, L2 flushed before each step --------------------
+    hb_rows = int(hb.sum().item())
+    lens0 = int(lens.sum().item())          # includes the timed region's last append
+    nd = wl.decode_steps if args.decode_steps < 0 else args.decode_steps
+    nd = max(1, min(nd, wl.reserve - 1))
+    # rebuild the flat cache so every decode step has a reserve row
+    kv.kv_compact(shape, inp["k"], inp["v"], scores, crit, wl.crit_alpha[0], wl.crit_alpha[1],
+                  wl.crit_eps, hb, wl.reserve, kept, cu, lens, kf, vf, cap, w_c, stream)
+    lens0 = int(lens.sum().item())
+    dts, dbytes = [], []
+    for s_ in range(nd):
+        d_in = W.make_decode_batch(wl, 1 + s_, inp["tau"], device=dev, seqs=seqs)
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        kv.flat_decode_attn(shape, d_in["q"], d_in["k_new"], d_in["v_new"], kf, vf, cu, lens,
+                            scale, out, w_d, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        dts.append(e0.elapsed_time(e1))
+        rows = lens0 + (s_ + 1) * B * L * wl.hkv
+        dbytes.append(algorithmic_bytes(wl, B, L, hb_rows, rows)["decode"])
+    if kv.kv_check_device_status(w_d, stream):
+        raise RuntimeError("device check in decode")
+    peak, peak_kind = read_peaks()
+    dec_gbs = sum(dbytes) / (sum(dts) / 1e3) / 1e9
+
+    # -------------------- roofline of the dominant stage --------------------
+    ab = algorithmic_bytes(wl, B, L, hb_rows, lens0)
+    dom = max(("score", "allocate", "compact"), key=lambda k: stage_ms[k])
+    achieved = ab[dom] / (stage_ms[dom] / 1e3) / 1e9
+    roofline = {"kernel": "kv_score (window scoring)" if dom == "score" else dom,
+                "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                "algorithmic_bytes_per_launch": ab[dom]}
+
+    # -------------------- end to end through host buffers --------------------
+    e2e = None
+    if args.e2e_steps > 0:
+        host = {}
+        h2d = 0
+        for name in ("q_win", "k", "v", "w_o"):
+            t = inp.get(name)
+            if t is None or (name == "v" and wl.mode == "ada"):
+                continue
+            host[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            host[name].copy_(t)
+            h2d += t.numel() * t.element_size()
+        for name in ("q", "k_new", "v_new"):
+            host["dec_" + name] = torch.empty(dec[name].shape, dtype=dec[name].dtype,
+                                              pin_memory=True)
+            host["dec_" + name].copy_(dec[name])
+            h2d += dec[name].numel() * dec[name].element_size()
+        budgets_h = budgets.cpu().pin_memory()
+        h2d += budgets.numel() * budgets.element_size()
+        res = {"out": torch.empty(out.shape, dtype=out.dtype, pin_memory=True),
+               "hb": torch.empty(hb.shape, dtype=hb.dtype, pin_memory=True),
+               "lb": torch.empty(lb.shape, dtype=lb.dtype, pin_memory=True),
+               "lens": torch.empty(lens.shape, dtype=lens.dtype, pin_memory=True)}
+        d2h = sum(t.numel() * t.element_size() for t in res.values())
+        e2e_ms = []
+        for _ in range(args.e2e_steps):
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for name in ("q_win", "k", "v", "w_o"):
+                if name in host:
+                    inp[name].copy_(host[name], non_blocking=True)
+            for name in ("q", "k_new", "v_new"):
+                dec[name].copy_(host["dec_" + name], non_blocking=True)
+            budgets.copy_(budgets_h, non_blocking=True)
+            step()
+            res["out"].copy_(out, non_blocking=True)
+            res["hb"].copy_(hb, non_blocking=True)
+            res["lb"].copy_(lb, non_blocking=True)
+            res["lens"].copy_(lens, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            e2e_ms.append(e0.elapsed_time(e1))
+        t_e2e = statistics.mean(e2e_ms)
+        if world > 1:
+            import torch.distributed as dist
+            tt = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            t_e2e = float(tt.item())
+        e2e = {"value": world * B * wl.n * L / (t_e2e / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e,
+               "steps": args.e2e_steps}
+        del host
+
+    # -------------------- CPU oracle baseline --------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        x = oracle_sample(wl, True)
+        t0 = time.perf_counter()
+        oracle_step(wl, x)
+        t_cpu = time.perf_counter() - t0
+        cpu = {"value": wl.n / (wl.hkv * t_cpu), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": sample_desc(wl), "seconds": t_cpu}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+            if wl.dtype == "bf16" else "f32",
+            "data": "synthetic (seeded generator; shapes of the pages' workloads)",
+            "config": {
+                "workload": wl.name, "batch_per_gpu": B, "layers": L, "hq": wl.hq,
+                "hkv": wl.hkv, "d": wl.d, "n": wl.n, "w": wl.w, "pool": wl.pool,
+                "score": wl.mode, "group": wl.group,
+                "budget": ("total %d per sequence" % wl.total_budget_value()
+                           if wl.budget_kind == "total" else
+                           "%d per layer" % wl.layer_budget_value()),
+                "alpha": "%d/%d" % wl.alpha, "accumulate": "f32",
+                "parallelism": "replicas (independent sequences per GPU)" if world > 1 else
+                "1 GPU",
+                "l2": ("inputs larger than L2 (K+V %.1f GiB per step)" % (input_bytes / 2**30))
+                if big_inputs else "L2 flushed between steps",
+                "step": "kv_score + kv_allocate + kv_compact over all layers, then one "
+                        "flat_decode_attn step over all layers",
+            },
+            "stages_ms": stage_ms,
+            "decode_attn": {"value": dec_gbs, "unit": "GB/s", "frac": dec_gbs / peak,
+                            "peak": peak, "steps": nd, "ms_per_step": statistics.mean(dts),
+                            "bytes_per_step": statistics.mean(dbytes),
+                            "l2": "flushed before each step"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

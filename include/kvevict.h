@@ -202,6 +202,10 @@ KV_API kv_status flat_decode_attn(const kv_shape* shape, const void* q,
  * `info` (nullable) receives the first recorded check code. */
 KV_API kv_status kv_check_device_status(void* ws, void* stream, uint32_t* info);
 
+/* Number of kernels the library has launched in this process so far (all calls, all
+ * streams); the difference across a region counts that region's launches. */
+KV_API uint64_t kv_kernel_launches(void);
+
 /* Static description of a status code. */
 KV_API const char* kv_status_string(kv_status status);
 

@@ -19,7 +19,7 @@ __all__ = [
     "KV_SCORE_CRITICAL", "KV_GROUP_MEAN", "KV_GROUP_MAX", "KV_OP_SCORE", "KV_OP_ALLOCATE",
     "KV_OP_COMPACT", "KV_OP_DECODE", "KvShape", "KvError", "lib", "library_path",
     "kv_workspace_size", "kv_score", "kv_allocate", "kv_compact", "flat_decode_attn",
-    "kv_check_device_status", "kv_status_string",
+    "kv_check_device_status", "kv_status_string", "kv_kernel_launches",
 ]
 
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_UNSUPPORTED, KV_ERR_WORKSPACE = 0, 1, 2, 3
@@ -73,6 +73,7 @@ _SIGS = {
                                         _vp, _i64, _f32, _vp, _vp, _sz, _vp]),
     "kv_check_device_status": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(_u32)]),
     "kv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "kv_kernel_launches": (ctypes.c_uint64, []),
 }
 
 
@@ -175,3 +176,8 @@ def kv_check_device_status(ws, stream=None) -> int:
         return int(info.value)
     _check("kv_check_device_status", st)
     return 0
+
+
+def kv_kernel_launches() -> int:
+    """Kernels launched by the library in this process so far."""
+    return int(lib().kv_kernel_launches())

@@ -230,11 +230,13 @@ cudaError_t launch_allocate(const Shape& s, const float* scores, const int64_t* 
         scores, (int64_t)s.Hkv * C, p.nchunkE, part);
     layer_budgets<<<s.B, 32, 0, st>>>(part, p.nchunkE, s.L, s.Hkv, s.n, s.w, C, budget,
                                       layer_budget, bprime, scratch, hdr);
+    count_launches(2);
   }
   alloc_select<<<(unsigned)S, kSelThreads, 0, st>>>(scores, s.Hkv, C, s.w,
                                                     entropy_mode ? nullptr : budget,
                                                     entropy_mode ? bprime : nullptr, an, ad,
                                                     layer_budget, head_budget, hdr);
+  count_launches(1);
   return cudaGetLastError();
 }
 

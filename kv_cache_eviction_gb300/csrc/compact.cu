@@ -233,6 +233,7 @@ cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const f
   compact_gather<<<dim3(gx, (unsigned)H), kGatherThreads, 0, st>>>(
       (const char*)k, (const char*)v, kept, cu, lens, s.Hkv, s.n, row_bytes, cap, (char*)kf,
       (char*)vf);
+  count_launches(3);
   return cudaGetLastError();
 }
 

@@ -208,6 +208,7 @@ static cudaError_t launch_decode_t(const Shape& s, const T* q, void* kf, void* v
   decode_partial<T><<<dim3(p.splits, (unsigned)units), kThreads, sm, st>>>(
       q, (const T*)kf, (const T*)vf, cu, lens, s.Hkv, G, d, p.splits, cap, c2, part);
   decode_combine<T><<<(unsigned)units, 256, 0, st>>>(part, p.splits, s.Hkv, G, d, out);
+  count_launches(2);
   return cudaGetLastError();
 }
 
@@ -222,6 +223,7 @@ cudaError_t launch_decode(const Shape& s, const void* q, const void* kn, const v
     decode_append<<<(unsigned)cdiv(H, warps), warps * 32, 0, st>>>(
         (const char*)kn, (const char*)vn, (char*)kf, (char*)vf, cu, lens, H, s.Hkv,
         s.d * s.esize(), cap, hdr);
+    count_launches(1);
   }
   if (s.dtype == KV_BF16)
     return launch_decode_t<__nv_bfloat16>(s, (const __nv_bfloat16*)q, kf, vf, cu, lens, cap,

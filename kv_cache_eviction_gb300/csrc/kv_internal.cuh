@@ -61,5 +61,7 @@ cudaError_t launch_decode(const Shape& s, const void* q, const void* kn, const v
                           cudaStream_t st);
 
 int num_sms();
+// Adds n to the library's running count of kernel launches (kv_kernel_launches()).
+void count_launches(int n);
 
 }  // namespace kv

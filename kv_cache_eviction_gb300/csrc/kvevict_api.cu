@@ -1,5 +1,6 @@
 // C ABI of libkvevict: argument validation, workspace layout, dispatch.
 // Every check here runs on the host before anything is enqueued.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -19,6 +20,9 @@ int num_sms() {
   }
   return cached;
 }
+
+static std::atomic<unsigned long long> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -195,6 +199,8 @@ kv_status kv_check_device_status(void* ws, void* stream, uint32_t* info) {
   if (cudaStreamSynchronize(st) != cudaSuccess) return KV_ERR_CUDA;
   return KV_ERR_DEVICE_CHECK;
 }
+
+uint64_t kv_kernel_launches(void) { return (uint64_t)g_launches.load(); }
 
 const char* kv_status_string(kv_status status) {
   switch (status) {

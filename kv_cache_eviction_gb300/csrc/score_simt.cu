@@ -286,6 +286,7 @@ static cudaError_t launch_score_simt_t(const Shape& s, int mode, int group, cons
   score_pass1_simt<T><<<dim3(p.nchunk1, (unsigned)units), kThreads, sm1, st>>>(
       q_win, k, n, w, d, R, p.chunk1, p.nchunk1, c2, part);
   score_lse_combine<<<(unsigned)units, 128, 0, st>>>(part, p.nchunk1, R, lse2);
+  count_launches(2);
   const float* vb = nullptr;
   if (mode == KV_SCORE_LAVA) {
     e = cudaMemsetAsync(vbar, 0, (size_t)units * sizeof(float), st);
@@ -293,6 +294,7 @@ static cudaError_t launch_score_simt_t(const Shape& s, int mode, int group, cons
     const int rows = 256;
     vbar_simt<T><<<dim3((unsigned)cdiv(n, rows), (unsigned)units), kThreads, 0, st>>>(
         v, n, d, rows, reinterpret_cast<unsigned int*>(vbar));
+    count_launches(1);
     vb = vbar;
   }
   if (C > 0) {
@@ -304,6 +306,7 @@ static cudaError_t launch_score_simt_t(const Shape& s, int mode, int group, cons
     if (e != cudaSuccess) return e;
     score_pass2_simt<T><<<dim3(p.nchunk2, (unsigned)units), kThreads, sm2, st>>>(
         q_win, k, lse2, vb, n, w, d, G, s.pool, group == KV_GROUP_MAX, p.chunk2, c2, scores);
+    count_launches(1);
   }
   return cudaGetLastError();
 }
@@ -319,6 +322,7 @@ static cudaError_t launch_crit_simt_t(const Shape& s, const T* v, const T* w_o, 
   if (e != cudaSuccess) return e;
   crit_norm_simt<T><<<dim3((unsigned)cdiv(C, 32), (unsigned)s.units()), kThreads, sm, st>>>(
       v, w_o, s.L, s.Hkv, s.n, C, s.d, D, crit);
+  count_launches(1);
   return cudaGetLastError();
 }
 

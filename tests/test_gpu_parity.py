@@ -4,7 +4,8 @@ Bars: scores within 1e-4 relative (+1e-12 absolute); budgets, kept indices, offs
 the gathered rows bit-exact when the selection kernels are fed the oracle's scores
 (rounded to float32, the kernels' input type); end to end, a kept index may differ only
 at a near-tie (oracle score gap <= 1e-5 of the head's threshold); decode outputs within
-1e-2 max-abs for bf16 and 1e-4 for float32 (float32 accumulation on the GPU).
+1e-2 max-abs for bf16 and 1e-4 for float32 (float32 accumulation on the GPU); a bf16
+output additionally carries its own storage rounding, half an ulp = 2^-8 |o| at most.
 """
 import math
 
@@ -137,7 +138,10 @@ def decode_and_check(wl, shape, flat, oracle_flat, steps, tau, atol):
                 ref, Kn, Vn, ln = O.flat_decode(qn[b, l], Kf, Vf, cu_r, lens_r, scale,
                                                 kn[b, l], vn[b, l])
                 state[(b, l)] = [cu_r, ln, Kn, Vn]
-                err = np.abs(o[b, l] - ref).max()
+                # the output is stored in the ABI dtype: bf16 rounding adds up to half an ulp
+                # (2^-8 |ref|) on top of the accumulation tolerance
+                store = 2.0 ** -8 * np.abs(ref) if wl.dtype == "bf16" else 0.0
+                err = (np.abs(o[b, l] - ref) - store).max()
                 worst = max(worst, err)
                 assert err <= atol, (step, b, l, err)
     lens_gpu = flat["lens"].cpu().numpy()
@@ -147,6 +151,7 @@ def decode_and_check(wl, shape, flat, oracle_flat, steps, tau, atol):
 
 
 def full_check(wl, B=None, L=None, budgets=None, decode_steps=1, dec_atol=None):
+    assert decode_steps <= wl.reserve, "each decode append needs a reserve row"
     B = wl.batch if B is None else B
     L = wl.layers if L is None else L
     shape = kv.KvShape.from_workload(wl, batch=B, layers=L)
@@ -196,7 +201,7 @@ def full_check(wl, B=None, L=None, budgets=None, decode_steps=1, dec_atol=None):
 
 
 def test_tiny_mha_f32_full():
-    full_check(W.WORKLOADS["tiny_mha_f32"], decode_steps=2)
+    full_check(W.WORKLOADS["tiny_mha_f32"].with_(reserve=2), decode_steps=2)
 
 
 @pytest.mark.parametrize("frac", [0.2, 0.4, 0.8])
@@ -255,7 +260,7 @@ def test_full_budget_decode_equals_dense_attention():
         K2 = np.concatenate([np64(inp["k"][0, l]), np64(dec["k_new"][0, l])[:, None]], axis=1)
         V2 = np.concatenate([np64(inp["v"][0, l]), np64(dec["v_new"][0, l])[:, None]], axis=1)
         ref = O.dense_decode(np64(dec["q"][0, l]), K2, V2, 1 / math.sqrt(wl.d))
-        assert np.abs(o[0, l] - ref).max() <= 1e-2
+        assert (np.abs(o[0, l] - ref) - 2.0 ** -8 * np.abs(ref)).max() <= 1e-2
 
 
 def test_all_tied_scores_follow_total_order():
