@@ -197,6 +197,41 @@ KV_API kv_status flat_decode_attn(const kv_shape* shape, const void* q,
                            int64_t flat_capacity_rows, float softmax_scale, void* out,
                            void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * flat_decode_attn_noalloc -- the same decode step as flat_decode_attn, for callers that
+ * cannot allocate device memory.  (The method's pages have no counterpart: this is a
+ * deployment convenience of this library.)
+ *
+ * Some callers own no allocator at the point where they run a decode step: a serving loop
+ * whose device memory was planned once at start-up and may not grow, an engine plugin that
+ * is handed only its input and output buffers when it is enqueued, or code that issues work
+ * while a stream is being captured, where allocation calls are not allowed.  This entry
+ * point takes no workspace.  Its split-K scratch is a fixed array of
+ * KV_DECODE_NOALLOC_SCRATCH_BYTES (16 MiB) compiled into the library; every GPU that loads
+ * the library holds that array until the process exits.  Nothing here calls cudaMalloc,
+ * cudaFree or any allocating routine.
+ *
+ * Arguments, results and validation are those of flat_decode_attn without `ws`/`ws_bytes`.
+ * - A shape whose decode needs more scratch than the fixed array (kv_workspace_size
+ *   (KV_OP_DECODE, shape) > KV_DECODE_NOALLOC_SCRATCH_BYTES) is rejected with
+ *   KV_ERR_WORKSPACE before anything is enqueued.
+ * - The first call on each device looks up that device's copy of the array (with the
+ *   device current) and caches it; make that first call before any stream capture.
+ * - Every call on a device shares the one array and leaves its last contents there.
+ *   Calls whose kernels overlap on the GPU (different streams without ordering between
+ *   them) race on it: order them on one stream, or use flat_decode_attn with separate
+ *   workspaces.
+ * - Device-side checks (an append with no reserve row left) behave as in flat_decode_attn
+ *   (the append is skipped and lens is not advanced) but are not reported: there is no
+ *   workspace for kv_check_device_status to read.
+ */
+#define KV_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
+KV_API kv_status flat_decode_attn_noalloc(const kv_shape* shape, const void* q,
+                                          const void* k_new, const void* v_new,
+                                          void* k_flat, void* v_flat, const int64_t* cu_off,
+                                          int32_t* lens, int64_t flat_capacity_rows,
+                                          float softmax_scale, void* out, void* stream);
+
 /* Synchronises `stream`, reads the device error word of `ws` and clears it.
  * Returns KV_OK or KV_ERR_DEVICE_CHECK (KV_ERR_CUDA if the copy fails).
  * `info` (nullable) receives the first recorded check code. */

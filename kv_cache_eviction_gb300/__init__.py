@@ -20,6 +20,7 @@ __all__ = [
     "KV_OP_COMPACT", "KV_OP_DECODE", "KvShape", "KvError", "lib", "library_path",
     "kv_workspace_size", "kv_score", "kv_allocate", "kv_compact", "flat_decode_attn",
     "kv_check_device_status", "kv_status_string", "kv_kernel_launches",
+    "flat_decode_attn_noalloc",
 ]
 
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_UNSUPPORTED, KV_ERR_WORKSPACE = 0, 1, 2, 3
@@ -74,6 +75,8 @@ _SIGS = {
     "kv_check_device_status": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(_u32)]),
     "kv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kv_kernel_launches": (ctypes.c_uint64, []),
+    "flat_decode_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(KvShape), _vp, _vp, _vp, _vp, _vp,
+                                                _vp, _vp, _i64, _f32, _vp, _vp]),
 }
 
 
@@ -166,6 +169,17 @@ def flat_decode_attn(shape: KvShape, q, k_new, v_new, k_flat, v_flat, cu_off, le
                                 _ptr(k_flat), _ptr(v_flat), _ptr(cu_off), _ptr(lens), cap,
                                 softmax_scale, _ptr(out), _ptr(ws), _nbytes(ws), _stream(stream))
     _check("flat_decode_attn", st)
+
+
+def flat_decode_attn_noalloc(shape: KvShape, q, k_new, v_new, k_flat, v_flat, cu_off, lens,
+                             softmax_scale: float, out, stream=None,
+                             flat_capacity_rows=None) -> None:
+    """flat_decode_attn without a workspace: the library's fixed device scratch is used."""
+    cap = k_flat.shape[0] if flat_capacity_rows is None else flat_capacity_rows
+    st = lib().flat_decode_attn_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                        _ptr(k_flat), _ptr(v_flat), _ptr(cu_off), _ptr(lens), cap,
+                                        softmax_scale, _ptr(out), _stream(stream))
+    _check("flat_decode_attn_noalloc", st)
 
 
 def kv_check_device_status(ws, stream=None) -> int:

@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "kv_internal.cuh"
 
@@ -51,6 +52,31 @@ static bool shape_supported(const Shape& s) {
 }
 
 static kv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KV_OK : KV_ERR_CUDA; }
+
+// Scratch of flat_decode_attn_noalloc: one fixed array per device, never allocated at run
+// time.  Host code must not pass the symbol itself to a kernel (on the host it names a
+// host-side stand-in); the device address comes from cudaGetSymbolAddress, looked up once
+// per device with that device current.
+static __device__ __align__(256) char g_decode_noalloc_scratch[KV_DECODE_NOALLOC_SCRATCH_BYTES];
+
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_ptr[256] = {};
+
+static cudaError_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
 
 }  // namespace kv
 
@@ -198,6 +224,21 @@ kv_status kv_check_device_status(void* ws, void* stream, uint32_t* info) {
   if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return KV_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return KV_ERR_CUDA;
   return KV_ERR_DEVICE_CHECK;
+}
+
+kv_status flat_decode_attn_noalloc(const kv_shape* shape, const void* q, const void* k_new,
+                                   const void* v_new, void* k_flat, void* v_flat,
+                                   const int64_t* cu_off, int32_t* lens,
+                                   int64_t flat_capacity_rows, float softmax_scale, void* out,
+                                   void* stream) {
+  void* scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return KV_ERR_CUDA;
+  // The split-K partials are fully written before they are read, so nothing in the shared
+  // scratch has to start at zero.  A decode that needs more than the fixed array gets
+  // KV_ERR_WORKSPACE from the size check below, before anything is enqueued.
+  return flat_decode_attn(shape, q, k_new, v_new, k_flat, v_flat, cu_off, lens,
+                          flat_capacity_rows, softmax_scale, out, scratch,
+                          (size_t)KV_DECODE_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 uint64_t kv_kernel_launches(void) { return (uint64_t)g_launches.load(); }
