@@ -262,10 +262,9 @@ ScorePlan score_plan(const Shape& s, int mode) {
   p.off_vbar = off;
   off += align_up((size_t)units * sizeof(float), 256);
   p.off_end = off;
-  if (p.path == 1) {
-    const size_t tc = score_tc_ws(s, mode);
-    if (tc > p.off_end) p.off_end = tc;
-  }
+  // the workspace covers either path, whichever runs
+  const size_t tc = score_tc_ws(s, mode);
+  if (tc > p.off_end) p.off_end = tc;
   return p;
 }
 

@@ -1,16 +1,640 @@
-// tcgen05 (5th-generation tensor core) path of the window scoring and of the
-// CriticalKV V*W_O row norm.  Placeholder until the kernels land: reports
-// "not supported" so the CUDA-core path runs.
+// Observation-window scoring on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Ada-KV Algorithm 2 (scoring steps) with the LAVa Definition 1 factor and GQA group
+// reduction, for bf16, d = 128 and G*w = 128 window rows per KV head (w in {16, 32, 64}).
+//
+// Work decomposition.  A (sequence, layer, KV head) "unit" has n keys in T_u tiles of 128.
+// The grid (one CTA per SM, cooperative launch so all CTAs are resident) is split into NG
+// groups of P_g CTAs; group g handles units g, g+NG, ...; inside a group CTA r owns the
+// same contiguous tile range [t0, t1) of every unit.  For each unit a CTA runs
+//   P1: S = Q_win K^T on the tensor core (M = 128 window rows, N = 128 keys), online row
+//       max / sum of exp2 over its keys -> one (max, sum) partial per row; the CTA that
+//       completes the unit's last partial combines them into the row log-sum-exp and
+//       publishes it (release flag);
+//   P2: S^T = K Q_win^T (M = 128 keys, N = 128 window rows): each epilogue thread owns one
+//       key and forms a[q, j] = (1/w) sum_t exp2(z2 - lse2[q,t]); then max-pool, group
+//       mean/max and the LAVa V-bar factor.
+// Items are ordered P1(u0), P1(u1), P2(u0), P1(u2), P2(u1), ... so a CTA's P2 of unit u
+// re-reads its K tiles from L2 after one unit of other traffic, and rarely waits for the
+// flag.  Keys whose pooling window crosses a CTA's range boundary are finished by
+// score_tc_fixup from per-range halo copies of the window means.
+//
+// Roles (384 threads): warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM
+// allocator, warps 4..11 = epilogue (TMEM lane quadrant = warp % 4, column half =
+// (warp - 4) / 4).  Every wait is bounded; on a timeout the CTA records DEV_WAIT_TIMEOUT,
+// unwinds, waits (bounded) for its copies and MMAs in flight and frees its TMEM.
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
 #include "kv_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace kv {
+namespace {
 
-bool score_tc_supported(const Shape&) { return false; }
-size_t score_tc_ws(const Shape&, int) { return 0; }
-cudaError_t launch_score_tc(const Shape&, int, int, const void*, const void*, const void*, float*,
-                            char*, cudaStream_t) {
-  return cudaErrorNotSupported;
+using namespace ptx;
+
+constexpr int kStages = 3;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = 32 * (4 + kEpiWarps);
+constexpr uint32_t kBoxBytes = 128 * 128;          // 128 rows x 64 bf16 (one 128-byte row each)
+constexpr uint32_t kTileBytes = 2 * kBoxBytes;     // 128 rows x 128 bf16
+constexpr int kAFloats = 8192;                     // window means of one range, all G heads
+constexpr uint32_t kTmemCols = 256;                // two 128-column fp32 accumulators
+constexpr int kMaxR = 15;                          // pool / 2
+
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = 2 * kTileBytes;
+constexpr uint32_t kOffA = kOffK + kStages * kTileBytes;
+constexpr uint32_t kOffLse = kOffA + kAFloats * 4;
+constexpr uint32_t kOffPart = kOffLse + 128 * 4;
+constexpr uint32_t kOffTail = kOffPart + 2 * 128 * 8;
+
+struct __align__(8) Tail {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t qfull[2], qempty[2];
+  uint64_t tfull[2], tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int last_flag;
+};
+constexpr uint32_t kSmemBytes = kOffTail + sizeof(Tail) + 1024;
+
+struct TcParams {
+  int n, w, C, G, r, group_max;
+  int64_t units;
+  int Pg, NG, Tu, Tc;
+  float c2, inv_w;
+  const float* vbar;
+  float2* partial;   // [units][Pg][128]
+  float* lse;        // [units][128] (log2 domain)
+  uint32_t* done1;   // [units]
+  uint32_t* ready;   // [units]
+  float* halo;       // [units][Pg][G][4r]
+  float* scores;     // [units][C]
+  WsHeader* hdr;
+};
+
+__device__ __forceinline__ void item_of(int64_t i, int64_t m, int& kind, int64_t& k) {
+  // P1(0), P1(1), P2(0), P1(2), P2(1), ..., P1(m-1), P2(m-2), P2(m-1); kind 1 = P1, 2 = P2
+  if (i == 0) { kind = 1; k = 0; return; }
+  if (i == 2 * m - 1) { kind = 2; k = m - 1; return; }
+  if (i & 1) { kind = 1; k = (i + 1) >> 1; } else { kind = 2; k = (i >> 1) - 1; }
 }
+
+template <int LW>
+__global__ void __launch_bounds__(kThreads, 1)
+score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Tail* tl = reinterpret_cast<Tail*>(smem + kOffTail);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int group = blockIdx.x / p.Pg, rank = blockIdx.x % p.Pg;
+  const int t0 = (int)(((int64_t)rank * p.Tu) / p.Pg);
+  const int t1 = (int)(((int64_t)(rank + 1) * p.Tu) / p.Pg);
+  const int t1c = t1 < p.Tc ? t1 : p.Tc;
+  const int64_t m = group < p.units ? (p.units - 1 - group) / p.NG + 1 : 0;
+  const int64_t n_items = 2 * m;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) { mbar_init(&tl->full[s], 1); mbar_init(&tl->empty[s], 1); }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tl->qfull[b], 1);
+      mbar_init(&tl->qempty[b], 1);
+      mbar_init(&tl->tfull[b], 1);
+      mbar_init(&tl->tempty[b], kEpiWarps);
+    }
+    mbar_init(&tl->drain, 1);
+    tl->abort_flag = 0;
+    tl->last_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&tl->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&qmap);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tl->tmem_base;
+  volatile int* abort_flag = &tl->abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      uint32_t g = 0, qi = 0;
+      uint32_t kissued[kStages] = {}, qissued[2] = {};   // 1 + use index of the last copy
+      bool ok = true;
+      for (int64_t i = 0; i < n_items && ok; ++i) {
+        int kind;
+        int64_t k;
+        item_of(i, m, kind, k);
+        const int64_t u = group + k * p.NG;
+        const int te = kind == 1 ? t1 : t1c;
+        if (t0 >= te) continue;
+        const int qb = qi & 1;
+        if (!mbar_wait(&tl->qempty[qb], ((qi >> 1) & 1) ^ 1) || *abort_flag) { ok = false; break; }
+        qissued[qb] = (qi >> 1) + 1;
+        mbar_arrive_expect_tx(&tl->qfull[qb], kTileBytes);
+        tma_load_3d(smem + kOffQ + qb * kTileBytes, &qmap, &tl->qfull[qb], 0, 0, (int)u);
+        tma_load_3d(smem + kOffQ + qb * kTileBytes + kBoxBytes, &qmap, &tl->qfull[qb], 64, 0,
+                    (int)u);
+        for (int t = t0; t < te; ++t, ++g) {
+          const int s = g % kStages;
+          if (!mbar_wait(&tl->empty[s], ((g / kStages) & 1) ^ 1) || *abort_flag) { ok = false; break; }
+          kissued[s] = g / kStages + 1;
+          mbar_arrive_expect_tx(&tl->full[s], kTileBytes);
+          tma_load_3d(smem + kOffK + s * kTileBytes, &kmap, &tl->full[s], 0, t * 128, (int)u);
+          tma_load_3d(smem + kOffK + s * kTileBytes + kBoxBytes, &kmap, &tl->full[s], 64, t * 128,
+                      (int)u);
+        }
+        ++qi;
+      }
+      if (!ok) {
+        raise_dev(p.hdr, DEV_WAIT_TIMEOUT, 1);
+        *abort_flag = 1;
+        // let the copies already issued land before the CTA exits
+        for (int s = 0; s < kStages; ++s)
+          if (kissued[s]) mbar_wait(&tl->full[s], (kissued[s] - 1) & 1, 20000000ull);
+        for (int b = 0; b < 2; ++b)
+          if (qissued[b]) mbar_wait(&tl->qfull[b], (qissued[b] - 1) & 1, 20000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer --------------------------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, 128);
+      uint32_t g = 0, qi = 0;
+      bool ok = true;
+      for (int64_t i = 0; i < n_items && ok; ++i) {
+        int kind;
+        int64_t k;
+        item_of(i, m, kind, k);
+        const int te = kind == 1 ? t1 : t1c;
+        if (t0 >= te) continue;
+        const int qb = qi & 1;
+        if (!mbar_wait(&tl->qfull[qb], (qi >> 1) & 1) || *abort_flag) { ok = false; break; }
+        const uint32_t qaddr = smem_u32(smem + kOffQ + qb * kTileBytes);
+        for (int t = t0; t < te; ++t, ++g) {
+          const int s = g % kStages, tb = g & 1;
+          if (!mbar_wait(&tl->full[s], (g / kStages) & 1) ||
+              !mbar_wait(&tl->tempty[tb], ((g >> 1) & 1) ^ 1) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kaddr = smem_u32(smem + kOffK + s * kTileBytes);
+          const uint32_t d = tmem + tb * 128;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            const uint64_t qd = sdesc_sw128(qaddr + off), kd = sdesc_sw128(kaddr + off);
+            if (kind == 1) mma_bf16(d, qd, kd, idesc, kk > 0 ? 1u : 0u);
+            else mma_bf16(d, kd, qd, idesc, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&tl->empty[s]);
+          mma_commit(&tl->tfull[tb]);
+        }
+        if (!ok) break;
+        mma_commit(&tl->qempty[qb]);
+        ++qi;
+      }
+      if (!ok) {
+        raise_dev(p.hdr, DEV_WAIT_TIMEOUT, 2);
+        *abort_flag = 1;
+      }
+      // every MMA issued has completed before TMEM is freed
+      mma_commit(&tl->drain);
+      mbar_wait(&tl->drain, 0, 20000000ull);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------ epilogue ----------------------------------
+    constexpr int W = 1 << LW;
+    constexpr int QH = 64 >> LW;                   // query heads per column half
+    const int quad = warp & 3, half = (warp - 4) >> 2, et = threadIdx.x - 128;
+    const int row = quad * 32 + lane;              // P1: window row; P2: key within the tile
+    float* A = reinterpret_cast<float*>(smem + kOffA);
+    float* nlse = reinterpret_cast<float*>(smem + kOffLse);
+    float2* part_s = reinterpret_cast<float2*>(smem + kOffPart);
+    const int RK = (t1 - t0) * 128;                // keys of this CTA's range (A stride)
+    const int r = p.r, C = p.C, G = p.G;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int64_t i = 0; i < n_items && ok; ++i) {
+      int kind;
+      int64_t k;
+      item_of(i, m, kind, k);
+      const int64_t u = group + k * p.NG;
+      const int te = kind == 1 ? t1 : t1c;
+      if (t0 >= te) continue;
+      if (kind == 2) {
+        if (et == 0) {
+          const uint64_t tw = globaltimer();
+          while (ld_acquire_u32(&p.ready[u]) == 0u) {
+            if (*abort_flag || globaltimer() - tw > 2000000000ull) {
+              raise_dev(p.hdr, DEV_WAIT_TIMEOUT, 3);
+              *abort_flag = 1;
+              break;
+            }
+            __nanosleep(128);
+          }
+        }
+        named_bar(1, kEpiThreads);
+        if (*abort_flag) { ok = false; break; }
+        if (et < 128) nlse[et] = -__ldcg(&p.lse[u * 128 + et]);
+        named_bar(1, kEpiThreads);
+      }
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int t = t0; t < te; ++t, ++g) {
+        const int tb = g & 1;
+        if (!mbar_wait(&tl->tfull[tb], (g >> 1) & 1) || *abort_flag) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + tb * 128 + half * 64;
+        uint32_t ra[32], rb[32];
+        tmem_ld32(taddr, ra);
+        tmem_ld32(taddr + 32, rb);
+        tmem_ld_wait(ra);
+        tmem_ld_wait(rb);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tl->tempty[tb]);
+        if (kind == 1) {
+          const int key0 = t * 128 + half * 64;
+          const int limit = p.n - W + (row & (W - 1));   // last key window row t can see
+          float v[64];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            v[c] = __uint_as_float(ra[c]) * p.c2;
+            v[32 + c] = __uint_as_float(rb[c]) * p.c2;
+          }
+          if (key0 + 63 > p.n - W) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (key0 + c > limit) v[c] = -INFINITY;
+          }
+          float mx = v[0];
+#pragma unroll
+          for (int c = 1; c < 64; ++c) mx = fmaxf(mx, v[c]);
+          const float mn = fmaxf(m_run, mx);
+          if (mn != -INFINITY) {
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+              s0 += ex2(v[c] - mn);
+              s1 += ex2(v[c + 1] - mn);
+            }
+            l_run = l_run * ex2(m_run - mn) + (s0 + s1);
+            m_run = mn;
+          }
+        } else {
+          float acc[QH];
+#pragma unroll
+          for (int q = 0; q < QH; ++q) acc[q] = 0.f;
+          const float* nl = nlse + half * 64;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            acc[c >> LW] += ex2(fmaf(__uint_as_float(ra[c]), p.c2, nl[c]));
+            acc[(32 + c) >> LW] += ex2(fmaf(__uint_as_float(rb[c]), p.c2, nl[32 + c]));
+          }
+          const int kl = (t - t0) * 128 + row;
+          const int q0 = (half * 64) >> LW;
+#pragma unroll
+          for (int q = 0; q < QH; ++q) A[(q0 + q) * RK + kl] = acc[q] * p.inv_w;
+        }
+      }
+      if (!ok) break;
+      if (kind == 1) {
+        part_s[half * 128 + row] = make_float2(m_run, l_run);
+        named_bar(1, kEpiThreads);
+        if (half == 0) {
+          const float2 a = part_s[row], b = part_s[128 + row];
+          const float M = fmaxf(a.x, b.x);
+          float L = 0.f;
+          if (a.x != -INFINITY) L += a.y * ex2(a.x - M);
+          if (b.x != -INFINITY) L += b.y * ex2(b.x - M);
+          p.partial[(u * p.Pg + rank) * 128 + row] = make_float2(M, L);
+        }
+        __threadfence();
+        named_bar(1, kEpiThreads);
+        if (et == 0) tl->last_flag = (atomicAdd(&p.done1[u], 1u) == (uint32_t)(p.Pg - 1)) ? 1 : 0;
+        named_bar(1, kEpiThreads);
+        if (tl->last_flag) {
+          __threadfence();
+          if (et < 128) {
+            const float2* P = p.partial + u * p.Pg * 128 + et;
+            float M = -INFINITY;
+            for (int q = 0; q < p.Pg; ++q) M = fmaxf(M, __ldcg(P + q * 128).x);
+            float S = 0.f;
+            for (int q = 0; q < p.Pg; ++q) {
+              const float2 v = __ldcg(P + q * 128);
+              if (v.x != -INFINITY) S += v.y * ex2(v.x - M);
+            }
+            p.lse[u * 128 + et] = M + log2f(S);
+          }
+          __threadfence();
+          named_bar(1, kEpiThreads);
+          if (et == 0) st_release_u32(&p.ready[u], 1u);
+        }
+      } else {
+        named_bar(1, kEpiThreads);
+        const int sK = t0 * 128;
+        const int eK = min(te * 128, C);
+        const float vb = p.vbar ? p.vbar[u] : 1.0f;
+        float* H = p.halo + (u * p.Pg + rank) * (int64_t)G * 4 * r;
+        for (int j = sK + et; j < eK; j += kEpiThreads) {
+          const int lo = max(0, j - r), hi = min(C - 1, j + r);
+          if (lo >= sK && hi < eK) {
+            float gv = p.group_max ? -INFINITY : 0.f;
+            for (int q = 0; q < G; ++q) {
+              const float* Aq = A + q * RK - sK;
+              float pm = -INFINITY;
+              for (int jj = lo; jj <= hi; ++jj) pm = fmaxf(pm, Aq[jj]);
+              gv = p.group_max ? fmaxf(gv, pm) : gv + pm;
+            }
+            if (!p.group_max) gv = gv / (float)G;
+            if (p.vbar) gv = gv * vb;
+            p.scores[u * C + j] = gv;
+          }
+          if (r > 0) {
+            if (j < sK + 2 * r)
+              for (int q = 0; q < G; ++q) H[q * 4 * r + (j - sK)] = A[q * RK + (j - sK)];
+            if (j >= eK - 2 * r)
+              for (int q = 0; q < G; ++q)
+                H[q * 4 * r + 2 * r + (j - (eK - 2 * r))] = A[q * RK + (j - sK)];
+          }
+        }
+        named_bar(1, kEpiThreads);
+      }
+    }
+    if (!ok) {
+      raise_dev(p.hdr, DEV_WAIT_TIMEOUT, 4);
+      *abort_flag = 1;
+    }
+  }
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Keys within pool/2 of a range boundary: pooled from the halo copies of both ranges.
+__global__ void score_tc_fixup(const float* __restrict__ halo, const float* __restrict__ vbar,
+                               int Pg, int Tu, int C, int G, int r, int group_max,
+                               float* __restrict__ scores) {
+  const int64_t u = blockIdx.x;
+  const int R4 = 4 * r;
+  for (int idx = threadIdx.x; idx < (Pg - 1) * 2 * r; idx += blockDim.x) {
+    const int bnd = idx / (2 * r) + 1;
+    const int b = (int)(((int64_t)bnd * Tu) / Pg) * 128;
+    if (b >= C) continue;
+    const int j = b - r + idx % (2 * r);
+    if (j < 0 || j >= C) continue;
+    const int lo = max(0, j - r), hi = min(C - 1, j + r);
+    const float* Hl = halo + (u * Pg + bnd - 1) * (int64_t)G * R4;
+    const float* Hr = halo + (u * Pg + bnd) * (int64_t)G * R4;
+    float gv = group_max ? -INFINITY : 0.f;
+    for (int q = 0; q < G; ++q) {
+      float pm = -INFINITY;
+      for (int jj = lo; jj <= hi; ++jj) {
+        const float x = jj < b ? Hl[q * R4 + 2 * r + (jj - (b - 2 * r))] : Hr[q * R4 + (jj - b)];
+        pm = fmaxf(pm, x);
+      }
+      gv = group_max ? fmaxf(gv, pm) : gv + pm;
+    }
+    if (!group_max) gv = gv / (float)G;
+    if (vbar) gv = gv * vbar[u];
+    scores[u * C + j] = gv;
+  }
+}
+
+// vbar[unit] = max over rows of ||V[row]||_1 for bf16 rows of 128 (16 lanes x 16 bytes).
+__global__ void __launch_bounds__(256)
+vbar_vec_bf16(const uint4* __restrict__ v, int n, int rows_per_cta, unsigned int* __restrict__ bits) {
+  const int64_t unit = blockIdx.y;
+  const int sub = threadIdx.x & 15, rr = threadIdx.x >> 4;
+  const int r0 = blockIdx.x * rows_per_cta, r1 = min(n, r0 + rows_per_cta);
+  const uint4* V = v + unit * (int64_t)n * 16;
+  float mx = 0.f;
+#pragma unroll 4
+  for (int row = r0 + rr; row < r1; row += 16) {
+    const uint4 x = __ldcs(V + (int64_t)row * 16 + sub);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      s += fabsf(f.x) + fabsf(f.y);
+    }
+    s += __shfl_xor_sync(0xffffffffu, s, 8);
+    s += __shfl_xor_sync(0xffffffffu, s, 4);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    mx = fmaxf(mx, s);
+  }
+  mx = warp_max(mx);
+  __shared__ float wm[8];
+  if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = wm[0];
+    for (int i = 1; i < 8; ++i) m = fmaxf(m, wm[i]);
+    atomicMax(&bits[unit], __float_as_uint(m));
+  }
+}
+
+// --------------------------------- host side ----------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t units) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {128, rows, units};
+  const cuuint64_t strides[2] = {128 * 2, rows * 128 * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int path_override() {
+  const char* e = std::getenv("KVEVICT_SCORE_PATH");
+  if (e == nullptr) return 0;
+  if (std::strcmp(e, "simt") == 0) return 1;
+  if (std::strcmp(e, "tc") == 0) return 2;
+  return 0;
+}
+
+struct TcPlan {
+  int NG, Pg, Tu, Tc, grid;
+  size_t off_partial, off_lse, off_flags, off_halo, off_vbar, off_end;
+};
+
+bool tc_plan(const Shape& s, TcPlan* out) {
+  if (s.dtype != KV_BF16 || s.d != 128 || s.R() != 128) return false;
+  if (!(s.w == 16 || s.w == 32 || s.w == 64)) return false;
+  if (s.C() < 1 || s.pool / 2 > kMaxR) return false;
+  TcPlan p{};
+  const int P = num_sms();
+  p.Tu = (int)cdiv(s.n, 128);
+  p.Tc = (int)cdiv(s.C(), 128);
+  const int64_t units = s.units();
+  const int max_tiles = kAFloats / (s.G() * 128);
+  // groups: each keeps about two units of K in L2 (about 64 MiB per group in total)
+  const double unit_bytes = (double)s.n * 128 * 2;
+  int NG = (int)(64.0 * 1024 * 1024 / (2.0 * unit_bytes));
+  if (NG < 1) NG = 1;
+  if (NG > P) NG = P;
+  if (NG > units) NG = (int)units;
+  int Pg = P / NG;
+  if (Pg > p.Tu) Pg = p.Tu;
+  if (cdiv(p.Tu, Pg) > max_tiles) {
+    // ranges too long for the window-mean buffer: use more CTAs per unit
+    Pg = (int)cdiv(p.Tu, max_tiles);
+    if (Pg > P) return false;
+    NG = P / Pg;
+    if (NG > units) NG = (int)units;
+  }
+  p.NG = NG;
+  p.Pg = Pg;
+  p.grid = NG * Pg;
+  const int r = s.pool / 2;
+  size_t off = kWsHeader;
+  p.off_partial = off;
+  off += align_up((size_t)units * Pg * 128 * sizeof(float2), 256);
+  p.off_lse = off;
+  off += align_up((size_t)units * 128 * sizeof(float), 256);
+  p.off_flags = off;
+  off += align_up((size_t)units * 2 * sizeof(uint32_t), 256);
+  p.off_halo = off;
+  off += align_up((size_t)units * Pg * s.G() * 4 * r * sizeof(float) + 4, 256);
+  p.off_vbar = off;
+  off += align_up((size_t)units * sizeof(float), 256);
+  p.off_end = off;
+  *out = p;
+  return true;
+}
+
+template <int LW>
+cudaError_t launch_main(const CUtensorMap& km, const CUtensorMap& qm, const TcParams& prm,
+                        int grid, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<LW>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, score_tc_kernel<LW>, km, qm, prm);
+}
+
+}  // namespace
+
+bool score_tc_supported(const Shape& s) {
+  const int ov = path_override();
+  if (ov == 1) return false;
+  TcPlan p;
+  if (!tc_plan(s, &p)) return false;
+  return encode_fn() != nullptr;
+}
+
+size_t score_tc_ws(const Shape& s, int) {
+  TcPlan p;
+  if (!tc_plan(s, &p)) return 0;
+  return p.off_end;
+}
+
+cudaError_t launch_score_tc(const Shape& s, int mode, int group, const void* q_win,
+                            const void* k, const void* v, float* scores, char* ws,
+                            cudaStream_t st) {
+  TcPlan tp;
+  if (!tc_plan(s, &tp)) return cudaErrorNotSupported;
+  const int64_t units = s.units();
+  CUtensorMap km, qm;
+  if (!make_map(&km, k, (uint64_t)s.n, (uint64_t)units) ||
+      !make_map(&qm, q_win, 128, (uint64_t)units))
+    return cudaErrorInvalidValue;
+  TcParams prm{};
+  prm.n = s.n;
+  prm.w = s.w;
+  prm.C = s.C();
+  prm.G = s.G();
+  prm.r = s.pool / 2;
+  prm.group_max = group == KV_GROUP_MAX;
+  prm.units = units;
+  prm.Pg = tp.Pg;
+  prm.NG = tp.NG;
+  prm.Tu = tp.Tu;
+  prm.Tc = tp.Tc;
+  prm.c2 = (1.0f / sqrtf((float)s.d)) * 1.4426950408889634f;
+  prm.inv_w = 1.0f / (float)s.w;
+  prm.partial = reinterpret_cast<float2*>(ws + tp.off_partial);
+  prm.lse = reinterpret_cast<float*>(ws + tp.off_lse);
+  prm.done1 = reinterpret_cast<uint32_t*>(ws + tp.off_flags);
+  prm.ready = prm.done1 + units;
+  prm.halo = reinterpret_cast<float*>(ws + tp.off_halo);
+  prm.scores = scores;
+  prm.hdr = reinterpret_cast<WsHeader*>(ws);
+  cudaError_t e = cudaMemsetAsync(prm.done1, 0, (size_t)units * 2 * sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  if (mode == KV_SCORE_LAVA) {
+    float* vbar = reinterpret_cast<float*>(ws + tp.off_vbar);
+    e = cudaMemsetAsync(vbar, 0, (size_t)units * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+    const int rows = 1024;
+    vbar_vec_bf16<<<dim3((unsigned)cdiv(s.n, rows), (unsigned)units), 256, 0, st>>>(
+        reinterpret_cast<const uint4*>(v), s.n, rows, reinterpret_cast<unsigned int*>(vbar));
+    count_launches(1);
+    prm.vbar = vbar;
+  }
+  switch (s.w) {
+    case 16: e = launch_main<4>(km, qm, prm, tp.grid, st); break;
+    case 32: e = launch_main<5>(km, qm, prm, tp.grid, st); break;
+    default: e = launch_main<6>(km, qm, prm, tp.grid, st); break;
+  }
+  if (e != cudaSuccess) return e;
+  count_launches(1);
+  if (prm.r > 0 && tp.Pg > 1) {
+    score_tc_fixup<<<(unsigned)units, 64, 0, st>>>(prm.halo, prm.vbar, tp.Pg, tp.Tu, prm.C,
+                                                   prm.G, prm.r, prm.group_max, scores);
+    count_launches(1);
+  }
+  return cudaGetLastError();
+}
+
+// CriticalKV V*W_O on tcgen05: not built yet, the CUDA-core kernel runs.
 bool crit_tc_supported(const Shape&, int) { return false; }
 cudaError_t launch_crit_tc(const Shape&, const void*, const void*, int, float*, cudaStream_t) {
   return cudaErrorNotSupported;
