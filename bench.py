@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the workload's layer count (profiling cases)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--decode-steps", type=int, default=-1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -124,6 +126,8 @@ def run_reference(args):
     import torch
     from kv_cache_eviction_gb300 import workloads as W
     wl = W.WORKLOADS[args.workload]
+    if args.layers > 0:
+        wl = wl.with_(layers=args.layers)
     use_cuda = torch.cuda.is_available()
     if use_cuda:
         torch.cuda.set_device(local)
@@ -240,6 +244,8 @@ def run_ours(args):
     __graft_entry__.build()
 
     wl = W.WORKLOADS[args.workload]
+    if args.layers > 0:
+        wl = wl.with_(layers=args.layers)
     B, L = wl.batch, wl.layers
     seqs = range(rank * B, (rank + 1) * B)
     shape = kv.KvShape.from_workload(wl)

@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/kvevict.h"
+#include "kvevict.h"
 
 namespace kv {
 

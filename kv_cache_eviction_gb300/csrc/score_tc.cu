@@ -38,27 +38,32 @@ namespace {
 using namespace ptx;
 
 constexpr int kStages = 3;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;                      // 4 TMEM lane quadrants x 4 column quarters
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 32 * (4 + kEpiWarps);
 constexpr uint32_t kBoxBytes = 128 * 128;          // 128 rows x 64 bf16 (one 128-byte row each)
 constexpr uint32_t kTileBytes = 2 * kBoxBytes;     // 128 rows x 128 bf16
-constexpr int kAFloats = 8192;                     // window means of one range, all G heads
-constexpr uint32_t kTmemCols = 256;                // two 128-column fp32 accumulators
+constexpr int kAFloats = 8192;                     // window sums of one range, all slots
+constexpr int kTBuf = 4;                           // TMEM accumulators of 128 fp32 columns
+constexpr uint32_t kTmemCols = 128 * kTBuf;
 constexpr int kMaxR = 15;                          // pool / 2
+#ifndef KV_TC_LAG
+#define KV_TC_LAG 2
+#endif
 
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = 2 * kTileBytes;
 constexpr uint32_t kOffA = kOffK + kStages * kTileBytes;
 constexpr uint32_t kOffLse = kOffA + kAFloats * 4;
 constexpr uint32_t kOffPart = kOffLse + 128 * 4;
-constexpr uint32_t kOffTail = kOffPart + 2 * 128 * 8;
+constexpr uint32_t kOffTail = kOffPart + 4 * 128 * 8;
 
 struct __align__(8) Tail {
   uint64_t full[kStages], empty[kStages];
   uint64_t qfull[2], qempty[2];
-  uint64_t tfull[2], tempty[2];
+  uint64_t tfull[kTBuf], tempty[kTBuf];
   uint64_t drain;
+  int64_t pf_unit;      // unit whose -lse already sits in the nlse buffer (-1: none)
   uint32_t tmem_base;
   int abort_flag;
   int last_flag;
@@ -68,23 +73,32 @@ constexpr uint32_t kSmemBytes = kOffTail + sizeof(Tail) + 1024;
 struct TcParams {
   int n, w, C, G, r, group_max;
   int64_t units;
-  int Pg, NG, Tu, Tc;
+  int Pg, PgS, NG, Tu, Tc;
+  int ncomb;            // CTAs that combine one unit's partials (power of two <= 16)
   float c2, inv_w;
   const float* vbar;
-  float2* partial;   // [units][Pg][128]
+  float2* partial;   // [units][128][PgS], PgS = Pg rounded up to even (padding unread)
   float* lse;        // [units][128] (log2 domain)
-  uint32_t* done1;   // [units]
-  uint32_t* ready;   // [units]
+  uint32_t* done1;   // [units] P1 partials written
+  uint32_t* ready;   // [units] LSE row slices published (complete at ncomb)
   float* halo;       // [units][Pg][G][4r]
   float* scores;     // [units][C]
   WsHeader* hdr;
 };
 
+// P2 of the k-th unit follows P1 of the (k + kLag)-th: P1(0..a-1), then P1(k), P2(k-a) pairs,
+// then the last P2s, with a = min(kLag, m).  kind 1 = P1, 2 = P2.
+constexpr int kLag = KV_TC_LAG;
 __device__ __forceinline__ void item_of(int64_t i, int64_t m, int& kind, int64_t& k) {
-  // P1(0), P1(1), P2(0), P1(2), P2(1), ..., P1(m-1), P2(m-2), P2(m-1); kind 1 = P1, 2 = P2
-  if (i == 0) { kind = 1; k = 0; return; }
-  if (i == 2 * m - 1) { kind = 2; k = m - 1; return; }
-  if (i & 1) { kind = 1; k = (i + 1) >> 1; } else { kind = 2; k = (i >> 1) - 1; }
+  const int64_t a = m < kLag ? m : kLag;
+  if (i < a) { kind = 1; k = i; return; }
+  const int64_t j = i - a;
+  if (j < 2 * (m - a)) {
+    if ((j & 1) == 0) { kind = 1; k = a + (j >> 1); } else { kind = 2; k = j >> 1; }
+    return;
+  }
+  kind = 2;
+  k = m - a + (j - 2 * (m - a));
 }
 
 template <int LW>
@@ -108,12 +122,15 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tl->qfull[b], 1);
       mbar_init(&tl->qempty[b], 1);
+    }
+    for (int b = 0; b < kTBuf; ++b) {
       mbar_init(&tl->tfull[b], 1);
       mbar_init(&tl->tempty[b], kEpiWarps);
     }
     mbar_init(&tl->drain, 1);
     tl->abort_flag = 0;
     tl->last_flag = 0;
+    tl->pf_unit = -1;
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -135,6 +152,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     if (lane == 0) {
       uint32_t g = 0, qi = 0;
       uint32_t kissued[kStages] = {}, qissued[2] = {};   // 1 + use index of the last copy
+      // P1 keeps its K tiles in L2 for the P2 re-read one unit later; P2 lets them go.
+      const uint64_t keep = make_policy_evict_last(), drop = make_policy_evict_first();
       bool ok = true;
       for (int64_t i = 0; i < n_items && ok; ++i) {
         int kind;
@@ -147,17 +166,20 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         if (!mbar_wait(&tl->qempty[qb], ((qi >> 1) & 1) ^ 1) || *abort_flag) { ok = false; break; }
         qissued[qb] = (qi >> 1) + 1;
         mbar_arrive_expect_tx(&tl->qfull[qb], kTileBytes);
-        tma_load_3d(smem + kOffQ + qb * kTileBytes, &qmap, &tl->qfull[qb], 0, 0, (int)u);
-        tma_load_3d(smem + kOffQ + qb * kTileBytes + kBoxBytes, &qmap, &tl->qfull[qb], 64, 0,
-                    (int)u);
+        tma_load_3d_hint(smem + kOffQ + qb * kTileBytes, &qmap, &tl->qfull[qb], 0, 0, (int)u,
+                         kind == 1 ? keep : drop);
+        tma_load_3d_hint(smem + kOffQ + qb * kTileBytes + kBoxBytes, &qmap, &tl->qfull[qb], 64, 0,
+                         (int)u, kind == 1 ? keep : drop);
+        const uint64_t pol = kind == 1 ? keep : drop;
         for (int t = t0; t < te; ++t, ++g) {
           const int s = g % kStages;
           if (!mbar_wait(&tl->empty[s], ((g / kStages) & 1) ^ 1) || *abort_flag) { ok = false; break; }
           kissued[s] = g / kStages + 1;
           mbar_arrive_expect_tx(&tl->full[s], kTileBytes);
-          tma_load_3d(smem + kOffK + s * kTileBytes, &kmap, &tl->full[s], 0, t * 128, (int)u);
-          tma_load_3d(smem + kOffK + s * kTileBytes + kBoxBytes, &kmap, &tl->full[s], 64, t * 128,
-                      (int)u);
+          tma_load_3d_hint(smem + kOffK + s * kTileBytes, &kmap, &tl->full[s], 0, t * 128, (int)u,
+                           pol);
+          tma_load_3d_hint(smem + kOffK + s * kTileBytes + kBoxBytes, &kmap, &tl->full[s], 64,
+                           t * 128, (int)u, pol);
         }
         ++qi;
       }
@@ -187,9 +209,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         if (!mbar_wait(&tl->qfull[qb], (qi >> 1) & 1) || *abort_flag) { ok = false; break; }
         const uint32_t qaddr = smem_u32(smem + kOffQ + qb * kTileBytes);
         for (int t = t0; t < te; ++t, ++g) {
-          const int s = g % kStages, tb = g & 1;
+          const int s = g % kStages, tb = g % kTBuf;
           if (!mbar_wait(&tl->full[s], (g / kStages) & 1) ||
-              !mbar_wait(&tl->tempty[tb], ((g >> 1) & 1) ^ 1) || *abort_flag) {
+              !mbar_wait(&tl->tempty[tb], ((g / kTBuf) & 1) ^ 1) || *abort_flag) {
             ok = false;
             break;
           }
@@ -218,17 +240,92 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       mma_commit(&tl->drain);
       mbar_wait(&tl->drain, 0, 20000000ull);
     }
+  } else if (warp == 3) {
+    // ------------------------------ LSE agent ---------------------------------
+    // For the units it is assigned to (ncomb CTAs per unit, rotating), this warp waits
+    // until all P_g partials of the unit are written, merges the partials of its slice of
+    // rows into the log-sum-exp and publishes the slice.  It never delays the epilogue.
+    const int rpc = 128 / p.ncomb;
+    const int nf4 = p.PgS >> 1;                  // float4 (two partials) per row
+    for (int64_t k = 0; k < m; ++k) {
+      const int ci = (int)(((int64_t)rank - k * p.ncomb) % p.Pg + p.Pg) % p.Pg;
+      if (ci >= p.ncomb) continue;
+      const int64_t u = group + k * p.NG;
+      bool ok = true;
+      if (lane == 0) {
+        const uint64_t tw = globaltimer();
+        while (ld_acquire_u32(&p.done1[u]) < (uint32_t)p.Pg) {
+          if (*abort_flag || globaltimer() - tw > 2000000000ull) { ok = false; break; }
+          __nanosleep(64);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) {
+        if (lane == 0) {
+          raise_dev(p.hdr, DEV_WAIT_TIMEOUT, 5);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      __threadfence();
+      for (int rr = 0; rr < rpc; ++rr) {
+        const int row = ci * rpc + rr;
+        const float4* P4 = reinterpret_cast<const float4*>(p.partial + (u * 128 + row) * p.PgS);
+        float M = -INFINITY, S = 0.f;
+        constexpr int kV = 4;
+        for (int b0 = lane; b0 < nf4; b0 += 32 * kV) {
+          float4 v[kV];
+#pragma unroll
+          for (int j = 0; j < kV; ++j)
+            v[j] = b0 + 32 * j < nf4 ? __ldcg(P4 + b0 + 32 * j)
+                                    : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+#pragma unroll
+          for (int j = 0; j < kV; ++j) {
+            const float ms[2] = {v[j].x, v[j].z}, ls[2] = {v[j].y, v[j].w};
+            const int q0 = 2 * (b0 + 32 * j);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (q0 + h >= p.Pg || ms[h] == -INFINITY) continue;   // padding / empty
+              const float Mn = fmaxf(M, ms[h]);
+              S = S * ex2(M - Mn) + ls[h] * ex2(ms[h] - Mn);
+              M = Mn;
+            }
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
+          const float So = __shfl_xor_sync(0xffffffffu, S, o);
+          const float Mn = fmaxf(M, Mo);
+          float Sn = 0.f;
+          if (M != -INFINITY) Sn += S * ex2(M - Mn);
+          if (Mo != -INFINITY) Sn += So * ex2(Mo - Mn);
+          M = Mn;
+          S = Sn;
+        }
+        if (lane == 0) p.lse[u * 128 + row] = M + log2f(S);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        atomicAdd(&p.ready[u], 1u);
+      }
+    }
   } else if (warp >= 4) {
     // ------------------------------ epilogue ----------------------------------
+    // Warp (4 + 4*qc + quad) reads TMEM lanes [32*quad, 32*quad + 32) and columns
+    // [32*qc, 32*qc + 32) of each accumulator.
     constexpr int W = 1 << LW;
-    constexpr int QH = 64 >> LW;                   // query heads per column half
-    const int quad = warp & 3, half = (warp - 4) >> 2, et = threadIdx.x - 128;
+    constexpr int SL = LW <= 5 ? (32 >> LW) : 1;   // window-sum slots per column quarter
+    constexpr int NSLOT = 4 * SL;                   // slots of all quarters (G or 2G)
+    const int quad = warp & 3, qc = (warp - 4) >> 2, et = threadIdx.x - 128;
     const int row = quad * 32 + lane;              // P1: window row; P2: key within the tile
     float* A = reinterpret_cast<float*>(smem + kOffA);
     float* nlse = reinterpret_cast<float*>(smem + kOffLse);
     float2* part_s = reinterpret_cast<float2*>(smem + kOffPart);
     const int RK = (t1 - t0) * 128;                // keys of this CTA's range (A stride)
     const int r = p.r, C = p.C, G = p.G;
+    const float c2 = p.c2;
     uint32_t g = 0;
     bool ok = true;
     for (int64_t i = 0; i < n_items && ok; ++i) {
@@ -239,127 +336,135 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       const int te = kind == 1 ? t1 : t1c;
       if (t0 >= te) continue;
       if (kind == 2) {
-        if (et == 0) {
-          const uint64_t tw = globaltimer();
-          while (ld_acquire_u32(&p.ready[u]) == 0u) {
-            if (*abort_flag || globaltimer() - tw > 2000000000ull) {
-              raise_dev(p.hdr, DEV_WAIT_TIMEOUT, 3);
-              *abort_flag = 1;
-              break;
+        if (tl->pf_unit != u) {     // not prefetched during the previous P1 item: wait now
+          if (et == 0) {
+            const uint64_t tw = globaltimer();
+            while (ld_acquire_u32(&p.ready[u]) < (uint32_t)p.ncomb) {
+              if (*abort_flag || globaltimer() - tw > 2000000000ull) {
+                raise_dev(p.hdr, DEV_WAIT_TIMEOUT, 3);
+                *abort_flag = 1;
+                break;
+              }
+              __nanosleep(64);
             }
-            __nanosleep(128);
           }
+          named_bar(1, kEpiThreads);
+          if (*abort_flag) { ok = false; break; }
+          if (et < 128) nlse[et] = -__ldcg(&p.lse[u * 128 + et]);
         }
         named_bar(1, kEpiThreads);
-        if (*abort_flag) { ok = false; break; }
-        if (et < 128) nlse[et] = -__ldcg(&p.lse[u * 128 + et]);
-        named_bar(1, kEpiThreads);
+      }
+      // During a P1 item, warp 4 watches for the LSE of the P2 item that comes next and
+      // stages it in nlse, so that item rarely has to wait.
+      int64_t pf_u = -1;
+      if (kind == 1 && warp == 4 && i + 1 < n_items) {
+        int k2kind;
+        int64_t k2;
+        item_of(i + 1, m, k2kind, k2);
+        if (k2kind == 2 && t0 < t1c) pf_u = group + k2 * p.NG;
       }
       float m_run = -INFINITY, l_run = 0.f;
       for (int t = t0; t < te; ++t, ++g) {
-        const int tb = g & 1;
-        if (!mbar_wait(&tl->tfull[tb], (g >> 1) & 1) || *abort_flag) { ok = false; break; }
+        const int tb = g % kTBuf;
+        uint32_t pf_flag = 0;
+        if (pf_u >= 0 && lane == 0) pf_flag = ld_relaxed_u32(&p.ready[pf_u]);   // used below
+        if (!mbar_wait(&tl->tfull[tb], (g / kTBuf) & 1) || *abort_flag) { ok = false; break; }
         tc_fence_after();
-        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + tb * 128 + half * 64;
-        uint32_t ra[32], rb[32];
-        tmem_ld32(taddr, ra);
-        tmem_ld32(taddr + 32, rb);
+        uint32_t ra[32];
+        tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + tb * 128 + qc * 32, ra);
         tmem_ld_wait(ra);
-        tmem_ld_wait(rb);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tl->tempty[tb]);
         if (kind == 1) {
-          const int key0 = t * 128 + half * 64;
-          const int limit = p.n - W + (row & (W - 1));   // last key window row t can see
-          float v[64];
+          const int key0 = t * 128 + qc * 32;
+          float v[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            v[c] = __uint_as_float(ra[c]) * p.c2;
-            v[32 + c] = __uint_as_float(rb[c]) * p.c2;
-          }
-          if (key0 + 63 > p.n - W) {
+          for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(ra[c]);
+          if (key0 + 31 > p.n - W) {
+            const int limit = p.n - W + (row & (W - 1));   // last key window row t sees
 #pragma unroll
-            for (int c = 0; c < 64; ++c)
+            for (int c = 0; c < 32; ++c)
               if (key0 + c > limit) v[c] = -INFINITY;
           }
-          float mx = v[0];
+          float mx[8];
 #pragma unroll
-          for (int c = 1; c < 64; ++c) mx = fmaxf(mx, v[c]);
-          const float mn = fmaxf(m_run, mx);
+          for (int j = 0; j < 8; ++j) mx[j] = fmaxf(fmaxf(v[j], v[j + 8]), fmaxf(v[j + 16], v[j + 24]));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mx[j] = fmaxf(mx[j], mx[j + 4]);
+          const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
+          const float mn = fmaxf(m_run, tmax);
           if (mn != -INFINITY) {
-            float s0 = 0.f, s1 = 0.f;
+            float sa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
-              s0 += ex2(v[c] - mn);
-              s1 += ex2(v[c + 1] - mn);
-            }
-            l_run = l_run * ex2(m_run - mn) + (s0 + s1);
+            for (int c = 0; c < 32; ++c) sa[c & 3] += ex2(fmaf(v[c], c2, -mn));
+            l_run = l_run * ex2(m_run - mn) + ((sa[0] + sa[1]) + (sa[2] + sa[3]));
             m_run = mn;
           }
         } else {
-          float acc[QH];
+          constexpr int CPS = 32 / SL;              // columns per slot
+          float acc[SL];
 #pragma unroll
-          for (int q = 0; q < QH; ++q) acc[q] = 0.f;
-          const float* nl = nlse + half * 64;
+          for (int j = 0; j < SL; ++j) acc[j] = 0.f;
+          const float* nl = nlse + qc * 32;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            acc[c >> LW] += ex2(fmaf(__uint_as_float(ra[c]), p.c2, nl[c]));
-            acc[(32 + c) >> LW] += ex2(fmaf(__uint_as_float(rb[c]), p.c2, nl[32 + c]));
-          }
+          for (int c = 0; c < 32; ++c) acc[c / CPS] += ex2(fmaf(__uint_as_float(ra[c]), c2, nl[c]));
           const int kl = (t - t0) * 128 + row;
-          const int q0 = (half * 64) >> LW;
 #pragma unroll
-          for (int q = 0; q < QH; ++q) A[(q0 + q) * RK + kl] = acc[q] * p.inv_w;
+          for (int j = 0; j < SL; ++j)
+            A[(qc * SL + j) * RK + kl] = LW <= 5 ? acc[j] * p.inv_w : acc[j];
+        }
+        if (pf_u >= 0) {
+          if (__shfl_sync(0xffffffffu, pf_flag, 0) >= (uint32_t)p.ncomb) {
+            __threadfence();
+            const float4 l4 = __ldcg(reinterpret_cast<const float4*>(p.lse + pf_u * 128) + lane);
+            reinterpret_cast<float4*>(nlse)[lane] = make_float4(-l4.x, -l4.y, -l4.z, -l4.w);
+            __syncwarp();
+            if (lane == 0) tl->pf_unit = pf_u;
+            pf_u = -1;
+          }
         }
       }
       if (!ok) break;
       if (kind == 1) {
-        part_s[half * 128 + row] = make_float2(m_run, l_run);
+        part_s[qc * 128 + row] = make_float2(m_run, l_run);
         named_bar(1, kEpiThreads);
-        if (half == 0) {
-          const float2 a = part_s[row], b = part_s[128 + row];
-          const float M = fmaxf(a.x, b.x);
+        if (et < 128) {
+          float M = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) M = fmaxf(M, part_s[j * 128 + et].x);
           float L = 0.f;
-          if (a.x != -INFINITY) L += a.y * ex2(a.x - M);
-          if (b.x != -INFINITY) L += b.y * ex2(b.x - M);
-          p.partial[(u * p.Pg + rank) * 128 + row] = make_float2(M, L);
-        }
-        __threadfence();
-        named_bar(1, kEpiThreads);
-        if (et == 0) tl->last_flag = (atomicAdd(&p.done1[u], 1u) == (uint32_t)(p.Pg - 1)) ? 1 : 0;
-        named_bar(1, kEpiThreads);
-        if (tl->last_flag) {
-          __threadfence();
-          if (et < 128) {
-            const float2* P = p.partial + u * p.Pg * 128 + et;
-            float M = -INFINITY;
-            for (int q = 0; q < p.Pg; ++q) M = fmaxf(M, __ldcg(P + q * 128).x);
-            float S = 0.f;
-            for (int q = 0; q < p.Pg; ++q) {
-              const float2 v = __ldcg(P + q * 128);
-              if (v.x != -INFINITY) S += v.y * ex2(v.x - M);
-            }
-            p.lse[u * 128 + et] = M + log2f(S);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 a = part_s[j * 128 + et];
+            if (a.x != -INFINITY) L += a.y * ex2(a.x - M);
           }
-          __threadfence();
-          named_bar(1, kEpiThreads);
-          if (et == 0) st_release_u32(&p.ready[u], 1u);
+          p.partial[(u * 128 + et) * p.PgS + rank] = make_float2(M, L);
         }
+        named_bar(1, kEpiThreads);
+        if (et == 0) {
+          __threadfence();   // cumulative: the partials written above become visible first
+          atomicAdd(&p.done1[u], 1u);
+        }
+        named_bar(1, kEpiThreads);     // part_s is free for the next item
       } else {
         named_bar(1, kEpiThreads);
         const int sK = t0 * 128;
         const int eK = min(te * 128, C);
         const float vb = p.vbar ? p.vbar[u] : 1.0f;
         float* H = p.halo + (u * p.Pg + rank) * (int64_t)G * 4 * r;
+        // window mean of query head q at key j (slots hold per-quarter sums for w = 64)
+        auto aval = [&](int q, int j) -> float {
+          if (LW <= 5) return A[q * RK + (j - sK)];
+          return (A[(2 * q) * RK + (j - sK)] + A[(2 * q + 1) * RK + (j - sK)]) * p.inv_w;
+        };
         for (int j = sK + et; j < eK; j += kEpiThreads) {
           const int lo = max(0, j - r), hi = min(C - 1, j + r);
           if (lo >= sK && hi < eK) {
             float gv = p.group_max ? -INFINITY : 0.f;
             for (int q = 0; q < G; ++q) {
-              const float* Aq = A + q * RK - sK;
               float pm = -INFINITY;
-              for (int jj = lo; jj <= hi; ++jj) pm = fmaxf(pm, Aq[jj]);
+              for (int jj = lo; jj <= hi; ++jj) pm = fmaxf(pm, aval(q, jj));
               gv = p.group_max ? fmaxf(gv, pm) : gv + pm;
             }
             if (!p.group_max) gv = gv / (float)G;
@@ -368,14 +473,15 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
           }
           if (r > 0) {
             if (j < sK + 2 * r)
-              for (int q = 0; q < G; ++q) H[q * 4 * r + (j - sK)] = A[q * RK + (j - sK)];
+              for (int q = 0; q < G; ++q) H[q * 4 * r + (j - sK)] = aval(q, j);
             if (j >= eK - 2 * r)
-              for (int q = 0; q < G; ++q)
-                H[q * 4 * r + 2 * r + (j - (eK - 2 * r))] = A[q * RK + (j - sK)];
+              for (int q = 0; q < G; ++q) H[q * 4 * r + 2 * r + (j - (eK - 2 * r))] = aval(q, j);
           }
         }
+        if (et == 0) tl->pf_unit = -1;
         named_bar(1, kEpiThreads);
       }
+      (void)NSLOT;
     }
     if (!ok) {
       raise_dev(p.hdr, DEV_WAIT_TIMEOUT, 4);
@@ -504,7 +610,8 @@ bool tc_plan(const Shape& s, TcPlan* out) {
   p.Tu = (int)cdiv(s.n, 128);
   p.Tc = (int)cdiv(s.C(), 128);
   const int64_t units = s.units();
-  const int max_tiles = kAFloats / (s.G() * 128);
+  const int slots = s.w <= 32 ? 4 * (32 / s.w) : 4;   // window-sum slots per key
+  const int max_tiles = kAFloats / (slots * 128);
   // groups: each keeps about two units of K in L2 (about 64 MiB per group in total)
   const double unit_bytes = (double)s.n * 128 * 2;
   int NG = (int)(64.0 * 1024 * 1024 / (2.0 * unit_bytes));
@@ -526,7 +633,7 @@ bool tc_plan(const Shape& s, TcPlan* out) {
   const int r = s.pool / 2;
   size_t off = kWsHeader;
   p.off_partial = off;
-  off += align_up((size_t)units * Pg * 128 * sizeof(float2), 256);
+  off += align_up((size_t)units * ((Pg + 1) & ~1) * 128 * sizeof(float2), 256);
   p.off_lse = off;
   off += align_up((size_t)units * 128 * sizeof(float), 256);
   p.off_flags = off;
@@ -595,6 +702,9 @@ cudaError_t launch_score_tc(const Shape& s, int mode, int group, const void* q_w
   prm.group_max = group == KV_GROUP_MAX;
   prm.units = units;
   prm.Pg = tp.Pg;
+  prm.PgS = (tp.Pg + 1) & ~1;
+  prm.ncomb = 1;
+  while (prm.ncomb * 2 <= 16 && prm.ncomb * 2 <= tp.Pg) prm.ncomb *= 2;
   prm.NG = tp.NG;
   prm.Tu = tp.Tu;
   prm.Tc = tp.Tc;
@@ -609,6 +719,7 @@ cudaError_t launch_score_tc(const Shape& s, int mode, int group, const void* q_w
   prm.hdr = reinterpret_cast<WsHeader*>(ws);
   cudaError_t e = cudaMemsetAsync(prm.done1, 0, (size_t)units * 2 * sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
+
   if (mode == KV_SCORE_LAVA) {
     float* vbar = reinterpret_cast<float*>(ws + tp.off_vbar);
     e = cudaMemsetAsync(vbar, 0, (size_t)units * sizeof(float), st);
