@@ -19,9 +19,14 @@
 // flag.  Keys whose pooling window crosses a CTA's range boundary are finished by
 // score_tc_fixup from per-range halo copies of the window means.
 //
-// Roles (384 threads): warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM
-// allocator, warps 4..11 = epilogue (TMEM lane quadrant = warp % 4, column half =
-// (warp - 4) / 4).  Every wait is bounded; on a timeout the CTA records DEV_WAIT_TIMEOUT,
+// LAVa: during P2 items (K then comes from L2) the producer also puts the V tiles of the
+// range into the ring; warp 2 folds them into max ||V[k]||_1 of the unit.  P2 writes
+// unscaled scores and the fix-up kernel applies the factor after the kernel, so nothing
+// here waits for V.
+//
+// Roles (640 threads): warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM
+// allocator and LAVa V streamer, warp 3 = LSE agent, warps 4..19 = epilogue (TMEM lane
+// quadrant = warp % 4, column quarter = (warp - 4) / 4).  Every wait is bounded; on a timeout the CTA records DEV_WAIT_TIMEOUT,
 // unwinds, waits (bounded) for its copies and MMAs in flight and frees its TMEM.
 #include <cudaTypedefs.h>
 
@@ -37,13 +42,13 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kEpiWarps = 16;                      // 4 TMEM lane quadrants x 4 column quarters
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 32 * (4 + kEpiWarps);
 constexpr uint32_t kBoxBytes = 128 * 128;          // 128 rows x 64 bf16 (one 128-byte row each)
 constexpr uint32_t kTileBytes = 2 * kBoxBytes;     // 128 rows x 128 bf16
-constexpr int kAFloats = 8192;                     // window sums of one range, all slots
+constexpr int kAFloats = 6144;                     // window sums of one range, all slots
 constexpr int kTBuf = 4;                           // TMEM accumulators of 128 fp32 columns
 constexpr uint32_t kTmemCols = 128 * kTBuf;
 constexpr int kMaxR = 15;                          // pool / 2
@@ -59,7 +64,10 @@ constexpr uint32_t kOffPart = kOffLse + 128 * 4;
 constexpr uint32_t kOffTail = kOffPart + 4 * 128 * 8;
 
 struct __align__(8) Tail {
-  uint64_t full[kStages], empty[kStages];
+  // A ring stage holds either a K tile (consumed by the MMA warp) or, in LAVa P2 items, a
+  // V tile (consumed by warp 2).  Each kind completes its own barrier so that no consumer
+  // ever has to skip a phase of the barrier it waits on (skipped phases alias in parity).
+  uint64_t full[kStages], fullv[kStages], empty[kStages];
   uint64_t qfull[2], qempty[2];
   uint64_t tfull[kTBuf], tempty[kTBuf];
   uint64_t drain;
@@ -69,6 +77,7 @@ struct __align__(8) Tail {
   int last_flag;
 };
 constexpr uint32_t kSmemBytes = kOffTail + sizeof(Tail) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 
 struct TcParams {
   int n, w, C, G, r, group_max;
@@ -76,7 +85,7 @@ struct TcParams {
   int Pg, PgS, NG, Tu, Tc;
   int ncomb;            // CTAs that combine one unit's partials (power of two <= 16)
   float c2, inv_w;
-  const float* vbar;
+  float* vbar;        // LAVa: per-unit max ||V[k]||_1 (float bits, atomicMax), else null
   float2* partial;   // [units][128][PgS], PgS = Pg rounded up to even (padding unread)
   float* lse;        // [units][128] (log2 domain)
   uint32_t* done1;   // [units] P1 partials written
@@ -104,7 +113,7 @@ __device__ __forceinline__ void item_of(int64_t i, int64_t m, int& kind, int64_t
 template <int LW>
 __global__ void __launch_bounds__(kThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
-                const TcParams p) {
+                const __grid_constant__ CUtensorMap vmap, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -118,7 +127,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   const int64_t n_items = 2 * m;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) { mbar_init(&tl->full[s], 1); mbar_init(&tl->empty[s], 1); }
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&tl->full[s], 1);
+      mbar_init(&tl->fullv[s], 1);
+      mbar_init(&tl->empty[s], 1);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tl->qfull[b], 1);
       mbar_init(&tl->qempty[b], 1);
@@ -151,7 +164,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
       uint32_t g = 0, qi = 0;
-      uint32_t kissued[kStages] = {}, qissued[2] = {};   // 1 + use index of the last copy
+      uint32_t kfill[kStages] = {}, vfill[kStages] = {};  // copies per stage and kind
+      bool lastv[kStages] = {};                           // kind of each stage's last copy
+      uint32_t qissued[2] = {};                           // 1 + use index of the last Q copy
       // P1 keeps its K tiles in L2 for the P2 re-read one unit later; P2 lets them go.
       const uint64_t keep = make_policy_evict_last(), drop = make_policy_evict_first();
       bool ok = true;
@@ -174,21 +189,44 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         for (int t = t0; t < te; ++t, ++g) {
           const int s = g % kStages;
           if (!mbar_wait(&tl->empty[s], ((g / kStages) & 1) ^ 1) || *abort_flag) { ok = false; break; }
-          kissued[s] = g / kStages + 1;
+          ++kfill[s];
+          lastv[s] = false;
           mbar_arrive_expect_tx(&tl->full[s], kTileBytes);
           tma_load_3d_hint(smem + kOffK + s * kTileBytes, &kmap, &tl->full[s], 0, t * 128, (int)u,
                            pol);
           tma_load_3d_hint(smem + kOffK + s * kTileBytes + kBoxBytes, &kmap, &tl->full[s], 64,
                            t * 128, (int)u, pol);
+          // LAVa: the V rows of this tile (and, after the last candidate tile, of the
+          // window-only tiles of the range) follow as ring entries that warp 2 consumes
+          const int vt_end = (kind == 2 && p.vbar != nullptr) ? (t + 1 < te ? t + 1 : t1) : t;
+          for (int vt = t; vt < vt_end && ok; ++vt) {
+            ++g;
+            const int sv = g % kStages;
+            if (!mbar_wait(&tl->empty[sv], ((g / kStages) & 1) ^ 1) || *abort_flag) {
+              ok = false;
+              break;
+            }
+            ++vfill[sv];
+            lastv[sv] = true;
+            mbar_arrive_expect_tx(&tl->fullv[sv], kTileBytes);
+            tma_load_3d_hint(smem + kOffK + sv * kTileBytes, &vmap, &tl->fullv[sv], 0, vt * 128,
+                             (int)u, drop);
+            tma_load_3d_hint(smem + kOffK + sv * kTileBytes + kBoxBytes, &vmap, &tl->fullv[sv], 64,
+                             vt * 128, (int)u, drop);
+          }
+          if (!ok) break;
         }
         ++qi;
       }
       if (!ok) {
         raise_dev(p.hdr, DEV_WAIT_TIMEOUT, 1);
         *abort_flag = 1;
-        // let the copies already issued land before the CTA exits
-        for (int s = 0; s < kStages; ++s)
-          if (kissued[s]) mbar_wait(&tl->full[s], (kissued[s] - 1) & 1, 20000000ull);
+        // let the copies already issued land before the CTA exits: the last copy of each
+        // stage is the only phase of its barrier that can still be pending
+        for (int s = 0; s < kStages; ++s) {
+          if (lastv[s]) mbar_wait(&tl->fullv[s], (vfill[s] - 1) & 1, 20000000ull);
+          else if (kfill[s]) mbar_wait(&tl->full[s], (kfill[s] - 1) & 1, 20000000ull);
+        }
         for (int b = 0; b < 2; ++b)
           if (qissued[b]) mbar_wait(&tl->qfull[b], (qissued[b] - 1) & 1, 20000000ull);
       }
@@ -197,7 +235,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     // ------------------------------ MMA issuer --------------------------------
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, 128);
-      uint32_t g = 0, qi = 0;
+      uint32_t g = 0, gt = 0, qi = 0;   // ring entries (K and V), TMEM accumulators (K)
+      uint32_t kuse[kStages] = {};      // K tiles consumed per stage (phases of full[s])
       bool ok = true;
       for (int64_t i = 0; i < n_items && ok; ++i) {
         int kind;
@@ -208,10 +247,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         const int qb = qi & 1;
         if (!mbar_wait(&tl->qfull[qb], (qi >> 1) & 1) || *abort_flag) { ok = false; break; }
         const uint32_t qaddr = smem_u32(smem + kOffQ + qb * kTileBytes);
-        for (int t = t0; t < te; ++t, ++g) {
-          const int s = g % kStages, tb = g % kTBuf;
-          if (!mbar_wait(&tl->full[s], (g / kStages) & 1) ||
-              !mbar_wait(&tl->tempty[tb], ((g / kTBuf) & 1) ^ 1) || *abort_flag) {
+        for (int t = t0; t < te; ++t, ++g, ++gt) {
+          const int s = g % kStages, tb = gt % kTBuf;
+          if (!mbar_wait(&tl->full[s], kuse[s]++ & 1) ||
+              !mbar_wait(&tl->tempty[tb], ((gt / kTBuf) & 1) ^ 1) || *abort_flag) {
             ok = false;
             break;
           }
@@ -227,6 +266,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
           }
           mma_commit(&tl->empty[s]);
           mma_commit(&tl->tfull[tb]);
+          if (kind == 2 && p.vbar != nullptr) g += (t + 1 < te ? 1 : t1 - t);   // V entries
         }
         if (!ok) break;
         mma_commit(&tl->qempty[qb]);
@@ -239,6 +279,71 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       // every MMA issued has completed before TMEM is freed
       mma_commit(&tl->drain);
       mbar_wait(&tl->drain, 0, 20000000ull);
+    }
+  } else if (warp == 2) {
+    // ------------------------------ LAVa V-bar --------------------------------
+    // Consumes the V entries the producer puts in the ring during P2 items (K comes from
+    // L2 then, so the two passes share DRAM evenly), folds max_k ||V[k]||_1 of the unit
+    // into vbar[u] and frees each entry with one arrive.  Nothing waits for it: the
+    // fix-up kernel applies the factor after this kernel.
+    if (p.vbar != nullptr) {
+      uint32_t g = 0;
+      uint32_t vuse[kStages] = {};      // V tiles consumed per stage (phases of fullv[s])
+      bool ok = true;
+      for (int64_t i = 0; i < n_items && ok; ++i) {
+        int kind;
+        int64_t k;
+        item_of(i, m, kind, k);
+        const int te = kind == 1 ? t1 : t1c;
+        if (t0 >= te) continue;
+        if (kind == 1) { g += te - t0; continue; }
+        float vmax = 0.f;
+        for (int t = t0; t < te && ok; ++t) {
+          ++g;   // the K entry of tile t
+          const int nv = t + 1 < te ? 1 : t1 - t;
+          for (int j = 0; j < nv; ++j, ++g) {
+            const int sv = g % kStages;
+            if (!mbar_wait(&tl->fullv[sv], vuse[sv]++ & 1) || *abort_flag) { ok = false; break; }
+            const uint8_t* base = smem + kOffK + sv * kTileBytes;
+            // lane l sums rows 4l..4l+3; the 16-byte pieces of a row are visited in a
+            // lane-rotated order (a row's sum does not depend on where the swizzle put them)
+#pragma unroll 1
+            for (int rr = 0; rr < 4; ++rr) {
+              const int row = 4 * lane + rr;
+              float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+              for (int bx = 0; bx < 2; ++bx) {
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                  const int jp = (jj + lane) & 7;
+                  const uint4 x =
+                      *reinterpret_cast<const uint4*>(base + bx * kBoxBytes + row * 128 + jp * 16);
+                  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(h[e]);
+                    a0 += fabsf(f.x);
+                    a1 += fabsf(f.y);
+                  }
+                }
+              }
+              vmax = fmaxf(vmax, a0 + a1);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tl->empty[sv]);
+          }
+        }
+        if (!ok) break;
+        const float wm = warp_max(vmax);
+        if (lane == 0 && wm > 0.f) {
+          const int64_t u = group + k * p.NG;
+          atomicMax(reinterpret_cast<unsigned int*>(p.vbar) + u, __float_as_uint(wm));
+        }
+      }
+      if (!ok && lane == 0) {
+        raise_dev(p.hdr, DEV_WAIT_TIMEOUT, 6);
+        *abort_flag = 1;
+      }
     }
   } else if (warp == 3) {
     // ------------------------------ LSE agent ---------------------------------
@@ -326,7 +431,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     const int RK = (t1 - t0) * 128;                // keys of this CTA's range (A stride)
     const int r = p.r, C = p.C, G = p.G;
     const float c2 = p.c2;
-    uint32_t g = 0;
+    uint32_t g = 0;     // TMEM accumulator counter (K tiles)
     bool ok = true;
     for (int64_t i = 0; i < n_items && ok; ++i) {
       int kind;
@@ -451,31 +556,74 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         named_bar(1, kEpiThreads);
         const int sK = t0 * 128;
         const int eK = min(te * 128, C);
-        const float vb = p.vbar ? p.vbar[u] : 1.0f;
         float* H = p.halo + (u * p.Pg + rank) * (int64_t)G * 4 * r;
         // window mean of query head q at key j (slots hold per-quarter sums for w = 64)
         auto aval = [&](int q, int j) -> float {
           if (LW <= 5) return A[q * RK + (j - sK)];
           return (A[(2 * q) * RK + (j - sK)] + A[(2 * q + 1) * RK + (j - sK)]) * p.inv_w;
         };
-        for (int j = sK + et; j < eK; j += kEpiThreads) {
-          const int lo = max(0, j - r), hi = min(C - 1, j + r);
-          if (lo >= sK && hi < eK) {
-            float gv = p.group_max ? -INFINITY : 0.f;
-            for (int q = 0; q < G; ++q) {
-              float pm = -INFINITY;
-              for (int jj = lo; jj <= hi; ++jj) pm = fmaxf(pm, aval(q, jj));
-              gv = p.group_max ? fmaxf(gv, pm) : gv + pm;
+        if (r == 3) {
+          // pool 7: one thread per (run of 8 keys, query head); the window maximum is
+          // max(max of 4, max of 2, 1) over values loaded once (-inf outside the range);
+          // the G query heads of a run sit in adjacent lanes and are combined by shuffles.
+          constexpr int RUN = 8;
+          const int qh = et & (G - 1), run = et / G;
+          const int nruns = (eK - sK + RUN - 1) / RUN;
+          const int stride = kEpiThreads / G;
+          for (int rr = run; rr < nruns + (stride - nruns % stride) % stride; rr += stride) {
+            const bool live = rr < nruns;
+            const int j0 = sK + rr * RUN;
+            float v[RUN + 6];
+#pragma unroll
+            for (int i = 0; i < RUN + 6; ++i) {
+              const int jj = j0 - 3 + i;
+              v[i] = (live && jj >= sK && jj < eK) ? aval(qh, jj) : -INFINITY;
             }
-            if (!p.group_max) gv = gv / (float)G;
-            if (p.vbar) gv = gv * vb;
-            p.scores[u * C + j] = gv;
+            float m2[RUN + 5], out[RUN];
+#pragma unroll
+            for (int i = 0; i < RUN + 5; ++i) m2[i] = fmaxf(v[i], v[i + 1]);
+#pragma unroll
+            for (int i = 0; i < RUN; ++i)
+              out[i] = fmaxf(fmaxf(fmaxf(m2[i], m2[i + 2]), m2[i + 4]), v[i + 6]);
+#pragma unroll
+            for (int i = 0; i < RUN; ++i) {
+              float gv = out[i];
+              for (int o = 1; o < G; o <<= 1) {
+                const float x = __shfl_xor_sync(0xffffffffu, gv, o);
+                gv = p.group_max ? fmaxf(gv, x) : gv + x;
+              }
+              out[i] = p.group_max ? gv : gv / (float)G;
+            }
+            if (live && qh == 0) {
+#pragma unroll
+              for (int i = 0; i < RUN; ++i) {
+                const int j = j0 + i;
+                if (j >= eK) break;
+                const int lo = max(0, j - 3), hi = min(C - 1, j + 3);
+                if (lo >= sK && hi < eK) p.scores[u * C + j] = out[i];
+              }
+            }
           }
-          if (r > 0) {
-            if (j < sK + 2 * r)
-              for (int q = 0; q < G; ++q) H[q * 4 * r + (j - sK)] = aval(q, j);
-            if (j >= eK - 2 * r)
-              for (int q = 0; q < G; ++q) H[q * 4 * r + 2 * r + (j - (eK - 2 * r))] = aval(q, j);
+        } else {
+          for (int j = sK + et; j < eK; j += kEpiThreads) {
+            const int lo = max(0, j - r), hi = min(C - 1, j + r);
+            if (lo >= sK && hi < eK) {
+              float gv = p.group_max ? -INFINITY : 0.f;
+              for (int q = 0; q < G; ++q) {
+                float pm = -INFINITY;
+                for (int jj = lo; jj <= hi; ++jj) pm = fmaxf(pm, aval(q, jj));
+                gv = p.group_max ? fmaxf(gv, pm) : gv + pm;
+              }
+              if (!p.group_max) gv = gv / (float)G;
+              p.scores[u * C + j] = gv;
+            }
+          }
+        }
+        if (r > 0) {   // halo copies for the fix-up of keys near the range's ends
+          for (int idx = et; idx < G * 4 * r; idx += kEpiThreads) {
+            const int q = idx / (4 * r), sl = idx % (4 * r);
+            const int j = sl < 2 * r ? sK + sl : eK - 2 * r + (sl - 2 * r);
+            if (j >= sK && j < eK) H[q * 4 * r + sl] = aval(q, j);
           }
         }
         if (et == 0) tl->pf_unit = -1;
@@ -495,12 +643,28 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   }
 }
 
-// Keys within pool/2 of a range boundary: pooled from the halo copies of both ranges.
+// After the main kernel: (LAVa) scale the unit's scores by max_k ||V[k]||_1, then pool the
+// keys within pool/2 of a range boundary from the halo copies of both ranges.
 __global__ void score_tc_fixup(const float* __restrict__ halo, const float* __restrict__ vbar,
                                int Pg, int Tu, int C, int G, int r, int group_max,
                                float* __restrict__ scores) {
   const int64_t u = blockIdx.x;
   const int R4 = 4 * r;
+  float vb = 1.0f;
+  float* S = scores + u * C;
+  if (vbar) {
+    vb = vbar[u];
+    for (int j = threadIdx.x * 4; j < C; j += blockDim.x * 4) {
+      if (j + 3 < C && ((reinterpret_cast<uintptr_t>(S + j) & 15) == 0)) {
+        float4 x = *reinterpret_cast<float4*>(S + j);
+        x.x *= vb; x.y *= vb; x.z *= vb; x.w *= vb;
+        *reinterpret_cast<float4*>(S + j) = x;
+      } else {
+        for (int jj = j; jj < min(C, j + 4); ++jj) S[jj] *= vb;
+      }
+    }
+    __syncthreads();
+  }
   for (int idx = threadIdx.x; idx < (Pg - 1) * 2 * r; idx += blockDim.x) {
     const int bnd = idx / (2 * r) + 1;
     const int b = (int)(((int64_t)bnd * Tu) / Pg) * 128;
@@ -520,43 +684,8 @@ __global__ void score_tc_fixup(const float* __restrict__ halo, const float* __re
       gv = group_max ? fmaxf(gv, pm) : gv + pm;
     }
     if (!group_max) gv = gv / (float)G;
-    if (vbar) gv = gv * vbar[u];
-    scores[u * C + j] = gv;
-  }
-}
-
-// vbar[unit] = max over rows of ||V[row]||_1 for bf16 rows of 128 (16 lanes x 16 bytes).
-__global__ void __launch_bounds__(256)
-vbar_vec_bf16(const uint4* __restrict__ v, int n, int rows_per_cta, unsigned int* __restrict__ bits) {
-  const int64_t unit = blockIdx.y;
-  const int sub = threadIdx.x & 15, rr = threadIdx.x >> 4;
-  const int r0 = blockIdx.x * rows_per_cta, r1 = min(n, r0 + rows_per_cta);
-  const uint4* V = v + unit * (int64_t)n * 16;
-  float mx = 0.f;
-#pragma unroll 4
-  for (int row = r0 + rr; row < r1; row += 16) {
-    const uint4 x = __ldcs(V + (int64_t)row * 16 + sub);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __bfloat1622float2(h[i]);
-      s += fabsf(f.x) + fabsf(f.y);
-    }
-    s += __shfl_xor_sync(0xffffffffu, s, 8);
-    s += __shfl_xor_sync(0xffffffffu, s, 4);
-    s += __shfl_xor_sync(0xffffffffu, s, 2);
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    mx = fmaxf(mx, s);
-  }
-  mx = warp_max(mx);
-  __shared__ float wm[8];
-  if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = mx;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float m = wm[0];
-    for (int i = 1; i < 8; ++i) m = fmaxf(m, wm[i]);
-    atomicMax(&bits[unit], __float_as_uint(m));
+    if (vbar) gv = gv * vb;
+    S[j] = gv;
   }
 }
 
@@ -576,12 +705,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t units) {
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t units,
+              uint32_t box_rows = 128) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[3] = {128, rows, units};
   const cuuint64_t strides[2] = {128 * 2, rows * 128 * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -619,7 +749,8 @@ bool tc_plan(const Shape& s, TcPlan* out) {
   if (NG > P) NG = P;
   if (NG > units) NG = (int)units;
   int Pg = P / NG;
-  if (Pg > p.Tu) Pg = p.Tu;
+  // every range holds at least one candidate tile (so its P2 item streams all its V rows)
+  if (Pg > p.Tc) Pg = p.Tc;
   if (cdiv(p.Tu, Pg) > max_tiles) {
     // ranges too long for the window-mean buffer: use more CTAs per unit
     Pg = (int)cdiv(p.Tu, max_tiles);
@@ -637,7 +768,7 @@ bool tc_plan(const Shape& s, TcPlan* out) {
   p.off_lse = off;
   off += align_up((size_t)units * 128 * sizeof(float), 256);
   p.off_flags = off;
-  off += align_up((size_t)units * 2 * sizeof(uint32_t), 256);
+  off += align_up((size_t)units * 3 * sizeof(uint32_t), 256);
   p.off_halo = off;
   off += align_up((size_t)units * Pg * s.G() * 4 * r * sizeof(float) + 4, 256);
   p.off_vbar = off;
@@ -648,8 +779,8 @@ bool tc_plan(const Shape& s, TcPlan* out) {
 }
 
 template <int LW>
-cudaError_t launch_main(const CUtensorMap& km, const CUtensorMap& qm, const TcParams& prm,
-                        int grid, cudaStream_t st) {
+cudaError_t launch_main(const CUtensorMap& km, const CUtensorMap& qm, const CUtensorMap& vm,
+                        const TcParams& prm, int grid, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<LW>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
@@ -664,7 +795,7 @@ cudaError_t launch_main(const CUtensorMap& km, const CUtensorMap& qm, const TcPa
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, score_tc_kernel<LW>, km, qm, prm);
+  return cudaLaunchKernelEx(&cfg, score_tc_kernel<LW>, km, qm, vm, prm);
 }
 
 }  // namespace
@@ -689,10 +820,16 @@ cudaError_t launch_score_tc(const Shape& s, int mode, int group, const void* q_w
   TcPlan tp;
   if (!tc_plan(s, &tp)) return cudaErrorNotSupported;
   const int64_t units = s.units();
-  CUtensorMap km, qm;
+  CUtensorMap km, qm, vm;
   if (!make_map(&km, k, (uint64_t)s.n, (uint64_t)units) ||
       !make_map(&qm, q_win, 128, (uint64_t)units))
     return cudaErrorInvalidValue;
+  // V is only read for LAVa; otherwise the map is a copy of K's and never used.
+  if (mode == KV_SCORE_LAVA) {
+    if (!make_map(&vm, v, (uint64_t)s.n, (uint64_t)units)) return cudaErrorInvalidValue;
+  } else {
+    vm = km;
+  }
   TcParams prm{};
   prm.n = s.n;
   prm.w = s.w;
@@ -717,29 +854,25 @@ cudaError_t launch_score_tc(const Shape& s, int mode, int group, const void* q_w
   prm.halo = reinterpret_cast<float*>(ws + tp.off_halo);
   prm.scores = scores;
   prm.hdr = reinterpret_cast<WsHeader*>(ws);
-  cudaError_t e = cudaMemsetAsync(prm.done1, 0, (size_t)units * 2 * sizeof(uint32_t), st);
+  cudaError_t e = cudaMemsetAsync(prm.done1, 0, (size_t)units * 3 * sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
 
   if (mode == KV_SCORE_LAVA) {
     float* vbar = reinterpret_cast<float*>(ws + tp.off_vbar);
     e = cudaMemsetAsync(vbar, 0, (size_t)units * sizeof(float), st);
     if (e != cudaSuccess) return e;
-    const int rows = 1024;
-    vbar_vec_bf16<<<dim3((unsigned)cdiv(s.n, rows), (unsigned)units), 256, 0, st>>>(
-        reinterpret_cast<const uint4*>(v), s.n, rows, reinterpret_cast<unsigned int*>(vbar));
-    count_launches(1);
     prm.vbar = vbar;
   }
   switch (s.w) {
-    case 16: e = launch_main<4>(km, qm, prm, tp.grid, st); break;
-    case 32: e = launch_main<5>(km, qm, prm, tp.grid, st); break;
-    default: e = launch_main<6>(km, qm, prm, tp.grid, st); break;
+    case 16: e = launch_main<4>(km, qm, vm, prm, tp.grid, st); break;
+    case 32: e = launch_main<5>(km, qm, vm, prm, tp.grid, st); break;
+    default: e = launch_main<6>(km, qm, vm, prm, tp.grid, st); break;
   }
   if (e != cudaSuccess) return e;
   count_launches(1);
-  if (prm.r > 0 && tp.Pg > 1) {
-    score_tc_fixup<<<(unsigned)units, 64, 0, st>>>(prm.halo, prm.vbar, tp.Pg, tp.Tu, prm.C,
-                                                   prm.G, prm.r, prm.group_max, scores);
+  if (prm.vbar != nullptr || (prm.r > 0 && tp.Pg > 1)) {
+    score_tc_fixup<<<(unsigned)units, 256, 0, st>>>(
+        prm.halo, prm.vbar, tp.Pg, tp.Tu, prm.C, prm.G, prm.r, prm.group_max, scores);
     count_launches(1);
   }
   return cudaGetLastError();
