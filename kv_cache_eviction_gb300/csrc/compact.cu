@@ -75,6 +75,93 @@ compact_offsets(const int32_t* __restrict__ head_budget, int64_t H, int Hkv, int
   if (threadIdx.x == 0 && carry > cap) raise_dev(hdr, DEV_FLAT_CAPACITY, 0);
 }
 
+
+// Ordered selection of positions j in [0, C): keep(j) = forced(j) || key(j) > tau ||
+// (key(j) == tau && rank of j among the tau-equal keys < keq), i.e. the (key desc,
+// position asc) order.  Kept positions go, ascending, to kept[base + r] (rows >= cap are
+// skipped) or, with BITS, as one bit per position to bits[j / 32].  Two sweeps: per-warp
+// counts over contiguous slices, one scan of the warp totals, then each warp emits its
+// slice with ballots.  Returns the number of kept positions.  All threads must call it.
+template <int BLOCK, bool BITS, typename KeyFn, typename ForcedFn>
+__device__ uint32_t select_ordered(int C, KeyFn key, ForcedFn forced, uint32_t tau, uint32_t keq,
+                                   int32_t* kept, int64_t base, int64_t cap, uint32_t* bits,
+                                   uint32_t* scr /* 4 * 32 */) {
+  constexpr int NW = BLOCK / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per = (((C + NW - 1) / NW) + 31) & ~31;   // slice length, a multiple of 32
+  const int s0 = min(C, warp * per), s1 = min(C, s0 + per);
+  constexpr int U = 8;   // 32-key steps fetched per batch (latency hiding)
+  uint32_t nkeep = 0, neq = 0;
+  for (int jb = s0; jb < s1; jb += 32 * U) {
+    uint32_t kk[U];
+    bool ff[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = jb + 32 * u + lane;
+      kk[u] = j < s1 ? key(j) : 0u;
+      ff[u] = j < s1 ? forced(j) : false;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const bool in = jb + 32 * u + lane < s1;
+      nkeep += (in && (ff[u] || kk[u] > tau)) ? 1u : 0u;
+      neq += (in && !ff[u] && kk[u] == tau) ? 1u : 0u;
+    }
+  }
+  nkeep = warp_sum_u(nkeep);
+  neq = warp_sum_u(neq);
+  if (lane == 0) { scr[warp] = nkeep; scr[32 + warp] = neq; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t eq = 0, out = 0;
+    for (int w = 0; w < NW; ++w) {
+      const uint32_t e = scr[32 + w];
+      const uint32_t take = eq >= keq ? 0u : (keq - eq < e ? keq - eq : e);
+      scr[64 + w] = eq;    // tau-equal keys before this warp's slice
+      scr[96 + w] = out;   // kept positions before this warp's slice
+      out += scr[w] + take;
+      eq += e;
+    }
+    scr[0] = out;          // total (the per-warp counts are no longer needed)
+  }
+  __syncthreads();
+  uint32_t eqc = scr[64 + warp], outc = scr[96 + warp];
+  const uint32_t total = scr[0];
+  const uint32_t below = (1u << lane) - 1u;
+  for (int jb = s0; jb < s1; jb += 32 * U) {
+    uint32_t kk[U];
+    bool ff[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = jb + 32 * u + lane;
+      kk[u] = j < s1 ? key(j) : 0u;
+      ff[u] = j < s1 ? forced(j) : false;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j0 = jb + 32 * u;
+      if (j0 >= s1) break;   // uniform across the warp
+      const int j = j0 + lane;
+      const bool in = j < s1;
+      const bool iseq = in && !ff[u] && kk[u] == tau;
+      bool keep = in && (ff[u] || kk[u] > tau);
+      const uint32_t meq = __ballot_sync(0xFFFFFFFFu, iseq);
+      if (iseq && eqc + __popc(meq & below) < keq) keep = true;
+      const uint32_t mk = __ballot_sync(0xFFFFFFFFu, keep);
+      if (BITS) {
+        if (lane == 0) bits[j0 >> 5] = mk;
+      } else if (keep) {
+        const int64_t row = base + outc + __popc(mk & below);
+        if (row < cap) kept[row] = j;
+      }
+      eqc += __popc(meq);
+      outc += __popc(mk);
+    }
+  }
+  __syncthreads();   // scr is reused by the caller
+  return total;
+}
+
 // One CTA per head: threshold(s), ordered kept positions, window and reserve rows.
 __global__ void __launch_bounds__(kSelThreads)
 compact_select(const float* __restrict__ scores, const float* __restrict__ crit, uint32_t can,
@@ -83,90 +170,44 @@ compact_select(const float* __restrict__ scores, const float* __restrict__ crit,
                int32_t* __restrict__ kept, int64_t cap, uint32_t* __restrict__ flags,
                int64_t words, WsHeader* hdr) {
   __shared__ RadixSmem rs;
-  __shared__ uint32_t eqscr[32];
   const int64_t h = blockIdx.x;
   const int64_t seg = h / Hkv;
   const int g = (int)(h - seg * Hkv);
   const int64_t base = cu[seg * (Hkv + 1) + g];
   const int64_t Bg = (int64_t)lens[h] - w;   // lens was clamped to [w, n]
   const float* S = scores + h * (int64_t)C;
+  __shared__ uint32_t scr[128];
+  auto no = [](int) { return false; };
   if (crit == nullptr) {
     uint32_t tau, keq;
-    block_topk_threshold<kSelThreads>(C, Bg, [&](int64_t i) { return score_key(S[i]); }, rs, tau,
-                                      keq);
-    {
-      uint32_t carry = 0, eqc = 0;
-      for (int t0 = 0; t0 < C; t0 += kSelThreads) {
-        const int j = t0 + threadIdx.x;
-        const uint32_t key = j < C ? score_key(S[j]) : 0u;
-        const uint32_t ise = (j < C && key == tau) ? 1u : 0u;
-        uint32_t etot;
-        const uint32_t eincl = block_incl_scan(ise, eqscr, &etot);
-        const uint32_t erank = eqc + eincl - ise;
-        const uint32_t f = (j < C) && (key > tau || (ise && erank < keq)) ? 1u : 0u;
-        uint32_t tot;
-        const uint32_t incl = block_incl_scan(f, rs.scratch, &tot);
-        if (f) {
-          const int64_t row = base + carry + incl - 1;
-          if (row < cap) kept[row] = j;
-        }
-        carry += tot;
-        eqc += etot;
-      }
-      if (threadIdx.x == 0 && carry != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
-    }
+    auto key = [&](int64_t i) { return score_key(S[i]); };
+    block_topk_threshold<kSelThreads>(C, Bg, key, rs, tau, keq);
+    const uint32_t n = select_ordered<kSelThreads, false>(
+        C, [&](int j) { return key(j); }, no, tau, keq, kept, base, cap, nullptr, scr);
+    if (threadIdx.x == 0 && n != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
   } else {
     const float* Cn = crit + h * (int64_t)C;
     uint32_t* F = flags + h * words;
     const int64_t K1 = ((int64_t)can * Bg) / cad;
     const int64_t K2 = Bg - K1;
     uint32_t tau1, keq1;
-    block_topk_threshold<kSelThreads>(C, K1, [&](int64_t i) { return score_key(S[i]); }, rs,
-                                      tau1, keq1);
+    auto key1 = [&](int64_t i) { return score_key(S[i]); };
+    block_topk_threshold<kSelThreads>(C, K1, key1, rs, tau1, keq1);
     // stage-1 membership bits
-    {
-      uint32_t eqc = 0;
-      for (int t0 = 0; t0 < C; t0 += kSelThreads) {
-        const int j = t0 + threadIdx.x;
-        const uint32_t key = j < C ? score_key(S[j]) : 0u;
-        const uint32_t ise = (j < C && key == tau1) ? 1u : 0u;
-        uint32_t etot;
-        const uint32_t eincl = block_incl_scan(ise, eqscr, &etot);
-        const uint32_t erank = eqc + eincl - ise;
-        const bool f = (j < C) && (key > tau1 || (ise && erank < keq1));
-        const uint32_t bits = __ballot_sync(0xffffffffu, f);
-        if ((threadIdx.x & 31) == 0 && j < C) F[j >> 5] = bits;
-        eqc += etot;
-      }
-    }
-    __syncthreads();
+    select_ordered<kSelThreads, true>(C, [&](int j) { return key1(j); }, no, tau1, keq1,
+                                      nullptr, 0, 0, F, scr);
+    auto in1 = [&](int64_t i) { return ((F[i >> 5] >> (i & 31)) & 1u) != 0u; };
     auto key2 = [&](int64_t i) -> uint32_t {
-      if ((F[i >> 5] >> (i & 31)) & 1u) return 0u;
+      if (in1(i)) return 0u;
       const float kap = __fmul_rn(__fadd_rn(S[i], ceps), Cn[i]);
       return score_key(kap) + 1u;
     };
     uint32_t tau2, keq2;
     block_topk_threshold<kSelThreads>(C, K2, key2, rs, tau2, keq2);
-    uint32_t carry = 0, eqc = 0;
-    for (int t0 = 0; t0 < C; t0 += kSelThreads) {
-      const int j = t0 + threadIdx.x;
-      const bool in1 = j < C && ((F[j >> 5] >> (j & 31)) & 1u);
-      const uint32_t k2 = j < C ? key2(j) : 0u;
-      const uint32_t ise = (j < C && !in1 && k2 == tau2) ? 1u : 0u;
-      uint32_t etot;
-      const uint32_t eincl = block_incl_scan(ise, eqscr, &etot);
-      const uint32_t erank = eqc + eincl - ise;
-      const uint32_t f = (j < C) && (in1 || k2 > tau2 || (ise && erank < keq2)) ? 1u : 0u;
-      uint32_t tot;
-      const uint32_t incl = block_incl_scan(f, rs.scratch, &tot);
-      if (f) {
-        const int64_t row = base + carry + incl - 1;
-        if (row < cap) kept[row] = j;
-      }
-      carry += tot;
-      eqc += etot;
-    }
-    if (threadIdx.x == 0 && carry != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
+    const uint32_t n = select_ordered<kSelThreads, false>(
+        C, [&](int j) { return key2(j); }, [&](int j) { return in1(j); }, tau2, keq2, kept,
+        base, cap, nullptr, scr);
+    if (threadIdx.x == 0 && n != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
   }
   for (int t = threadIdx.x; t < w + reserve; t += kSelThreads) {
     const int64_t row = base + Bg + t;

@@ -106,6 +106,21 @@ __device__ __forceinline__ unsigned int block_incl_scan(unsigned int v, unsigned
   return base + x;
 }
 
+// Histogram update of one bin per lane (0xFFFFFFFF = none) with runs of equal bins in
+// adjacent lanes merged into one add (max-pooled scores come in plateaus, so equal keys
+// sit next to each other; other repeats fall back to the atomic unit).  Warps with no
+// bin skip the vote.  All 32 lanes must call it.
+__device__ __forceinline__ void hist_add_runs(uint32_t* hist, uint32_t bin) {
+  if (__ballot_sync(0xFFFFFFFFu, bin != 0xFFFFFFFFu) == 0u) return;
+  const int lane = threadIdx.x & 31;
+  const uint32_t prev = __shfl_up_sync(0xFFFFFFFFu, bin, 1);
+  const bool start = lane == 0 || prev != bin;
+  const uint32_t starts = __ballot_sync(0xFFFFFFFFu, start);
+  const uint32_t after = starts & ~((2u << lane) - 1u);   // run starts after this lane
+  const int next = after ? __ffs(after) - 1 : 32;
+  if (start && bin != 0xFFFFFFFFu) atomicAdd(&hist[bin], (uint32_t)(next - lane));
+}
+
 __host__ __device__ __forceinline__ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

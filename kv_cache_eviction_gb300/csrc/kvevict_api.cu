@@ -141,7 +141,7 @@ kv_status kv_allocate(const kv_shape* shape, const float* scores, const int64_t*
   if (!aligned16(scores) || !aligned16(budget) || !aligned16(layer_budget) ||
       !aligned16(head_budget))
     return KV_ERR_INVALID_ARG;
-  if (!shape_supported(s)) return KV_ERR_UNSUPPORTED;
+  if (!shape_supported(s) || (layer_entropy_mode && s.L > 1024)) return KV_ERR_UNSUPPORTED;
   const AllocPlan p = alloc_plan(s);
   if (ws_bytes < p.off_end) return KV_ERR_WORKSPACE;
   return cuda_status(launch_allocate(s, scores, budget, layer_entropy_mode, alpha_num, alpha_den,

@@ -36,9 +36,25 @@ __device__ void block_topk_threshold(int64_t N, int64_t K, KeyFn key_of, RadixSm
     const int nb = pass == 2 ? 1024 : 2048;
     for (int i = threadIdx.x; i < nb; i += BLOCK) sm.hist[i] = 0u;
     __syncthreads();
-    for (int64_t i = threadIdx.x; i < N; i += BLOCK) {
-      const uint32_t key = key_of(i);
-      if ((key & mask) == prefix) atomicAdd(&sm.hist[(key >> sh) & (uint32_t)(nb - 1)], 1u);
+    // equal bins in adjacent lanes are added once (see hist_add_runs)
+    // 8 keys per thread per step, all fetched before use (latency hiding); the step
+    // count is the same for every thread so the warp votes stay convergent
+    constexpr int U = 8;
+    for (int64_t base = 0; base < N; base += (int64_t)U * BLOCK) {
+      uint32_t key[U];
+      bool valid[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const int64_t i = base + (int64_t)k * BLOCK + threadIdx.x;
+        valid[k] = i < N;
+        key[k] = valid[k] ? key_of(i) : 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const uint32_t bin = (valid[k] && (key[k] & mask) == prefix)
+                                 ? (key[k] >> sh) & (uint32_t)(nb - 1) : 0xFFFFFFFFu;
+        hist_add_runs(sm.hist, bin);
+      }
     }
     __syncthreads();
     // Counts from the top bin downwards: thread t owns reversed bins [t*per, (t+1)*per).
