@@ -51,8 +51,8 @@ cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const f
 
 // ----------------------------- decode --------------------------------------
 struct DecodePlan {
-  int splits;
-  size_t off_part, off_end;
+  int64_t max_chunks;   // flat-row chunks (one CTA each) the launch may use
+  size_t off_part, off_map, off_work, off_end;
 };
 DecodePlan decode_plan(const Shape& s);
 cudaError_t launch_decode(const Shape& s, const void* q, const void* kn, const void* vn,

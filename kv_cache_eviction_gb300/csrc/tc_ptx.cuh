@@ -45,6 +45,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// As mbar_try_wait, but the thread may be suspended for up to `hint_ns` while the phase is
+// still open (fewer polling instructions competing with the warps that compute).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait built on mbar_try_wait_hint.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                uint32_t hint_ns = 2000,
+                                                uint64_t limit_ns = 1000000000ull) {
+  if (mbar_try_wait_hint(bar, parity, hint_ns)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait_hint(bar, parity, hint_ns)) {
+    if (globaltimer() - t0 > limit_ns) return false;
+  }
+  return true;
+}
 // Waits for the phase with the given parity to complete.  Gives up after `limit_ns`
 // and returns false (the caller records the timeout and unwinds).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
@@ -88,6 +113,31 @@ __device__ __forceinline__ uint64_t make_policy_evict_first() {
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Untiled bulk copy of `bytes` contiguous bytes global -> shared, completion counted on
+// `bar` in bytes.  Both addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// Orders this thread's generic-proxy shared-memory accesses before later async-proxy
+// (bulk copy / TMA) accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Programmatic dependent launch: the next kernel in the stream may start launching now /
+// wait until the previous kernel in the stream has finished and its writes are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------- tcgen05 -------------------------------------
@@ -182,6 +232,24 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Packed fp32 pair arithmetic (one instruction for two IEEE fp32 results):
+// d = a * b + c and d = a * b, element by element, round to nearest.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
+        "l"(*reinterpret_cast<const uint64_t*>(&c)));
+  return *reinterpret_cast<const float2*>(&d);
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)));
+  return *reinterpret_cast<const float2*>(&d);
 }
 
 __device__ __forceinline__ void named_bar(int id, int nthreads) {

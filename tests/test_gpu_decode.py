@@ -1,0 +1,192 @@
+"""flat_decode_attn against the oracle on hand-built flat caches.
+
+The caches are built directly (no scoring or compaction) so that the per-head lengths can
+be pushed to the cases the decode kernel has to get right: empty heads, one-row heads, heads
+longer than a whole row chunk (their partials are merged across CTAs), heads sharing a
+chunk, reserve rows exhausted, and every lane layout (16-byte slices per row of 1, 2, 4, 8,
+16 and 32) and group size 1, 2, 3, 4, 8.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import kv_cache_eviction_gb300 as kv
+import oracle as O
+
+from .kvpath import np64, workspace
+
+pytestmark = pytest.mark.gpu
+
+
+def build_cache(B, L, hkv, G, d, lens, reserve, dtype, seed):
+    """Flat cache with the given per-head lengths; rows past lens hold junk (never read)."""
+    gen = torch.Generator().manual_seed(seed)
+    H = B * L * hkv
+    lens = np.asarray(lens, dtype=np.int64)
+    assert lens.shape == (H,)
+    ext = lens + reserve
+    flat = np.concatenate([[0], np.cumsum(ext)])
+    cu = np.stack([flat[s * hkv: s * hkv + hkv + 1] for s in range(B * L)])
+    cap = int(flat[-1])
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    kf = torch.randn(cap, d, generator=gen).to(tdt)
+    vf = (torch.randn(cap, d, generator=gen) * torch.exp(0.5 * torch.randn(cap, 1, generator=gen))).to(tdt)
+    tau = torch.exp(torch.rand(B, L, hkv * G, 1, generator=gen) * math.log(8.0)) * 0.5
+    q = (torch.randn(B, L, hkv * G, d, generator=gen) * tau).to(tdt)
+    kn = torch.randn(B, L, hkv, d, generator=gen).to(tdt)
+    vn = torch.randn(B, L, hkv, d, generator=gen).to(tdt)
+    return dict(kf=kf, vf=vf, q=q, kn=kn, vn=vn, cu=torch.from_numpy(cu.copy()),
+                lens=torch.from_numpy(lens.astype(np.int32)), cap=cap)
+
+
+def oracle_decode(c, B, L, hkv, scale, append):
+    Kf, Vf = np64(c["kf"]), np64(c["vf"])
+    lens = c["lens"].numpy().astype(np.int64).reshape(B, L, hkv)
+    cu = c["cu"].numpy().reshape(B, L, hkv + 1)
+    outs = np.zeros(tuple(c["q"].shape))
+    new_lens = lens.copy()
+    for b in range(B):
+        for l in range(L):
+            kn = np64(c["kn"][b, l]) if append else None
+            vn = np64(c["vn"][b, l]) if append else None
+            o, Kf2, Vf2, ln = _flat_decode_partial(np64(c["q"][b, l]), Kf, Vf, cu[b, l], lens[b, l],
+                                                   scale, kn, vn)
+            outs[b, l] = o
+            new_lens[b, l] = ln
+            Kf, Vf = Kf2, Vf2
+    return outs, new_lens
+
+
+def _flat_decode_partial(q, Kf, Vf, cu, lens, scale, kn, vn):
+    """The oracle's decode step, with the append skipped for heads that have no reserve row."""
+    if kn is None:
+        return O.flat_decode(q, Kf, Vf, cu, lens, scale)
+    hkv = len(lens)
+    ok = cu[:-1] + lens < cu[1:]
+    Kf = Kf.copy()
+    Vf = Vf.copy()
+    lens = lens.copy()
+    for g in range(hkv):
+        if ok[g]:
+            Kf[cu[g] + lens[g]] = kn[g]
+            Vf[cu[g] + lens[g]] = vn[g]
+            lens[g] += 1
+    o, _, _, _ = O.flat_decode(q, Kf, Vf, cu, lens, scale)
+    return o, Kf, Vf, lens
+
+
+def check(c, B, L, hkv, G, d, dtype, append, expect_code=0):
+    dev = "cuda"
+    shape = kv.KvShape.of(batch=B, layers=L, hq=hkv * G, hkv=hkv, d=d, n=100000, w=1, pool=1,
+                          dtype=dtype)
+    scale = 1.0 / math.sqrt(d)
+    ref, ref_lens = oracle_decode(c, B, L, hkv, scale, append)
+    kf, vf = c["kf"].to(dev), c["vf"].to(dev)
+    cu, lens = c["cu"].to(dev), c["lens"].to(dev)
+    q = c["q"].to(dev)
+    out = torch.full_like(q, float("nan"))
+    ws = workspace(kv.KV_OP_DECODE, shape)
+    kn = c["kn"].to(dev) if append else None
+    vn = c["vn"].to(dev) if append else None
+    kv.flat_decode_attn(shape, q, kn, vn, kf, vf, cu, lens, scale, out, ws)
+    code = kv.kv_check_device_status(ws)
+    assert code == expect_code
+    got = np64(out)
+    assert np.isfinite(got).all()
+    if dtype == "bf16":
+        tol = 1e-2 + 2.0 ** -8 * np.abs(ref)      # fp32 accumulation, bf16 output rounding
+    else:
+        tol = 1e-4 + 1e-4 * np.abs(ref)
+    err = np.abs(got - ref)
+    assert (err <= tol).all(), "max err %g at %s" % (err.max(), np.unravel_index(err.argmax(), err.shape))
+    np.testing.assert_array_equal(lens.cpu().numpy().reshape(B, L, hkv), ref_lens)
+    if append:
+        # the appended rows are exact copies of k_new / v_new
+        cu_h = c["cu"].numpy()
+        l0 = c["lens"].numpy().reshape(B, L, hkv)
+        for b in range(B):
+            for l in range(L):
+                for g in range(hkv):
+                    r = cu_h[b * L + l, g] + l0[b, l, g]
+                    if r < cu_h[b * L + l, g + 1]:
+                        assert torch.equal(kf[r].cpu(), c["kn"][b, l, g])
+                        assert torch.equal(vf[r].cpu(), c["vn"][b, l, g])
+
+
+CASES = [
+    # (dtype, d, G, hkv) -- slices per row: bf16 d/8, f32 d/4
+    ("bf16", 128, 4, 4),    # 16 slices, transposed reduction, G = 4
+    ("bf16", 128, 8, 2),    # 16 slices, transposed reduction, G = 8
+    ("f32", 64, 4, 2),      # 16 slices, fp32
+    ("bf16", 64, 3, 2),     # 8 slices, butterfly reduction, G = 3 padded to 4
+    ("f32", 32, 1, 4),      # 8 slices, G = 1
+    ("bf16", 8, 2, 3),      # 1 slice per row
+    ("f32", 128, 2, 2),     # 32 slices per row
+    ("bf16", 96, 4, 2),     # 12 slices: lanes 12..15 of each row idle
+]
+
+
+@pytest.mark.parametrize("dtype,d,G,hkv", CASES)
+@pytest.mark.parametrize("append", [True, False])
+def test_decode_uneven_heads(dtype, d, G, hkv, append):
+    B, L = 2, 2
+    H = B * L * hkv
+    rng = np.random.default_rng(d * 31 + G * 7 + hkv + int(append))
+    # heads of 0 and 1 rows, short heads, and heads longer than any row chunk
+    base = [0, 1, 3, 5000, 17, 1200, 64, 2]
+    lens = np.array([base[i % len(base)] for i in range(H)], dtype=np.int64)
+    lens = np.where(rng.random(H) < 0.3, rng.integers(0, 300, H), lens)
+    c = build_cache(B, L, hkv, G, d, lens, reserve=3, dtype=dtype, seed=int(rng.integers(1 << 30)))
+    check(c, B, L, hkv, G, d, dtype, append)
+
+
+def test_decode_no_reserve_left():
+    """Heads with no reserve row skip the append (device check 3) and attend without it."""
+    B, L, hkv, G, d = 1, 2, 4, 4, 128
+    lens = np.array([10, 700, 0, 33, 5, 6, 7, 4000])
+    c = build_cache(B, L, hkv, G, d, lens, reserve=0, dtype="bf16", seed=5)
+    check(c, B, L, hkv, G, d, "bf16", append=True, expect_code=3)
+
+
+def test_decode_many_small_heads_per_chunk():
+    """Hundreds of tiny heads: one CTA walks more than one table of heads."""
+    B, L, hkv, G, d = 1, 40, 8, 4, 128
+    rng = np.random.default_rng(9)
+    lens = rng.integers(0, 2, B * L * hkv)
+    c = build_cache(B, L, hkv, G, d, lens, reserve=1, dtype="bf16", seed=6)
+    check(c, B, L, hkv, G, d, "bf16", append=True)
+
+
+def test_decode_repeated_steps_match_single_oracle_run():
+    """Several decode steps in a row (appends accumulate) against the oracle step by step."""
+    B, L, hkv, G, d = 1, 1, 4, 4, 128
+    lens = np.array([100, 3000, 1, 0])
+    c = build_cache(B, L, hkv, G, d, lens, reserve=4, dtype="bf16", seed=7)
+    dev = "cuda"
+    shape = kv.KvShape.of(batch=B, layers=L, hq=hkv * G, hkv=hkv, d=d, n=100000, w=1, pool=1,
+                          dtype="bf16")
+    scale = 1.0 / math.sqrt(d)
+    kf, vf = c["kf"].to(dev), c["vf"].to(dev)
+    cu, lens_d = c["cu"].to(dev), c["lens"].to(dev)
+    ws = workspace(kv.KV_OP_DECODE, shape)
+    Kf, Vf = np64(c["kf"]), np64(c["vf"])
+    ln = c["lens"].numpy().astype(np.int64)
+    cu_h = c["cu"].numpy()[0]
+    gen = torch.Generator().manual_seed(11)
+    for step in range(4):
+        q = torch.randn(B, L, hkv * G, d, generator=gen).to(torch.bfloat16)
+        kn = torch.randn(B, L, hkv, d, generator=gen).to(torch.bfloat16)
+        vn = torch.randn(B, L, hkv, d, generator=gen).to(torch.bfloat16)
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+        kv.flat_decode_attn(shape, q.to(dev), kn.to(dev), vn.to(dev), kf, vf, cu, lens_d, scale,
+                            out, ws)
+        assert kv.kv_check_device_status(ws) == 0
+        ref, Kf, Vf, ln = O.flat_decode(np64(q[0, 0]), Kf, Vf, cu_h, ln, scale, np64(kn[0, 0]),
+                                        np64(vn[0, 0]))
+        got = np64(out[0, 0])
+        assert (np.abs(got - ref) <= 1e-2 + 2.0 ** -8 * np.abs(ref)).all(), step
+    np.testing.assert_array_equal(lens_d.cpu().numpy(), ln)
