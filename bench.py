@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--decode-steps", type=int, default=-1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode-large", action="store_true",
+                    help="skip the decode-only measurement on the large flat cache")
     return ap.parse_args()
 
 
@@ -60,6 +62,39 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "score_tc_kernel_traffic.txt")
+TRAFFIC_SOURCES = ("kv_cache_eviction_gb300/csrc/score_tc.cu",
+                   "kv_cache_eviction_gb300/csrc/tc_ptx.cuh")
+
+
+def score_kernel_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def read_traffic(workload: str):
+    """DRAM bytes of one score_tc_kernel launch of `workload` from the committed ncu
+    summary, or None when there is none or the kernel's source changed since."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256") != score_kernel_sha():
+            return None
+        if kv.get("workload") != workload:
+            return None
+        return int(kv["bytes_per_launch"])
+    except Exception:
+        return None
 
 
 def read_peaks():
@@ -226,6 +261,42 @@ def algorithmic_bytes(wl, B, L, head_budget_total_rows, decode_rows):
     return {"score": score, "allocate": allocate, "compact": compact, "decode": decode}
 
 
+def decode_large(kv, W, dev, stream, flush, args):
+    """flat_decode_attn alone on a flat cache of the batch-4, 32-layer, 32K-context
+    Llama-3.1-8B-shaped set (1024 rows per KV head on average, log-normal spread, 256
+    reserve rows), L2 flushed before each step."""
+    import torch
+    wl = W.WORKLOADS["llama8b_32k_b4"]
+    fc = W.make_flat_cache(wl, mean_len=1024, sigma=0.7, reserve=256, seed=0xDEC0, device=dev)
+    shape = kv.KvShape.from_workload(wl)
+    wsd = torch.zeros(max(kv.kv_workspace_size(kv.KV_OP_DECODE, shape), 256), dtype=torch.uint8,
+                      device=dev)
+    out = torch.empty_like(fc["q"])
+    scale = 1.0 / math.sqrt(wl.d)
+    steps = 10
+    B, L = wl.batch, wl.layers
+    dts, byts = [], []
+    for i in range(steps + 2):
+        rows = int(fc["lens"].sum().item()) + B * L * wl.hkv     # after this step's append
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        kv.flat_decode_attn(shape, fc["q"], fc["k_new"], fc["v_new"], fc["k_flat"], fc["v_flat"],
+                            fc["cu"], fc["lens"], scale, out, wsd, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= 2:
+            dts.append(e0.elapsed_time(e1))
+            byts.append(algorithmic_bytes(wl, B, L, 0, rows)["decode"])
+    if kv.kv_check_device_status(wsd, stream):
+        raise RuntimeError("device check in the large decode")
+    gbs = sum(byts) / (sum(dts) / 1e3) / 1e9
+    return {"value": gbs, "unit": "GB/s", "steps": steps,
+            "ms_per_step": statistics.mean(dts), "bytes_per_step": statistics.mean(byts),
+            "cache": "llama8b_32k_b4 shape: 1024 KV heads, 1024 rows each on average "
+                     "(log-normal, sigma 0.7), 256 reserve rows; L2 flushed before each step"}
+
+
 def run_ours(args):
     import torch
     import kv_cache_eviction_gb300 as kv
@@ -382,6 +453,8 @@ def run_ours(args):
         raise RuntimeError("device check in decode")
     peak, peak_kind = read_peaks()
     dec_gbs = sum(dbytes) / (sum(dts) / 1e3) / 1e9
+    dec_large = (decode_large(kv, W, dev, stream, flush, args)
+                 if rank == 0 and not args.no_decode_large else None)
 
     # -------------------- roofline of the dominant stage --------------------
     ab = algorithmic_bytes(wl, B, L, hb_rows, lens0)
@@ -389,7 +462,8 @@ def run_ours(args):
     achieved = ab[dom] / (stage_ms[dom] / 1e3) / 1e9
     roofline = {"kernel": "kv_score (window scoring)" if dom == "score" else dom,
                 "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                "frac": achieved / peak, "peak_kind": peak_kind,
+                "traffic": read_traffic(wl.name) if dom == "score" else None,
                 "algorithmic_bytes_per_launch": ab[dom]}
 
     # -------------------- end to end through host buffers --------------------
@@ -483,6 +557,8 @@ def run_ours(args):
                             "peak": peak, "steps": nd, "ms_per_step": statistics.mean(dts),
                             "bytes_per_step": statistics.mean(dbytes),
                             "l2": "flushed before each step"},
+            "decode_attn_large": dict(dec_large, frac=dec_large["value"] / peak)
+            if dec_large else None,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,

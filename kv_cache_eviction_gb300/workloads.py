@@ -261,3 +261,37 @@ def make_decode_batch(wl: Workload, step: int, tau: torch.Tensor, device="cpu",
             kn[bi, li] = st["k_new"]
             vn[bi, li] = st["v_new"]
     return {"q": q, "k_new": kn, "v_new": vn}
+
+
+def make_flat_cache(wl: Workload, mean_len: int, sigma: float, reserve: int, seed: int,
+                    device="cpu") -> dict:
+    """A flat cache laid out as kv_compact writes it, for decode-only measurements.
+
+    Per-head lengths are log-normal (sigma) around mean_len, at least wl.w (the window
+    rows every head keeps), each head followed by `reserve` free rows; K, V, q, k_new and
+    v_new are N(0, 1) in the storage dtype.  Returns cu [B][L][Hkv+1], lens [B][L][Hkv],
+    k_flat / v_flat [cap][d], q [B][L][Hq][d], k_new / v_new [B][L][Hkv][d] and cap.
+    """
+    dev = torch.device(device)
+    g = _gen(torch.device("cpu"), seed)
+    B, L, hkv = wl.batch, wl.layers, wl.hkv
+    H = B * L * hkv
+    f = torch.exp(torch.randn(H, generator=g) * sigma)
+    lens = (f / f.mean() * mean_len).round().clamp(min=wl.w).to(torch.int64)
+    ext = lens + reserve
+    flat = torch.cat([torch.zeros(1, dtype=torch.int64), ext.cumsum(0)])
+    cu = torch.stack([flat[s * hkv: s * hkv + hkv + 1] for s in range(B * L)])
+    cap = int(flat[-1])
+    dt = wl.torch_dtype
+    gd = _gen(dev, seed + 1)
+    out = {
+        "cu": cu.reshape(B, L, hkv + 1).to(dev),
+        "lens": lens.to(torch.int32).reshape(B, L, hkv).to(dev),
+        "k_flat": torch.randn(cap, wl.d, generator=gd, device=dev).to(dt),
+        "v_flat": torch.randn(cap, wl.d, generator=gd, device=dev).to(dt),
+        "q": torch.randn(B, L, wl.hq, wl.d, generator=gd, device=dev).to(dt),
+        "k_new": torch.randn(B, L, hkv, wl.d, generator=gd, device=dev).to(dt),
+        "v_new": torch.randn(B, L, hkv, wl.d, generator=gd, device=dev).to(dt),
+        "cap": cap,
+    }
+    return out
