@@ -11,6 +11,9 @@
 // logits of the candidate keys, forms exp(z - lse), averages over the window
 // rows, pools and reduces over the query-head group.  Logits are kept in the
 // log2 domain: z2 = (q.k) * scale * log2(e).
+#include <cstdlib>
+#include <cstring>
+
 #include "kv_internal.cuh"
 
 namespace kv {
@@ -243,7 +246,13 @@ cudaError_t launch_score_tc(const Shape& s, int mode, int group, const void* q_w
                             cudaStream_t st);
 bool crit_tc_supported(const Shape& s, int D);
 cudaError_t launch_crit_tc(const Shape& s, const void* v, const void* w_o, int D, float* crit,
-                           cudaStream_t st);
+                           char* ws, cudaStream_t st);
+
+// KVEVICT_SCORE_PATH=simt forces the CUDA-core kernels (tests compare the two paths).
+static bool simt_forced() {
+  const char* e = std::getenv("KVEVICT_SCORE_PATH");
+  return e != nullptr && std::strcmp(e, "simt") == 0;
+}
 
 ScorePlan score_plan(const Shape& s, int mode) {
   ScorePlan p{};
@@ -340,7 +349,8 @@ cudaError_t launch_score(const Shape& s, int mode, int group, const void* q_win,
                                    (const float*)v, scores, ws, p, st);
   }
   if (e != cudaSuccess || mode != KV_SCORE_CRITICAL) return e;
-  if (crit_tc_supported(s, D)) return launch_crit_tc(s, v, w_o, D, crit, st);
+  if (crit_tc_supported(s, D) && !simt_forced())
+    return launch_crit_tc(s, v, w_o, D, crit, ws, st);
   if (s.dtype == KV_BF16)
     return launch_crit_simt_t<__nv_bfloat16>(s, (const __nv_bfloat16*)v,
                                              (const __nv_bfloat16*)w_o, D, crit, st);

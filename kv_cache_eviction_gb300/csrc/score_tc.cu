@@ -878,10 +878,4 @@ cudaError_t launch_score_tc(const Shape& s, int mode, int group, const void* q_w
   return cudaGetLastError();
 }
 
-// CriticalKV V*W_O on tcgen05: not built yet, the CUDA-core kernel runs.
-bool crit_tc_supported(const Shape&, int) { return false; }
-cudaError_t launch_crit_tc(const Shape&, const void*, const void*, int, float*, cudaStream_t) {
-  return cudaErrorNotSupported;
-}
-
 }  // namespace kv

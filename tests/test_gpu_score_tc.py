@@ -2,6 +2,7 @@
 CUDA-core path on the same inputs.  Shapes cover ragged n, every supported w, several
 units per launch (the P1/P2 interleave and the cross-CTA LSE publication) and LAVa."""
 import os
+import zlib
 
 import numpy as np
 import pytest
@@ -56,7 +57,7 @@ def test_tc_scores_match_oracle(case):
     name, hq, hkv, w, n, B, L, mode, group, pool = case
     wl = W.Workload(name=name, batch=B, layers=L, hq=hq, hkv=hkv, d=128, n=n, w=w, pool=pool,
                     dtype="bf16", temp=(0.5, 16.0), v_lognormal=0.5 if mode == "lava" else 0.0,
-                    mode=mode, group=group, head_budget_tokens=8, seed=hash(name) & 0xFFFF)
+                    mode=mode, group=group, head_budget_tokens=8, seed=zlib.crc32(name.encode()) & 0xFFFF)
     shape = kv.KvShape.from_workload(wl)
     inp = W.make_batch(wl, device="cuda")
     s_tc, launches_tc = score_with("tc", wl, shape, inp)
@@ -72,3 +73,44 @@ def test_tc_scores_match_oracle(case):
             assert_scores_close(s_tc[b, l].astype(np.float64), ref, what="tc b%d l%d" % (b, l))
             assert_scores_close(s_simt[b, l].astype(np.float64), ref,
                                 what="simt b%d l%d" % (b, l))
+
+
+CRIT_CASES = [
+    # name, n, D, batch, layers, hkv: ragged key tails, D not a multiple of the 128-column
+    # tile, several (layer, KV head) output blocks
+    ("crit_ragged", 1000 + 7, 1000, 2, 2, 2),
+    ("crit_d4096", 600, 4096, 1, 1, 8),
+    ("crit_tiny_c", 40, 136, 1, 3, 2),
+]
+
+
+@pytest.mark.parametrize("case", CRIT_CASES, ids=[c[0] for c in CRIT_CASES])
+def test_crit_norm_tc_matches_oracle(case):
+    """||(V W_O)_j||_1 on the tensor cores (one MN-major W_O operand per (layer, KV head))
+    against the oracle's fp64 product, and the CUDA-core kernel on the same inputs."""
+    import oracle as O
+    name, n, D, B, L, hkv = case
+    wl = W.Workload(name=name, batch=B, layers=L, hq=4 * hkv, hkv=hkv, d=128, n=n, w=32, pool=7,
+                    dtype="bf16", temp=(0.5, 16.0), mode="critical", head_budget_frac=0.4,
+                    model_dim=D, seed=zlib.crc32(name.encode()) & 0xFFFF)
+    shape = kv.KvShape.from_workload(wl)
+    inp = W.make_batch(wl, device="cuda")
+    crits = {}
+    for path in ("tc", "simt"):
+        old = os.environ.get("KVEVICT_SCORE_PATH")
+        os.environ["KVEVICT_SCORE_PATH"] = path
+        try:
+            _, c = run_score(wl, shape, inp)
+            crits[path] = c.cpu().numpy()
+        finally:
+            if old is None:
+                del os.environ["KVEVICT_SCORE_PATH"]
+            else:
+                os.environ["KVEVICT_SCORE_PATH"] = old
+    C = n - wl.w
+    for b in range(B):
+        for l in range(L):
+            ref = O.critical_row_norm(np64(inp["v"][b, l]), np64(inp["w_o"][l]), C)
+            for path, c in crits.items():
+                assert_scores_close(c[b, l].astype(np.float64), ref,
+                                    what="crit %s b%d l%d" % (path, b, l))
