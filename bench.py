@@ -57,6 +57,29 @@ def parse_args():
     return ap.parse_args()
 
 
+def rank_sequences(rank: int, batch: int) -> range:
+    """The sequences rank `rank` evicts: each rank owns `batch` sequences of its own (weak
+    scaling, no data-path exchange)."""
+    return range(rank * batch, (rank + 1) * batch)
+
+
+def max_over_ranks(t: float, device=None) -> float:
+    """The slowest rank's time (all ranks get it); the local time when not distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return t
+    tt = torch.tensor([t], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def aggregate_value(world: int, batch: int, n: int, layers: int, ms: float) -> float:
+    """Whole-job eviction-pass prefix tokens/s per layer: every rank's batch * n * L prefix
+    tokens through one layer's eviction in (slowest rank's step time / L)."""
+    return world * batch * n * layers / (ms / 1e3)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -95,6 +118,16 @@ def read_traffic(workload: str):
         return int(kv["bytes_per_launch"])
     except Exception:
         return None
+
+
+def read_tensor_peak():
+    """Sustained dense bf16 TFLOP/s (the norm kernel runs inside a long step)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops_sustained"]), "measured (sustained)"
+    except Exception:
+        return 1700.0, "fallback (sustained)"
 
 
 def read_peaks():
@@ -318,7 +351,7 @@ def run_ours(args):
     if args.layers > 0:
         wl = wl.with_(layers=args.layers)
     B, L = wl.batch, wl.layers
-    seqs = range(rank * B, (rank + 1) * B)
+    seqs = rank_sequences(rank, B)
     shape = kv.KvShape.from_workload(wl)
     C = wl.n - wl.w
     mode = {"ada": kv.KV_SCORE_ADA, "lava": kv.KV_SCORE_LAVA, "critical": kv.KV_SCORE_CRITICAL}[
@@ -414,13 +447,8 @@ def run_ours(args):
     else:
         ms_per_step = statistics.mean(evs[i][0].elapsed_time(evs[i][4])
                                       for i in range(args.steps))
-    t_local = ms_per_step
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([t_local], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_local = float(tt.item())
-    value = world * B * wl.n * L / (t_local / 1e3)
+    t_local = max_over_ranks(ms_per_step, dev)
+    value = aggregate_value(world, B, wl.n, L, t_local)
 
     for w_ in (w_s, w_a, w_c, w_d):
         code = kv.kv_check_device_status(w_, stream)
@@ -465,6 +493,35 @@ def run_ours(args):
                 "frac": achieved / peak, "peak_kind": peak_kind,
                 "traffic": read_traffic(wl.name) if dom == "score" else None,
                 "algorithmic_bytes_per_launch": ab[dom]}
+    crit_norm = None
+    if wl.mode == "critical":
+        # The CriticalKV norm (tensor-bound) is the dominant kernel of kv_score here: its
+        # time is kv_score in CriticalKV mode minus kv_score in Ada mode on the same inputs.
+        def t_score(m, reps=3):
+            ts = []
+            for _ in range(reps + 1):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                kv.kv_score(shape, m, group, inp["q_win"], inp["k"], inp["v"],
+                            inp["w_o"] if m == kv.KV_SCORE_CRITICAL else None, wl.model_dim,
+                            scores, crit if m == kv.KV_SCORE_CRITICAL else None, w_s, stream)
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                ts.append(e0.elapsed_time(e1))
+            return statistics.median(ts[1:])
+        t_crit, t_ada = t_score(kv.KV_SCORE_CRITICAL), t_score(kv.KV_SCORE_ADA)
+        flops = 2.0 * B * L * wl.hkv * C * wl.d * wl.model_dim
+        crit_ms = max(t_crit - t_ada, 1e-6)
+        tf = flops / (crit_ms / 1e3) / 1e12
+        tpeak, tkind = read_tensor_peak()
+        crit_norm = {"kernel": "crit_tc_kernel (||(V W_O)_j||_1 on tcgen05)", "ms": crit_ms,
+                     "flops": flops, "achieved": tf, "unit": "TFLOP/s", "peak": tpeak,
+                     "frac": tf / tpeak, "peak_kind": tkind,
+                     "how": "kv_score(CRITICAL) - kv_score(ADA) on the same inputs"}
+        roofline = {"kernel": crit_norm["kernel"], "bound": "tensor", "achieved": tf,
+                    "peak": tpeak, "unit": "TFLOP/s", "frac": tf / tpeak, "peak_kind": tkind,
+                    "traffic": None, "flops_per_launch": flops,
+                    "how": crit_norm["how"]}
 
     # -------------------- end to end through host buffers --------------------
     e2e = None
@@ -509,13 +566,8 @@ def run_ours(args):
             e1.record(stream)
             torch.cuda.synchronize(dev)
             e2e_ms.append(e0.elapsed_time(e1))
-        t_e2e = statistics.mean(e2e_ms)
-        if world > 1:
-            import torch.distributed as dist
-            tt = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            t_e2e = float(tt.item())
-        e2e = {"value": world * B * wl.n * L / (t_e2e / 1e3), "unit": UNIT,
+        t_e2e = max_over_ranks(statistics.mean(e2e_ms), dev)
+        e2e = {"value": aggregate_value(world, B, wl.n, L, t_e2e), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e,
                "steps": args.e2e_steps}
         del host
@@ -560,6 +612,7 @@ def run_ours(args):
             "decode_attn_large": dict(dec_large, frac=dec_large["value"] / peak)
             if dec_large else None,
             "roofline": roofline,
+            "crit_norm": crit_norm,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,
