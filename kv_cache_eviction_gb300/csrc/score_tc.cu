@@ -20,12 +20,13 @@
 // score_tc_fixup from per-range halo copies of the window means.
 //
 // LAVa: during P2 items (K then comes from L2) the producer also puts the V tiles of the
-// range into the ring; warp 2 folds them into max ||V[k]||_1 of the unit.  P2 writes
-// unscaled scores and the fix-up kernel applies the factor after the kernel, so nothing
-// here waits for V.
+// range into the ring; the epilogue warps fold each one into max ||V[k]||_1 of the unit
+// right after the K tile it follows (4 threads per row, so a V tile costs each thread four
+// 16-byte loads).  P2 writes unscaled scores and the fix-up kernel applies the factor
+// after the kernel, so nothing here waits for V.
 //
 // Roles (640 threads): warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM
-// allocator and LAVa V streamer, warp 3 = LSE agent, warps 4..19 = epilogue (TMEM lane
+// allocator, warp 3 = LSE agent, warps 4..19 = epilogue (TMEM lane
 // quadrant = warp % 4, column quarter = (warp - 4) / 4).  Every wait is bounded; on a timeout the CTA records DEV_WAIT_TIMEOUT,
 // unwinds, waits (bounded) for its copies and MMAs in flight and frees its TMEM.
 #include <cudaTypedefs.h>
@@ -53,7 +54,7 @@ constexpr int kTBuf = 4;                           // TMEM accumulators of 128 f
 constexpr uint32_t kTmemCols = 128 * kTBuf;
 constexpr int kMaxR = 15;                          // pool / 2
 #ifndef KV_TC_LAG
-#define KV_TC_LAG 2
+#define KV_TC_LAG 1
 #endif
 
 constexpr uint32_t kOffQ = 0;
@@ -71,6 +72,7 @@ struct __align__(8) Tail {
   uint64_t qfull[2], qempty[2];
   uint64_t tfull[kTBuf], tempty[kTBuf];
   uint64_t drain;
+  uint32_t vcnt[kStages];  // epilogue warps done with the V entry in each stage
   int64_t pf_unit;      // unit whose -lse already sits in the nlse buffer (-1: none)
   uint32_t tmem_base;
   int abort_flag;
@@ -94,6 +96,33 @@ struct TcParams {
   float* scores;     // [units][C]
   WsHeader* hdr;
 };
+
+// L1 norm of one row of a V tile in the ring (128 rows x 128 bf16, two 128-byte swizzled
+// boxes).  Four threads share a row, 32 elements each; a row's sum does not depend on the
+// order of its 16-byte pieces, so each thread reads physical pieces, rotated so that the
+// 8 threads of a shared-memory phase (2 rows x 4 parts) hit 8 different bank groups.
+__device__ __forceinline__ float vrow_l1(const uint8_t* base, int et) {
+  const int row = et >> 2, part = et & 3;
+  const int rot = 2 * (part >> 1) + (row & 1);
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int pc = 4 * part + ((i + rot) & 3);
+    const uint4 x = *reinterpret_cast<const uint4*>(base + (pc >> 3) * kBoxBytes + row * 128 +
+                                                    (pc & 7) * 16);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h[e]);
+      a0 += fabsf(f.x);
+      a1 += fabsf(f.y);
+    }
+  }
+  float sum = a0 + a1;
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  return sum;
+}
 
 // P2 of the k-th unit follows P1 of the (k + kLag)-th: P1(0..a-1), then P1(k), P2(k-a) pairs,
 // then the last P2s, with a = min(kLag, m).  kind 1 = P1, 2 = P2.
@@ -141,6 +170,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       mbar_init(&tl->tempty[b], kEpiWarps);
     }
     mbar_init(&tl->drain, 1);
+    for (int st = 0; st < kStages; ++st) tl->vcnt[st] = 0;
     tl->abort_flag = 0;
     tl->last_flag = 0;
     tl->pf_unit = -1;
@@ -280,71 +310,6 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       mma_commit(&tl->drain);
       mbar_wait(&tl->drain, 0, 20000000ull);
     }
-  } else if (warp == 2) {
-    // ------------------------------ LAVa V-bar --------------------------------
-    // Consumes the V entries the producer puts in the ring during P2 items (K comes from
-    // L2 then, so the two passes share DRAM evenly), folds max_k ||V[k]||_1 of the unit
-    // into vbar[u] and frees each entry with one arrive.  Nothing waits for it: the
-    // fix-up kernel applies the factor after this kernel.
-    if (p.vbar != nullptr) {
-      uint32_t g = 0;
-      uint32_t vuse[kStages] = {};      // V tiles consumed per stage (phases of fullv[s])
-      bool ok = true;
-      for (int64_t i = 0; i < n_items && ok; ++i) {
-        int kind;
-        int64_t k;
-        item_of(i, m, kind, k);
-        const int te = kind == 1 ? t1 : t1c;
-        if (t0 >= te) continue;
-        if (kind == 1) { g += te - t0; continue; }
-        float vmax = 0.f;
-        for (int t = t0; t < te && ok; ++t) {
-          ++g;   // the K entry of tile t
-          const int nv = t + 1 < te ? 1 : t1 - t;
-          for (int j = 0; j < nv; ++j, ++g) {
-            const int sv = g % kStages;
-            if (!mbar_wait(&tl->fullv[sv], vuse[sv]++ & 1) || *abort_flag) { ok = false; break; }
-            const uint8_t* base = smem + kOffK + sv * kTileBytes;
-            // lane l sums rows 4l..4l+3; the 16-byte pieces of a row are visited in a
-            // lane-rotated order (a row's sum does not depend on where the swizzle put them)
-#pragma unroll 1
-            for (int rr = 0; rr < 4; ++rr) {
-              const int row = 4 * lane + rr;
-              float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-              for (int bx = 0; bx < 2; ++bx) {
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                  const int jp = (jj + lane) & 7;
-                  const uint4 x =
-                      *reinterpret_cast<const uint4*>(base + bx * kBoxBytes + row * 128 + jp * 16);
-                  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    const float2 f = __bfloat1622float2(h[e]);
-                    a0 += fabsf(f.x);
-                    a1 += fabsf(f.y);
-                  }
-                }
-              }
-              vmax = fmaxf(vmax, a0 + a1);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tl->empty[sv]);
-          }
-        }
-        if (!ok) break;
-        const float wm = warp_max(vmax);
-        if (lane == 0 && wm > 0.f) {
-          const int64_t u = group + k * p.NG;
-          atomicMax(reinterpret_cast<unsigned int*>(p.vbar) + u, __float_as_uint(wm));
-        }
-      }
-      if (!ok && lane == 0) {
-        raise_dev(p.hdr, DEV_WAIT_TIMEOUT, 6);
-        *abort_flag = 1;
-      }
-    }
   } else if (warp == 3) {
     // ------------------------------ LSE agent ---------------------------------
     // For the units it is assigned to (ncomb CTAs per unit, rotating), this warp waits
@@ -432,6 +397,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     const int r = p.r, C = p.C, G = p.G;
     const float c2 = p.c2;
     uint32_t g = 0;     // TMEM accumulator counter (K tiles)
+    uint32_t gr = 0;    // ring entries (K and V), as the producer counts them
+    uint32_t vuse[kStages] = {};   // V entries consumed per stage (phases of fullv[s])
+    float vmax = 0.f;   // LAVa: max row L1 of V over this CTA's range of the unit
     bool ok = true;
     for (int64_t i = 0; i < n_items && ok; ++i) {
       int kind;
@@ -492,18 +460,24 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             for (int c = 0; c < 32; ++c)
               if (key0 + c > limit) v[c] = -INFINITY;
           }
-          float mx[8];
+          float mx[11];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) mx[j] = fmaxf(fmaxf(v[j], v[j + 8]), fmaxf(v[j + 16], v[j + 24]));
-#pragma unroll
-          for (int j = 0; j < 4; ++j) mx[j] = fmaxf(mx[j], mx[j + 4]);
-          const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
+          for (int j = 0; j < 10; ++j) mx[j] = max3f(v[3 * j], v[3 * j + 1], v[3 * j + 2]);
+          mx[10] = fmaxf(v[30], v[31]);
+          const float tmax = fmaxf(max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), max3f(mx[6], mx[7], mx[8])), fmaxf(mx[9], mx[10])) * c2;
           const float mn = fmaxf(m_run, tmax);
           if (mn != -INFINITY) {
-            float sa[4] = {0.f, 0.f, 0.f, 0.f};
+            const float2 sc = make_float2(c2, c2), sh = make_float2(-mn, -mn);
+            float2 sa0 = make_float2(0.f, 0.f), sa1 = sa0;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) sa[c & 3] += ex2(fmaf(v[c], c2, -mn));
-            l_run = l_run * ex2(m_run - mn) + ((sa[0] + sa[1]) + (sa[2] + sa[3]));
+            for (int c = 0; c < 32; c += 4) {
+              const float2 x0 = ffma2(make_float2(v[c], v[c + 1]), sc, sh);
+              const float2 x1 = ffma2(make_float2(v[c + 2], v[c + 3]), sc, sh);
+              sa0 = fadd2(sa0, make_float2(ex2(x0.x), ex2(x0.y)));
+              sa1 = fadd2(sa1, make_float2(ex2(x1.x), ex2(x1.y)));
+            }
+            const float2 st = fadd2(sa0, sa1);
+            l_run = l_run * ex2(m_run - mn) + (st.x + st.y);
             m_run = mn;
           }
         } else {
@@ -511,9 +485,21 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
           float acc[SL];
 #pragma unroll
           for (int j = 0; j < SL; ++j) acc[j] = 0.f;
-          const float* nl = nlse + qc * 32;
+          const float2* nl2 = reinterpret_cast<const float2*>(nlse + qc * 32);
+          const float2 sc = make_float2(c2, c2);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) acc[c / CPS] += ex2(fmaf(__uint_as_float(ra[c]), c2, nl[c]));
+          for (int j = 0; j < SL; ++j) {
+            float2 s0 = make_float2(0.f, 0.f), s1 = s0;
+#pragma unroll
+            for (int c = j * CPS; c < (j + 1) * CPS; c += 4) {
+              const float2 x0 = ffma2(make_float2(__uint_as_float(ra[c]), __uint_as_float(ra[c + 1])), sc, nl2[c / 2]);
+              const float2 x1 = ffma2(make_float2(__uint_as_float(ra[c + 2]), __uint_as_float(ra[c + 3])), sc, nl2[c / 2 + 1]);
+              s0 = fadd2(s0, make_float2(ex2(x0.x), ex2(x0.y)));
+              s1 = fadd2(s1, make_float2(ex2(x1.x), ex2(x1.y)));
+            }
+            const float2 st = fadd2(s0, s1);
+            acc[j] += st.x + st.y;
+          }
           const int kl = (t - t0) * 128 + row;
 #pragma unroll
           for (int j = 0; j < SL; ++j)
@@ -529,8 +515,31 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             pf_u = -1;
           }
         }
+        ++gr;                                    // the K entry of tile t
+        if (kind == 2 && p.vbar != nullptr) {
+          // the V rows that follow this K tile (after the last candidate tile, also those of
+          // the window-only tiles of the range); the last warp done releases the stage
+          const int nv = t + 1 < te ? 1 : t1 - t;
+          for (int j = 0; j < nv; ++j, ++gr) {
+            const int sv = gr % kStages;
+            if (!mbar_wait(&tl->fullv[sv], vuse[sv]++ & 1) || *abort_flag) { ok = false; break; }
+            vmax = fmaxf(vmax, vrow_l1(smem + kOffK + sv * kTileBytes, et));
+            __syncwarp();
+            if (lane == 0 && atomicAdd(&tl->vcnt[sv], 1u) == (uint32_t)(kEpiWarps - 1)) {
+              tl->vcnt[sv] = 0;
+              mbar_arrive(&tl->empty[sv]);
+            }
+          }
+          if (!ok) break;
+        }
       }
       if (!ok) break;
+      if (kind == 2 && p.vbar != nullptr) {
+        const float wm = warp_max(vmax);
+        if (lane == 0 && wm > 0.f)
+          atomicMax(reinterpret_cast<unsigned int*>(p.vbar) + u, __float_as_uint(wm));
+        vmax = 0.f;
+      }
       if (kind == 1) {
         part_s[qc * 128 + row] = make_float2(m_run, l_run);
         named_bar(1, kEpiThreads);
