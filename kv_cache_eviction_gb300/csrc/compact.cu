@@ -12,7 +12,8 @@ namespace kv {
 
 namespace {
 constexpr int kScanThreads = 1024;
-constexpr int kSelThreads = 1024;
+constexpr int kSelThreads = 256;
+constexpr int kSelCl = 8;       // CTAs (one cluster) per head
 constexpr int kGatherThreads = 256;
 }
 
@@ -76,115 +77,34 @@ compact_offsets(const int32_t* __restrict__ head_budget, int64_t H, int Hkv, int
 }
 
 
-// Ordered selection of positions j in [0, C): keep(j) = forced(j) || key(j) > tau ||
-// (key(j) == tau && rank of j among the tau-equal keys < keq), i.e. the (key desc,
-// position asc) order.  Kept positions go, ascending, to kept[base + r] (rows >= cap are
-// skipped) or, with BITS, as one bit per position to bits[j / 32].  Two sweeps: per-warp
-// counts over contiguous slices, one scan of the warp totals, then each warp emits its
-// slice with ballots.  Returns the number of kept positions.  All threads must call it.
-template <int BLOCK, bool BITS, typename KeyFn, typename ForcedFn>
-__device__ uint32_t select_ordered(int C, KeyFn key, ForcedFn forced, uint32_t tau, uint32_t keq,
-                                   int32_t* kept, int64_t base, int64_t cap, uint32_t* bits,
-                                   uint32_t* scr /* 4 * 32 */) {
-  constexpr int NW = BLOCK / 32;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int per = (((C + NW - 1) / NW) + 31) & ~31;   // slice length, a multiple of 32
-  const int s0 = min(C, warp * per), s1 = min(C, s0 + per);
-  constexpr int U = 8;   // 32-key steps fetched per batch (latency hiding)
-  uint32_t nkeep = 0, neq = 0;
-  for (int jb = s0; jb < s1; jb += 32 * U) {
-    uint32_t kk[U];
-    bool ff[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int j = jb + 32 * u + lane;
-      kk[u] = j < s1 ? key(j) : 0u;
-      ff[u] = j < s1 ? forced(j) : false;
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const bool in = jb + 32 * u + lane < s1;
-      nkeep += (in && (ff[u] || kk[u] > tau)) ? 1u : 0u;
-      neq += (in && !ff[u] && kk[u] == tau) ? 1u : 0u;
-    }
-  }
-  nkeep = warp_sum_u(nkeep);
-  neq = warp_sum_u(neq);
-  if (lane == 0) { scr[warp] = nkeep; scr[32 + warp] = neq; }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t eq = 0, out = 0;
-    for (int w = 0; w < NW; ++w) {
-      const uint32_t e = scr[32 + w];
-      const uint32_t take = eq >= keq ? 0u : (keq - eq < e ? keq - eq : e);
-      scr[64 + w] = eq;    // tau-equal keys before this warp's slice
-      scr[96 + w] = out;   // kept positions before this warp's slice
-      out += scr[w] + take;
-      eq += e;
-    }
-    scr[0] = out;          // total (the per-warp counts are no longer needed)
-  }
-  __syncthreads();
-  uint32_t eqc = scr[64 + warp], outc = scr[96 + warp];
-  const uint32_t total = scr[0];
-  const uint32_t below = (1u << lane) - 1u;
-  for (int jb = s0; jb < s1; jb += 32 * U) {
-    uint32_t kk[U];
-    bool ff[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int j = jb + 32 * u + lane;
-      kk[u] = j < s1 ? key(j) : 0u;
-      ff[u] = j < s1 ? forced(j) : false;
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int j0 = jb + 32 * u;
-      if (j0 >= s1) break;   // uniform across the warp
-      const int j = j0 + lane;
-      const bool in = j < s1;
-      const bool iseq = in && !ff[u] && kk[u] == tau;
-      bool keep = in && (ff[u] || kk[u] > tau);
-      const uint32_t meq = __ballot_sync(0xFFFFFFFFu, iseq);
-      if (iseq && eqc + __popc(meq & below) < keq) keep = true;
-      const uint32_t mk = __ballot_sync(0xFFFFFFFFu, keep);
-      if (BITS) {
-        if (lane == 0) bits[j0 >> 5] = mk;
-      } else if (keep) {
-        const int64_t row = base + outc + __popc(mk & below);
-        if (row < cap) kept[row] = j;
-      }
-      eqc += __popc(meq);
-      outc += __popc(mk);
-    }
-  }
-  __syncthreads();   // scr is reused by the caller
-  return total;
-}
-
-// One CTA per head: threshold(s), ordered kept positions, window and reserve rows.
+// One thread-block cluster of kSelCl CTAs per head: threshold(s), ordered kept positions,
+// window and reserve rows.  CTA r of the cluster owns candidate positions
+// [r * span, (r + 1) * span), span a multiple of 32 (whole words of the stage-1 bits).
 __global__ void __launch_bounds__(kSelThreads)
 compact_select(const float* __restrict__ scores, const float* __restrict__ crit, uint32_t can,
                uint32_t cad, float ceps, const int32_t* __restrict__ lens,
                const int64_t* __restrict__ cu, int Hkv, int C, int w, int reserve,
                int32_t* __restrict__ kept, int64_t cap, uint32_t* __restrict__ flags,
                int64_t words, WsHeader* hdr) {
-  __shared__ RadixSmem rs;
-  const int64_t h = blockIdx.x;
+  __shared__ ClusterSelectSmem rs;
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = (int)cl.block_rank(), ncta = (int)cl.num_blocks();
+  const int64_t h = blockIdx.y;
   const int64_t seg = h / Hkv;
   const int g = (int)(h - seg * Hkv);
   const int64_t base = cu[seg * (Hkv + 1) + g];
   const int64_t Bg = (int64_t)lens[h] - w;   // lens was clamped to [w, n]
   const float* S = scores + h * (int64_t)C;
-  __shared__ uint32_t scr[128];
+  const int span = ((C + ncta - 1) / ncta + 31) & ~31;
+  const int p0 = min(C, rank * span), p1 = min(C, p0 + span);
   auto no = [](int) { return false; };
   if (crit == nullptr) {
     uint32_t tau, keq;
     auto key = [&](int64_t i) { return score_key(S[i]); };
-    block_topk_threshold<kSelThreads>(C, Bg, key, rs, tau, keq);
-    const uint32_t n = select_ordered<kSelThreads, false>(
-        C, [&](int j) { return key(j); }, no, tau, keq, kept, base, cap, nullptr, scr);
-    if (threadIdx.x == 0 && n != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
+    cluster_topk_threshold<kSelThreads>(p0, p1, Bg, key, rs, tau, keq);
+    const uint32_t n = cluster_select_ordered<kSelThreads, false>(
+        p0, p1, [&](int j) { return key(j); }, no, tau, keq, kept, base, cap, nullptr, rs);
+    if (rank == 0 && threadIdx.x == 0 && n != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
   } else {
     const float* Cn = crit + h * (int64_t)C;
     uint32_t* F = flags + h * words;
@@ -192,10 +112,10 @@ compact_select(const float* __restrict__ scores, const float* __restrict__ crit,
     const int64_t K2 = Bg - K1;
     uint32_t tau1, keq1;
     auto key1 = [&](int64_t i) { return score_key(S[i]); };
-    block_topk_threshold<kSelThreads>(C, K1, key1, rs, tau1, keq1);
-    // stage-1 membership bits
-    select_ordered<kSelThreads, true>(C, [&](int j) { return key1(j); }, no, tau1, keq1,
-                                      nullptr, 0, 0, F, scr);
+    cluster_topk_threshold<kSelThreads>(p0, p1, K1, key1, rs, tau1, keq1);
+    // stage-1 membership bits (each CTA writes and later reads the words of its own span)
+    cluster_select_ordered<kSelThreads, true>(p0, p1, [&](int j) { return key1(j); }, no, tau1,
+                                              keq1, nullptr, 0, 0, F, rs);
     auto in1 = [&](int64_t i) { return ((F[i >> 5] >> (i & 31)) & 1u) != 0u; };
     auto key2 = [&](int64_t i) -> uint32_t {
       if (in1(i)) return 0u;
@@ -203,16 +123,18 @@ compact_select(const float* __restrict__ scores, const float* __restrict__ crit,
       return score_key(kap) + 1u;
     };
     uint32_t tau2, keq2;
-    block_topk_threshold<kSelThreads>(C, K2, key2, rs, tau2, keq2);
-    const uint32_t n = select_ordered<kSelThreads, false>(
-        C, [&](int j) { return key2(j); }, [&](int j) { return in1(j); }, tau2, keq2, kept,
-        base, cap, nullptr, scr);
-    if (threadIdx.x == 0 && n != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
+    cluster_topk_threshold<kSelThreads>(p0, p1, K2, key2, rs, tau2, keq2);
+    const uint32_t n = cluster_select_ordered<kSelThreads, false>(
+        p0, p1, [&](int j) { return key2(j); }, [&](int j) { return in1(j); }, tau2, keq2, kept,
+        base, cap, nullptr, rs);
+    if (rank == 0 && threadIdx.x == 0 && n != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
   }
-  for (int t = threadIdx.x; t < w + reserve; t += kSelThreads) {
+  for (int t = rank * kSelThreads + threadIdx.x; t < w + reserve; t += ncta * kSelThreads) {
     const int64_t row = base + Bg + t;
     if (row < cap) kept[row] = t < w ? C + t : -1;
   }
+  // rank 0's shared memory was read by the other CTAs: none leaves before all are done
+  cl.sync();
 }
 
 // Copy the kept rows of K and V into the flat buffers, 16 bytes per thread.
@@ -264,9 +186,24 @@ cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const f
   const int64_t H = s.units();
   compact_offsets<<<1, kScanThreads, 0, st>>>(head_budget, H, s.Hkv, s.w, s.n, reserve, cap, cu,
                                                lens, hdr);
-  compact_select<<<(unsigned)H, kSelThreads, 0, st>>>(
-      scores, crit, can, cad, ceps, lens, cu, s.Hkv, s.C(), s.w, reserve, kept, cap,
-      reinterpret_cast<uint32_t*>(ws + p.off_flags), p.flag_words, hdr);
+  {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(kSelCl, (unsigned)H);
+    cfg.blockDim = dim3(kSelThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kSelCl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(
+        &cfg, compact_select, scores, crit, can, cad, ceps, (const int32_t*)lens,
+        (const int64_t*)cu, s.Hkv, s.C(), s.w, reserve, kept, cap,
+        reinterpret_cast<uint32_t*>(ws + p.off_flags), p.flag_words, hdr);
+    if (e != cudaSuccess) return e;
+  }
   const int row_bytes = s.d * s.esize();
   int gx = (int)cdiv((int64_t)num_sms() * 16, H);
   if (gx < 1) gx = 1;
