@@ -20,15 +20,15 @@
 // score_tc_fixup from per-range halo copies of the window means.
 //
 // LAVa: during P2 items (K then comes from L2) the producer also puts the V tiles of the
-// range into the ring; the epilogue warps fold each one into max ||V[k]||_1 of the unit
-// right after the K tile it follows (4 threads per row, so a V tile costs each thread four
-// 16-byte loads).  P2 writes unscaled scores and the fix-up kernel applies the factor
-// after the kernel, so nothing here waits for V.
+// range into the ring; a warpgroup of its own folds each one into max ||V[k]||_1 of the
+// unit (one row per thread).  P2 writes unscaled scores and the fix-up kernel applies the
+// factor after the kernel, so nothing here waits for V.
 //
-// Roles (640 threads): warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM
-// allocator, warp 3 = LSE agent, warps 4..19 = epilogue (TMEM lane
-// quadrant = warp % 4, column quarter = (warp - 4) / 4).  Every wait is bounded; on a timeout the CTA records DEV_WAIT_TIMEOUT,
-// unwinds, waits (bounded) for its copies and MMAs in flight and frees its TMEM.
+// Roles (768 threads): warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM
+// allocator, warp 3 = LSE agent, warps 4..19 = epilogue (TMEM lane quadrant = warp % 4,
+// column quarter = (warp - 4) / 4), warps 20..23 = LAVa V rows.  Every wait is bounded; on a
+// timeout the CTA records DEV_WAIT_TIMEOUT, unwinds, waits (bounded) for its copies and MMAs
+// in flight and frees its TMEM.
 #include <cudaTypedefs.h>
 
 #include <cstdlib>
@@ -46,7 +46,8 @@ using namespace ptx;
 constexpr int kStages = 4;
 constexpr int kEpiWarps = 16;                      // 4 TMEM lane quadrants x 4 column quarters
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kThreads = 32 * (4 + kEpiWarps);
+constexpr int kVWarps = 4;                         // LAVa V-row reducers (one warpgroup)
+constexpr int kThreads = 32 * (4 + kEpiWarps + kVWarps);
 constexpr uint32_t kBoxBytes = 128 * 128;          // 128 rows x 64 bf16 (one 128-byte row each)
 constexpr uint32_t kTileBytes = 2 * kBoxBytes;     // 128 rows x 128 bf16
 constexpr int kAFloats = 6144;                     // window sums of one range, all slots
@@ -97,31 +98,29 @@ struct TcParams {
   WsHeader* hdr;
 };
 
-// L1 norm of one row of a V tile in the ring (128 rows x 128 bf16, two 128-byte swizzled
-// boxes).  Four threads share a row, 32 elements each; a row's sum does not depend on the
-// order of its 16-byte pieces, so each thread reads physical pieces, rotated so that the
-// 8 threads of a shared-memory phase (2 rows x 4 parts) hit 8 different bank groups.
-__device__ __forceinline__ float vrow_l1(const uint8_t* base, int et) {
-  const int row = et >> 2, part = et & 3;
-  const int rot = 2 * (part >> 1) + (row & 1);
+// L1 norm of row `row` of a V tile in the ring (128 rows x 128 bf16, two 128-byte swizzled
+// boxes).  A row's sum does not depend on the order of its 16-byte pieces, so thread t reads
+// physical piece (j + t) % 8 of each box at step j: the 8 threads of a shared-memory phase
+// (8 consecutive rows) then hit 8 different bank groups.
+__device__ __forceinline__ float vrow_l1_row(const uint8_t* base, int row) {
   float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int pc = 4 * part + ((i + rot) & 3);
-    const uint4 x = *reinterpret_cast<const uint4*>(base + (pc >> 3) * kBoxBytes + row * 128 +
-                                                    (pc & 7) * 16);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+  for (int bx = 0; bx < 2; ++bx) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(h[e]);
-      a0 += fabsf(f.x);
-      a1 += fabsf(f.y);
+    for (int j = 0; j < 8; ++j) {
+      const int pc = (j + row) & 7;
+      const uint4 x =
+          *reinterpret_cast<const uint4*>(base + bx * kBoxBytes + row * 128 + pc * 16);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        a0 += fabsf(f.x);
+        a1 += fabsf(f.y);
+      }
     }
   }
-  float sum = a0 + a1;
-  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-  return sum;
+  return a0 + a1;
 }
 
 // P2 of the k-th unit follows P1 of the (k + kLag)-th: P1(0..a-1), then P1(k), P2(k-a) pairs,
@@ -381,6 +380,52 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         atomicAdd(&p.ready[u], 1u);
       }
     }
+  } else if (warp >= 4 + kEpiWarps) {
+    // ------------------------------ LAVa V rows --------------------------------
+    // The V entries the producer puts in the ring during P2 items (K then comes from L2,
+    // so the two passes share DRAM evenly): thread t of this warpgroup sums |V| over row t
+    // of each V tile, keeps the maximum over the unit's rows in its range, and the last of
+    // the four warps done with an entry frees its stage.  The fix-up kernel applies
+    // max_k ||V[k]||_1 after this kernel, so nothing here holds the epilogue up.
+    if (p.vbar != nullptr) {
+      const int vt_ = threadIdx.x - 32 * (4 + kEpiWarps);   // V row of this thread
+      uint32_t g = 0;
+      uint32_t vuse[kStages] = {};      // V tiles consumed per stage (phases of fullv[s])
+      bool ok = true;
+      for (int64_t i = 0; i < n_items && ok; ++i) {
+        int kind;
+        int64_t k;
+        item_of(i, m, kind, k);
+        const int te = kind == 1 ? t1 : t1c;
+        if (t0 >= te) continue;
+        if (kind == 1) { g += te - t0; continue; }
+        float vmax = 0.f;
+        for (int t = t0; t < te && ok; ++t) {
+          ++g;   // the K entry of tile t
+          const int nv = t + 1 < te ? 1 : t1 - t;
+          for (int j = 0; j < nv; ++j, ++g) {
+            const int sv = g % kStages;
+            if (!mbar_wait(&tl->fullv[sv], vuse[sv]++ & 1) || *abort_flag) { ok = false; break; }
+            vmax = fmaxf(vmax, vrow_l1_row(smem + kOffK + sv * kTileBytes, vt_));
+            __syncwarp();
+            if (lane == 0 && atomicAdd(&tl->vcnt[sv], 1u) == (uint32_t)(kVWarps - 1)) {
+              tl->vcnt[sv] = 0;
+              mbar_arrive(&tl->empty[sv]);
+            }
+          }
+        }
+        if (!ok) break;
+        const float wm = warp_max(vmax);
+        if (lane == 0 && wm > 0.f) {
+          const int64_t u = group + k * p.NG;
+          atomicMax(reinterpret_cast<unsigned int*>(p.vbar) + u, __float_as_uint(wm));
+        }
+      }
+      if (!ok && lane == 0) {
+        raise_dev(p.hdr, DEV_WAIT_TIMEOUT, 6);
+        *abort_flag = 1;
+      }
+    }
   } else if (warp >= 4) {
     // ------------------------------ epilogue ----------------------------------
     // Warp (4 + 4*qc + quad) reads TMEM lanes [32*quad, 32*quad + 32) and columns
@@ -397,9 +442,6 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     const int r = p.r, C = p.C, G = p.G;
     const float c2 = p.c2;
     uint32_t g = 0;     // TMEM accumulator counter (K tiles)
-    uint32_t gr = 0;    // ring entries (K and V), as the producer counts them
-    uint32_t vuse[kStages] = {};   // V entries consumed per stage (phases of fullv[s])
-    float vmax = 0.f;   // LAVa: max row L1 of V over this CTA's range of the unit
     bool ok = true;
     for (int64_t i = 0; i < n_items && ok; ++i) {
       int kind;
@@ -515,31 +557,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             pf_u = -1;
           }
         }
-        ++gr;                                    // the K entry of tile t
-        if (kind == 2 && p.vbar != nullptr) {
-          // the V rows that follow this K tile (after the last candidate tile, also those of
-          // the window-only tiles of the range); the last warp done releases the stage
-          const int nv = t + 1 < te ? 1 : t1 - t;
-          for (int j = 0; j < nv; ++j, ++gr) {
-            const int sv = gr % kStages;
-            if (!mbar_wait(&tl->fullv[sv], vuse[sv]++ & 1) || *abort_flag) { ok = false; break; }
-            vmax = fmaxf(vmax, vrow_l1(smem + kOffK + sv * kTileBytes, et));
-            __syncwarp();
-            if (lane == 0 && atomicAdd(&tl->vcnt[sv], 1u) == (uint32_t)(kEpiWarps - 1)) {
-              tl->vcnt[sv] = 0;
-              mbar_arrive(&tl->empty[sv]);
-            }
-          }
-          if (!ok) break;
-        }
       }
       if (!ok) break;
-      if (kind == 2 && p.vbar != nullptr) {
-        const float wm = warp_max(vmax);
-        if (lane == 0 && wm > 0.f)
-          atomicMax(reinterpret_cast<unsigned int*>(p.vbar) + u, __float_as_uint(wm));
-        vmax = 0.f;
-      }
       if (kind == 1) {
         part_s[qc * 128 + row] = make_float2(m_run, l_run);
         named_bar(1, kEpiThreads);
