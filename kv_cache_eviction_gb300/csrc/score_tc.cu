@@ -73,6 +73,7 @@ struct __align__(8) Tail {
   uint64_t qfull[2], qempty[2];
   uint64_t tfull[kTBuf], tempty[kTBuf];
   uint64_t drain;
+  uint64_t afull, aempty;   // window sums ready for pooling / pooled (A free again)
   uint32_t vcnt[kStages];  // epilogue warps done with the V entry in each stage
   int64_t pf_unit;      // unit whose -lse already sits in the nlse buffer (-1: none)
   uint32_t tmem_base;
@@ -123,6 +124,85 @@ __device__ __forceinline__ float vrow_l1_row(const uint8_t* base, int row) {
   return a0 + a1;
 }
 
+// Max-pool over the window means of one range, group reduction, scores of the keys whose
+// pooling window lies inside the range, and the halo copies for the fix-up of the others.
+// A holds the window sums of keys [sK, eK) (see the epilogue); tid / nthr are this thread's
+// index and the number of threads (a multiple of 32) that share the work.
+template <int LW>
+__device__ __forceinline__ void pool_range(const float* A, int RK, int sK, int eK, int C, int G,
+                                           int r, int group_max, float inv_w, float* S,
+                                           float* H, int tid, int nthr) {
+  // window mean of query head q at key j (slots hold per-quarter sums for w = 64)
+  auto aval = [&](int q, int j) -> float {
+    if (LW <= 5) return A[q * RK + (j - sK)];
+    return (A[(2 * q) * RK + (j - sK)] + A[(2 * q + 1) * RK + (j - sK)]) * inv_w;
+  };
+  if (r == 3) {
+    // pool 7: one thread per (run of 8 keys, query head); the window maximum is
+    // max(max of 4, max of 2, 1) over values loaded once (-inf outside the range);
+    // the G query heads of a run sit in adjacent lanes and are combined by shuffles.
+    constexpr int RUN = 8;
+    const int qh = tid & (G - 1), run = tid / G;
+    const int nruns = (eK - sK + RUN - 1) / RUN;
+    const int stride = nthr / G;
+    for (int rr = run; rr < nruns + (stride - nruns % stride) % stride; rr += stride) {
+      const bool live = rr < nruns;
+      const int j0 = sK + rr * RUN;
+      float v[RUN + 6];
+#pragma unroll
+      for (int i = 0; i < RUN + 6; ++i) {
+        const int jj = j0 - 3 + i;
+        v[i] = (live && jj >= sK && jj < eK) ? aval(qh, jj) : -INFINITY;
+      }
+      float m2[RUN + 5], out[RUN];
+#pragma unroll
+      for (int i = 0; i < RUN + 5; ++i) m2[i] = fmaxf(v[i], v[i + 1]);
+#pragma unroll
+      for (int i = 0; i < RUN; ++i)
+        out[i] = fmaxf(fmaxf(fmaxf(m2[i], m2[i + 2]), m2[i + 4]), v[i + 6]);
+#pragma unroll
+      for (int i = 0; i < RUN; ++i) {
+        float gv = out[i];
+        for (int o = 1; o < G; o <<= 1) {
+          const float x = __shfl_xor_sync(0xffffffffu, gv, o);
+          gv = group_max ? fmaxf(gv, x) : gv + x;
+        }
+        out[i] = group_max ? gv : gv / (float)G;
+      }
+      if (live && qh == 0) {
+#pragma unroll
+        for (int i = 0; i < RUN; ++i) {
+          const int j = j0 + i;
+          if (j >= eK) break;
+          const int lo = max(0, j - 3), hi = min(C - 1, j + 3);
+          if (lo >= sK && hi < eK) S[j] = out[i];
+        }
+      }
+    }
+  } else {
+    for (int j = sK + tid; j < eK; j += nthr) {
+      const int lo = max(0, j - r), hi = min(C - 1, j + r);
+      if (lo >= sK && hi < eK) {
+        float gv = group_max ? -INFINITY : 0.f;
+        for (int q = 0; q < G; ++q) {
+          float pm = -INFINITY;
+          for (int jj = lo; jj <= hi; ++jj) pm = fmaxf(pm, aval(q, jj));
+          gv = group_max ? fmaxf(gv, pm) : gv + pm;
+        }
+        if (!group_max) gv = gv / (float)G;
+        S[j] = gv;
+      }
+    }
+  }
+  if (r > 0) {   // halo copies for the fix-up of keys near the range's ends
+    for (int idx = tid; idx < G * 4 * r; idx += nthr) {
+      const int q = idx / (4 * r), sl = idx % (4 * r);
+      const int j = sl < 2 * r ? sK + sl : eK - 2 * r + (sl - 2 * r);
+      if (j >= sK && j < eK) H[q * 4 * r + sl] = aval(q, j);
+    }
+  }
+}
+
 // P2 of the k-th unit follows P1 of the (k + kLag)-th: P1(0..a-1), then P1(k), P2(k-a) pairs,
 // then the last P2s, with a = min(kLag, m).  kind 1 = P1, 2 = P2.
 constexpr int kLag = KV_TC_LAG;
@@ -169,6 +249,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       mbar_init(&tl->tempty[b], kEpiWarps);
     }
     mbar_init(&tl->drain, 1);
+    mbar_init(&tl->afull, 1);
+    mbar_init(&tl->aempty, kVWarps);
     for (int st = 0; st < kStages; ++st) tl->vcnt[st] = 0;
     tl->abort_flag = 0;
     tl->last_flag = 0;
@@ -387,9 +469,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     // of each V tile, keeps the maximum over the unit's rows in its range, and the last of
     // the four warps done with an entry frees its stage.  The fix-up kernel applies
     // max_k ||V[k]||_1 after this kernel, so nothing here holds the epilogue up.
-    if (p.vbar != nullptr) {
-      const int vt_ = threadIdx.x - 32 * (4 + kEpiWarps);   // V row of this thread
-      uint32_t g = 0;
+    {
+      const int vt_ = threadIdx.x - 32 * (4 + kEpiWarps);   // V row / pooling thread
+      float* A = reinterpret_cast<float*>(smem + kOffA);
+      const int RK = (t1 - t0) * 128;
+      const bool lava = p.vbar != nullptr;
+      uint32_t g = 0, np2 = 0;
       uint32_t vuse[kStages] = {};      // V tiles consumed per stage (phases of fullv[s])
       bool ok = true;
       for (int64_t i = 0; i < n_items && ok; ++i) {
@@ -399,8 +484,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         const int te = kind == 1 ? t1 : t1c;
         if (t0 >= te) continue;
         if (kind == 1) { g += te - t0; continue; }
+        const int64_t u = group + k * p.NG;
         float vmax = 0.f;
-        for (int t = t0; t < te && ok; ++t) {
+        for (int t = t0; t < te && ok && lava; ++t) {
           ++g;   // the K entry of tile t
           const int nv = t + 1 < te ? 1 : t1 - t;
           for (int j = 0; j < nv; ++j, ++g) {
@@ -415,11 +501,19 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
           }
         }
         if (!ok) break;
-        const float wm = warp_max(vmax);
-        if (lane == 0 && wm > 0.f) {
-          const int64_t u = group + k * p.NG;
-          atomicMax(reinterpret_cast<unsigned int*>(p.vbar) + u, __float_as_uint(wm));
+        if (lava) {
+          const float wm = warp_max(vmax);
+          if (lane == 0 && wm > 0.f)
+            atomicMax(reinterpret_cast<unsigned int*>(p.vbar) + u, __float_as_uint(wm));
         }
+        // pool the item's window sums once the epilogue has written all of them
+        if (!mbar_wait(&tl->afull, np2 & 1) || *abort_flag) { ok = false; break; }
+        ++np2;
+        const int sK = t0 * 128, eK = min(te * 128, p.C);
+        pool_range<LW>(A, RK, sK, eK, p.C, p.G, p.r, p.group_max, p.inv_w, p.scores + u * p.C,
+                       p.halo + (u * p.Pg + rank) * (int64_t)p.G * 4 * p.r, vt_, 32 * kVWarps);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tl->aempty);
       }
       if (!ok && lane == 0) {
         raise_dev(p.hdr, DEV_WAIT_TIMEOUT, 6);
@@ -439,9 +533,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     float* nlse = reinterpret_cast<float*>(smem + kOffLse);
     float2* part_s = reinterpret_cast<float2*>(smem + kOffPart);
     const int RK = (t1 - t0) * 128;                // keys of this CTA's range (A stride)
-    const int r = p.r, C = p.C, G = p.G;
     const float c2 = p.c2;
     uint32_t g = 0;     // TMEM accumulator counter (K tiles)
+    uint32_t np2 = 0;   // P2 items finished (phases of afull / aempty)
     bool ok = true;
     for (int64_t i = 0; i < n_items && ok; ++i) {
       int kind;
@@ -451,6 +545,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       const int te = kind == 1 ? t1 : t1c;
       if (t0 >= te) continue;
       if (kind == 2) {
+        // the window sums of the previous P2 item have been pooled
+        if (!mbar_wait(&tl->aempty, (np2 & 1) ^ 1) || *abort_flag) { ok = false; break; }
         if (tl->pf_unit != u) {     // not prefetched during the previous P1 item: wait now
           if (et == 0) {
             const uint64_t tw = globaltimer();
@@ -581,80 +677,14 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         }
         named_bar(1, kEpiThreads);     // part_s is free for the next item
       } else {
+        // every epilogue warp has written its window sums: the V warpgroup pools them while
+        // the epilogue goes on with the next item
         named_bar(1, kEpiThreads);
-        const int sK = t0 * 128;
-        const int eK = min(te * 128, C);
-        float* H = p.halo + (u * p.Pg + rank) * (int64_t)G * 4 * r;
-        // window mean of query head q at key j (slots hold per-quarter sums for w = 64)
-        auto aval = [&](int q, int j) -> float {
-          if (LW <= 5) return A[q * RK + (j - sK)];
-          return (A[(2 * q) * RK + (j - sK)] + A[(2 * q + 1) * RK + (j - sK)]) * p.inv_w;
-        };
-        if (r == 3) {
-          // pool 7: one thread per (run of 8 keys, query head); the window maximum is
-          // max(max of 4, max of 2, 1) over values loaded once (-inf outside the range);
-          // the G query heads of a run sit in adjacent lanes and are combined by shuffles.
-          constexpr int RUN = 8;
-          const int qh = et & (G - 1), run = et / G;
-          const int nruns = (eK - sK + RUN - 1) / RUN;
-          const int stride = kEpiThreads / G;
-          for (int rr = run; rr < nruns + (stride - nruns % stride) % stride; rr += stride) {
-            const bool live = rr < nruns;
-            const int j0 = sK + rr * RUN;
-            float v[RUN + 6];
-#pragma unroll
-            for (int i = 0; i < RUN + 6; ++i) {
-              const int jj = j0 - 3 + i;
-              v[i] = (live && jj >= sK && jj < eK) ? aval(qh, jj) : -INFINITY;
-            }
-            float m2[RUN + 5], out[RUN];
-#pragma unroll
-            for (int i = 0; i < RUN + 5; ++i) m2[i] = fmaxf(v[i], v[i + 1]);
-#pragma unroll
-            for (int i = 0; i < RUN; ++i)
-              out[i] = fmaxf(fmaxf(fmaxf(m2[i], m2[i + 2]), m2[i + 4]), v[i + 6]);
-#pragma unroll
-            for (int i = 0; i < RUN; ++i) {
-              float gv = out[i];
-              for (int o = 1; o < G; o <<= 1) {
-                const float x = __shfl_xor_sync(0xffffffffu, gv, o);
-                gv = p.group_max ? fmaxf(gv, x) : gv + x;
-              }
-              out[i] = p.group_max ? gv : gv / (float)G;
-            }
-            if (live && qh == 0) {
-#pragma unroll
-              for (int i = 0; i < RUN; ++i) {
-                const int j = j0 + i;
-                if (j >= eK) break;
-                const int lo = max(0, j - 3), hi = min(C - 1, j + 3);
-                if (lo >= sK && hi < eK) p.scores[u * C + j] = out[i];
-              }
-            }
-          }
-        } else {
-          for (int j = sK + et; j < eK; j += kEpiThreads) {
-            const int lo = max(0, j - r), hi = min(C - 1, j + r);
-            if (lo >= sK && hi < eK) {
-              float gv = p.group_max ? -INFINITY : 0.f;
-              for (int q = 0; q < G; ++q) {
-                float pm = -INFINITY;
-                for (int jj = lo; jj <= hi; ++jj) pm = fmaxf(pm, aval(q, jj));
-                gv = p.group_max ? fmaxf(gv, pm) : gv + pm;
-              }
-              if (!p.group_max) gv = gv / (float)G;
-              p.scores[u * C + j] = gv;
-            }
-          }
+        if (et == 0) {
+          tl->pf_unit = -1;
+          mbar_arrive(&tl->afull);
         }
-        if (r > 0) {   // halo copies for the fix-up of keys near the range's ends
-          for (int idx = et; idx < G * 4 * r; idx += kEpiThreads) {
-            const int q = idx / (4 * r), sl = idx % (4 * r);
-            const int j = sl < 2 * r ? sK + sl : eK - 2 * r + (sl - 2 * r);
-            if (j >= sK && j < eK) H[q * 4 * r + sl] = aval(q, j);
-          }
-        }
-        if (et == 0) tl->pf_unit = -1;
+        ++np2;
         named_bar(1, kEpiThreads);
       }
       (void)NSLOT;
