@@ -80,13 +80,19 @@ compact_offsets(const int32_t* __restrict__ head_budget, int64_t H, int Hkv, int
 // One thread-block cluster of kSelCl CTAs per head: threshold(s), ordered kept positions,
 // window and reserve rows.  CTA r of the cluster owns candidate positions
 // [r * span, (r + 1) * span), span a multiple of 32 (whole words of the stage-1 bits).
-__global__ void __launch_bounds__(kSelThreads)
+// STAGED: the CTA first copies its span of scores into shared memory (16-byte loads, the
+// copy aligned like the source) and every pass of the selection reads it from there, so the
+// scores cross HBM once; CriticalKV's stage-2 keys then replace the staged scores in place
+// (0 marks a stage-1 position).  Otherwise every pass reads the scores from global memory.
+template <bool STAGED>
+__global__ void __launch_bounds__(kSelThreads, 2)
 compact_select(const float* __restrict__ scores, const float* __restrict__ crit, uint32_t can,
                uint32_t cad, float ceps, const int32_t* __restrict__ lens,
                const int64_t* __restrict__ cu, int Hkv, int C, int w, int reserve,
                int32_t* __restrict__ kept, int64_t cap, uint32_t* __restrict__ flags,
                int64_t words, WsHeader* hdr) {
   __shared__ ClusterSelectSmem rs;
+  extern __shared__ float4 stage4[];
   cg::cluster_group cl = cg::this_cluster();
   const int rank = (int)cl.block_rank(), ncta = (int)cl.num_blocks();
   const int64_t h = blockIdx.y;
@@ -98,35 +104,60 @@ compact_select(const float* __restrict__ scores, const float* __restrict__ crit,
   const int span = ((C + ncta - 1) / ncta + 31) & ~31;
   const int p0 = min(C, rank * span), p1 = min(C, p0 + span);
   auto no = [](int) { return false; };
+  float* sv = reinterpret_cast<float*>(stage4);
+  int shift = 0;   // sv[i + shift] holds S[i] for i in [p0, p1)
+  if (STAGED) {
+    const int64_t f0 = h * (int64_t)C + p0, f1 = h * (int64_t)C + p1;
+    const int64_t a0 = f0 & ~(int64_t)3;            // aligned start (inside the array)
+    const int64_t a1 = f1 > a0 ? (f1 & ~(int64_t)3) : a0;
+    shift = (int)(f0 - a0) - p0;
+    const float4* src = reinterpret_cast<const float4*>(scores + a0);
+    const int nv = (int)((a1 - a0) >> 2);
+    constexpr int U = 4;
+    for (int j0 = threadIdx.x; j0 < nv; j0 += U * kSelThreads) {
+      float4 x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + u * kSelThreads;
+        x[u] = j < nv ? src[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (j0 + u * kSelThreads < nv) stage4[j0 + u * kSelThreads] = x[u];
+    }
+    for (int64_t f = a1 + threadIdx.x; f < f1; f += kSelThreads) sv[f - a0] = scores[f];
+    __syncthreads();
+  }
+  auto sval = [&](int64_t i) -> float { return STAGED ? sv[i + shift] : S[i]; };
   if (crit == nullptr) {
-    uint32_t tau, keq;
-    auto key = [&](int64_t i) { return score_key(S[i]); };
-    cluster_topk_threshold<kSelThreads>(p0, p1, Bg, key, rs, tau, keq);
-    const uint32_t n = cluster_select_ordered<kSelThreads, false>(
-        p0, p1, [&](int j) { return key(j); }, no, tau, keq, kept, base, cap, nullptr, rs);
+    auto key = [&](int j) { return score_key(sval(j)); };
+    const uint32_t n = cluster_topk_select<kSelThreads, false>(p0, p1, Bg, key, no, kept, base,
+                                                               cap, nullptr, rs);
     if (rank == 0 && threadIdx.x == 0 && n != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
   } else {
     const float* Cn = crit + h * (int64_t)C;
     uint32_t* F = flags + h * words;
     const int64_t K1 = ((int64_t)can * Bg) / cad;
     const int64_t K2 = Bg - K1;
-    uint32_t tau1, keq1;
-    auto key1 = [&](int64_t i) { return score_key(S[i]); };
-    cluster_topk_threshold<kSelThreads>(p0, p1, K1, key1, rs, tau1, keq1);
+    auto key1 = [&](int j) { return score_key(sval(j)); };
     // stage-1 membership bits (each CTA writes and later reads the words of its own span)
-    cluster_select_ordered<kSelThreads, true>(p0, p1, [&](int j) { return key1(j); }, no, tau1,
-                                              keq1, nullptr, 0, 0, F, rs);
+    cluster_topk_select<kSelThreads, true>(p0, p1, K1, key1, no, nullptr, 0, 0, F, rs);
     auto in1 = [&](int64_t i) { return ((F[i >> 5] >> (i & 31)) & 1u) != 0u; };
-    auto key2 = [&](int64_t i) -> uint32_t {
+    auto key2g = [&](int64_t i) -> uint32_t {
       if (in1(i)) return 0u;
-      const float kap = __fmul_rn(__fadd_rn(S[i], ceps), Cn[i]);
+      const float kap = __fmul_rn(__fadd_rn(sval(i), ceps), Cn[i]);
       return score_key(kap) + 1u;
     };
-    uint32_t tau2, keq2;
-    cluster_topk_threshold<kSelThreads>(p0, p1, K2, key2, rs, tau2, keq2);
-    const uint32_t n = cluster_select_ordered<kSelThreads, false>(
-        p0, p1, [&](int j) { return key2(j); }, [&](int j) { return in1(j); }, tau2, keq2, kept,
-        base, cap, nullptr, rs);
+    uint32_t* sk = reinterpret_cast<uint32_t*>(sv);
+    if (STAGED) {
+      // the bits were written by this CTA before the barrier that ends the selection
+      for (int i = p0 + threadIdx.x; i < p1; i += kSelThreads) sk[i + shift] = key2g(i);
+      __syncthreads();
+    }
+    auto key2 = [&](int j) -> uint32_t { return STAGED ? sk[j + shift] : key2g(j); };
+    auto forced2 = [&](int j) { return STAGED ? sk[j + shift] == 0u : in1(j); };
+    const uint32_t n = cluster_topk_select<kSelThreads, false>(p0, p1, K2, key2, forced2, kept,
+                                                               base, cap, nullptr, rs);
     if (rank == 0 && threadIdx.x == 0 && n != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
   }
   for (int t = rank * kSelThreads + threadIdx.x; t < w + reserve; t += ncta * kSelThreads) {
@@ -198,9 +229,25 @@ cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const f
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // staged when a span (plus the alignment slack) fits next to the selection's own state
+    const int C = s.C();
+    const int span = ((C + kSelCl - 1) / kSelCl + 31) & ~31;
+    const size_t stage_bytes = align_up(((size_t)span + 8) * sizeof(float), 16);
+    const bool staged = C > 0 && stage_bytes + sizeof(ClusterSelectSmem) + 1024 <= max_smem_optin();
+    auto kern = staged ? compact_select<true> : compact_select<false>;
+    if (staged) {
+      static size_t opted = 0;   // the largest size opted in so far
+      if (stage_bytes > opted) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)stage_bytes);
+        if (e != cudaSuccess) return e;
+        opted = stage_bytes;
+      }
+      cfg.dynamicSmemBytes = stage_bytes;
+    }
     cudaError_t e = cudaLaunchKernelEx(
-        &cfg, compact_select, scores, crit, can, cad, ceps, (const int32_t*)lens,
-        (const int64_t*)cu, s.Hkv, s.C(), s.w, reserve, kept, cap,
+        &cfg, kern, scores, crit, can, cad, ceps, (const int32_t*)lens,
+        (const int64_t*)cu, s.Hkv, C, s.w, reserve, kept, cap,
         reinterpret_cast<uint32_t*>(ws + p.off_flags), p.flag_words, hdr);
     if (e != cudaSuccess) return e;
   }

@@ -61,6 +61,8 @@ cudaError_t launch_decode(const Shape& s, const void* q, const void* kn, const v
                           cudaStream_t st);
 
 int num_sms();
+// Largest dynamic + static shared memory one CTA may opt in to.
+size_t max_smem_optin();
 // Adds n to the library's running count of kernel launches (kv_kernel_launches()).
 void count_launches(int n);
 

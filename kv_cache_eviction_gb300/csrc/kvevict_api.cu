@@ -22,6 +22,20 @@ int num_sms() {
   return cached;
 }
 
+size_t max_smem_optin() {
+  static size_t cached = 0;
+  if (cached == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+        v > 0)
+      cached = (size_t)v;
+    else
+      cached = 48 * 1024;
+  }
+  return cached;
+}
+
 static std::atomic<unsigned long long> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
 
