@@ -27,6 +27,12 @@ cudaError_t launch_score(const Shape& s, int mode, int group, const void* q_win,
                          const void* v, const void* w_o, int D, float* scores, float* crit,
                          char* ws, const ScorePlan& p, cudaStream_t st);
 
+// After the tcgen05 scoring kernel: LAVa's V-bar factor (vbar != nullptr) and the keys whose
+// pooling window crosses a range boundary (from the halo copies of both ranges).
+cudaError_t launch_score_fixup(const float* halo, const float* vbar, int64_t units, int Pg,
+                               int Tu, int C, int G, int r, int group_max, float* scores,
+                               cudaStream_t st);
+
 // ----------------------------- allocation ----------------------------------
 struct AllocPlan {
   int nchunkE;          // entropy partial CTAs per segment

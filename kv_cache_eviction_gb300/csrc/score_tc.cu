@@ -17,7 +17,7 @@
 // Items are ordered P1(u0), P1(u1), P2(u0), P1(u2), P2(u1), ... so a CTA's P2 of unit u
 // re-reads its K tiles from L2 after one unit of other traffic, and rarely waits for the
 // flag.  Keys whose pooling window crosses a CTA's range boundary are finished by
-// score_tc_fixup from per-range halo copies of the window means.
+// score_tc_fixup (score_fixup.cu) from per-range halo copies of the window means.
 //
 // LAVa: during P2 items (K then comes from L2) the producer also puts the V tiles of the
 // range into the ring; a warpgroup of its own folds each one into max ||V[k]||_1 of the
@@ -701,52 +701,6 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   }
 }
 
-// After the main kernel: (LAVa) scale the unit's scores by max_k ||V[k]||_1, then pool the
-// keys within pool/2 of a range boundary from the halo copies of both ranges.
-__global__ void score_tc_fixup(const float* __restrict__ halo, const float* __restrict__ vbar,
-                               int Pg, int Tu, int C, int G, int r, int group_max,
-                               float* __restrict__ scores) {
-  const int64_t u = blockIdx.x;
-  const int R4 = 4 * r;
-  float vb = 1.0f;
-  float* S = scores + u * C;
-  if (vbar) {
-    vb = vbar[u];
-    for (int j = threadIdx.x * 4; j < C; j += blockDim.x * 4) {
-      if (j + 3 < C && ((reinterpret_cast<uintptr_t>(S + j) & 15) == 0)) {
-        float4 x = *reinterpret_cast<float4*>(S + j);
-        x.x *= vb; x.y *= vb; x.z *= vb; x.w *= vb;
-        *reinterpret_cast<float4*>(S + j) = x;
-      } else {
-        for (int jj = j; jj < min(C, j + 4); ++jj) S[jj] *= vb;
-      }
-    }
-    __syncthreads();
-  }
-  for (int idx = threadIdx.x; idx < (Pg - 1) * 2 * r; idx += blockDim.x) {
-    const int bnd = idx / (2 * r) + 1;
-    const int b = (int)(((int64_t)bnd * Tu) / Pg) * 128;
-    if (b >= C) continue;
-    const int j = b - r + idx % (2 * r);
-    if (j < 0 || j >= C) continue;
-    const int lo = max(0, j - r), hi = min(C - 1, j + r);
-    const float* Hl = halo + (u * Pg + bnd - 1) * (int64_t)G * R4;
-    const float* Hr = halo + (u * Pg + bnd) * (int64_t)G * R4;
-    float gv = group_max ? -INFINITY : 0.f;
-    for (int q = 0; q < G; ++q) {
-      float pm = -INFINITY;
-      for (int jj = lo; jj <= hi; ++jj) {
-        const float x = jj < b ? Hl[q * R4 + 2 * r + (jj - (b - 2 * r))] : Hr[q * R4 + (jj - b)];
-        pm = fmaxf(pm, x);
-      }
-      gv = group_max ? fmaxf(gv, pm) : gv + pm;
-    }
-    if (!group_max) gv = gv / (float)G;
-    if (vbar) gv = gv * vb;
-    S[j] = gv;
-  }
-}
-
 // --------------------------------- host side ----------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -929,9 +883,9 @@ cudaError_t launch_score_tc(const Shape& s, int mode, int group, const void* q_w
   if (e != cudaSuccess) return e;
   count_launches(1);
   if (prm.vbar != nullptr || (prm.r > 0 && tp.Pg > 1)) {
-    score_tc_fixup<<<(unsigned)units, 256, 0, st>>>(
-        prm.halo, prm.vbar, tp.Pg, tp.Tu, prm.C, prm.G, prm.r, prm.group_max, scores);
-    count_launches(1);
+    e = launch_score_fixup(prm.halo, prm.vbar, units, tp.Pg, tp.Tu, prm.C, prm.G, prm.r,
+                           prm.group_max, scores, st);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
