@@ -5,6 +5,9 @@
 // every head of a layer into one tensor (cu_seqlens-style offsets), filled by a
 // cache-update kernel.  CriticalKV: two-stage greedy selection, stage 1 by the
 // attention score, stage 2 by (A + eps) * ||(V W^O)_j||_1.
+#include <cstdlib>
+#include <cstring>
+
 #include "kv_internal.cuh"
 #include "radix_select.cuh"
 
@@ -12,7 +15,7 @@ namespace kv {
 
 namespace {
 constexpr int kScanThreads = 1024;
-constexpr int kSelThreads = 256;
+constexpr int kSelThreads = 512;
 constexpr int kSelCl = 8;       // CTAs (one cluster) per head
 constexpr int kGatherThreads = 256;
 }
@@ -129,10 +132,15 @@ compact_select(const float* __restrict__ scores, const float* __restrict__ crit,
     __syncthreads();
   }
   auto sval = [&](int64_t i) -> float { return STAGED ? sv[i + shift] : S[i]; };
+  const uint32_t* raw = reinterpret_cast<const uint32_t*>(sv);
+  const int s0 = p0 + shift, s1 = p1 + shift;   // the span's slots when staged
   if (crit == nullptr) {
     auto key = [&](int j) { return score_key(sval(j)); };
-    const uint32_t n = cluster_topk_select<kSelThreads, false>(p0, p1, Bg, key, no, kept, base,
-                                                               cap, nullptr, rs);
+    const uint32_t n =
+        STAGED ? cluster_topk_select_staged<kSelThreads, false, ScoreKeys>(
+                     raw, s0, s1, shift, Bg, kept, base, cap, nullptr, rs)
+               : cluster_topk_select<kSelThreads, false>(p0, p1, Bg, key, no, kept, base, cap,
+                                                         nullptr, rs);
     if (rank == 0 && threadIdx.x == 0 && n != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
   } else {
     const float* Cn = crit + h * (int64_t)C;
@@ -141,7 +149,11 @@ compact_select(const float* __restrict__ scores, const float* __restrict__ crit,
     const int64_t K2 = Bg - K1;
     auto key1 = [&](int j) { return score_key(sval(j)); };
     // stage-1 membership bits (each CTA writes and later reads the words of its own span)
-    cluster_topk_select<kSelThreads, true>(p0, p1, K1, key1, no, nullptr, 0, 0, F, rs);
+    if (STAGED)
+      cluster_topk_select_staged<kSelThreads, true, ScoreKeys>(raw, s0, s1, shift, K1, nullptr, 0,
+                                                                0, F, rs);
+    else
+      cluster_topk_select<kSelThreads, true>(p0, p1, K1, key1, no, nullptr, 0, 0, F, rs);
     auto in1 = [&](int64_t i) { return ((F[i >> 5] >> (i & 31)) & 1u) != 0u; };
     auto key2g = [&](int64_t i) -> uint32_t {
       if (in1(i)) return 0u;
@@ -156,8 +168,11 @@ compact_select(const float* __restrict__ scores, const float* __restrict__ crit,
     }
     auto key2 = [&](int j) -> uint32_t { return STAGED ? sk[j + shift] : key2g(j); };
     auto forced2 = [&](int j) { return STAGED ? sk[j + shift] == 0u : in1(j); };
-    const uint32_t n = cluster_topk_select<kSelThreads, false>(p0, p1, K2, key2, forced2, kept,
-                                                               base, cap, nullptr, rs);
+    const uint32_t n =
+        STAGED ? cluster_topk_select_staged<kSelThreads, false, StoredKeys>(
+                     raw, s0, s1, shift, K2, kept, base, cap, nullptr, rs)
+               : cluster_topk_select<kSelThreads, false>(p0, p1, K2, key2, forced2, kept, base,
+                                                         cap, nullptr, rs);
     if (rank == 0 && threadIdx.x == 0 && n != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
   }
   for (int t = rank * kSelThreads + threadIdx.x; t < w + reserve; t += ncta * kSelThreads) {
@@ -198,6 +213,13 @@ compact_gather(const char* __restrict__ k, const char* __restrict__ v,
   }
 }
 
+// KVEVICT_SELECT_PATH=global forces the selection that reads the scores from global memory
+// on every pass (the one spans too long for shared memory take); tests compare the two.
+static bool global_select_forced() {
+  const char* e = std::getenv("KVEVICT_SELECT_PATH");
+  return e != nullptr && std::strcmp(e, "global") == 0;
+}
+
 CompactPlan compact_plan(const Shape& s, bool critical) {
   CompactPlan p{};
   size_t off = kWsHeader;
@@ -233,7 +255,8 @@ cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const f
     const int C = s.C();
     const int span = ((C + kSelCl - 1) / kSelCl + 31) & ~31;
     const size_t stage_bytes = align_up(((size_t)span + 8) * sizeof(float), 16);
-    const bool staged = C > 0 && stage_bytes + sizeof(ClusterSelectSmem) + 1024 <= max_smem_optin();
+    const bool staged = C > 0 && !global_select_forced() &&
+                        stage_bytes + sizeof(ClusterSelectSmem) + 1024 <= max_smem_optin();
     auto kern = staged ? compact_select<true> : compact_select<false>;
     if (staged) {
       static size_t opted = 0;   // the largest size opted in so far

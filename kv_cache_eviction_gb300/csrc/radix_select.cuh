@@ -60,6 +60,11 @@ __device__ void cluster_pick(ClusterSelectSmem& sm, int nb, uint32_t krem, uint3
   }
   cl.sync();
   if (lead) {
+    // fewer than krem keys in all: bin 0 (the caller's bound then covers every key)
+    if (threadIdx.x == 0) {
+      sm.res[0] = 0u;
+      sm.res[1] = krem;
+    }
     // thread t owns reversed bins [t*per, (t+1)*per)
     const int per = nb / BLOCK;
     uint32_t local = 0;
@@ -365,6 +370,250 @@ __device__ uint32_t cluster_topk_select(int p0, int p1, int64_t K, KeyFn key, Fo
         emit(j0 + lane, j0 + lane < s1, kk[u], ff[u]);
       }
     }
+  }
+  __syncthreads();   // lists and scr are reused by the next call
+  return total;
+}
+
+// Keys of a staged span: the selection reads 32-bit raw values from shared memory and maps
+// them to keys.  Scores: the raw value is the fp32 score, the key its score_key, nothing is
+// forced.  Stored keys: the raw value is the key itself and 0 marks a forced position.
+struct ScoreKeys {
+  static __device__ __forceinline__ uint32_t key(uint32_t raw) {
+    return score_key(__uint_as_float(raw));
+  }
+  static __device__ __forceinline__ bool forced(uint32_t) { return false; }
+};
+struct StoredKeys {
+  static __device__ __forceinline__ uint32_t key(uint32_t raw) { return raw; }
+  static __device__ __forceinline__ bool forced(uint32_t raw) { return raw == 0u; }
+};
+
+// cluster_topk_select over a span staged in shared memory: raw[slot] holds position
+// slot - shift for slots [s0, s1), raw is 16-byte aligned and readable up to the next multiple
+// of 4 slots.  Before any exact pass, a histogram of the first digit of each aligned group
+// of 4 slots' largest key gives a bin g whose groups number at least K, so at least K keys
+// have a first digit >= g and tau's first digit is >= g.  The candidate lists then hold the
+// positions with first digit >= g (or forced), read 16 bytes at a time, and all three exact
+// passes walk the lists; a CTA whose list overflows walks its whole span instead.  The result
+// is the same as cluster_topk_select's.
+template <int BLOCK, bool BITS, class P>
+__device__ uint32_t cluster_topk_select_staged(const uint32_t* raw, int s0, int s1, int shift,
+                                               int64_t K, int32_t* kept, int64_t base,
+                                               int64_t cap, uint32_t* bits,
+                                               ClusterSelectSmem& sm) {
+  static_assert(BLOCK <= 1024 && (1024 % BLOCK) == 0, "block must divide 1024");
+  constexpr int NW = BLOCK / 32;
+  constexpr int LW = kListCap / NW;   // list entries per warp
+  constexpr int U = 4;                // 16-byte groups per thread fetched before use
+  cg::cluster_group cl = cg::this_cluster();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t below = (1u << lane) - 1u;
+  const uint4* raw4 = reinterpret_cast<const uint4*>(raw);
+  const int nq = (s1 + 3) >> 2;        // groups holding the span (group 0 holds slot s0)
+  auto valid = [&](int slot) { return (unsigned)(slot - s0) < (unsigned)(s1 - s0); };
+  auto comp = [](const uint4& v, int c) { return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w; };
+  if (threadIdx.x == 0) sm.lover = 0u;
+  if (cl.block_rank() == 0)
+    for (int i = threadIdx.x; i < 2048; i += BLOCK) sm.ghist[i] = 0u;
+  cl.sync();
+
+  // ---- lower bound g for tau's first digit, from the groups' largest keys
+  const bool any = K > 0;   // the same in every CTA
+  uint32_t g = 2048u;       // with K == 0 no key is a candidate: only forced positions
+  if (any) {
+    for (int i = threadIdx.x; i < 2048; i += BLOCK) sm.hist[i] = 0u;
+    __syncthreads();
+    for (int qb = 0; qb < nq; qb += U * BLOCK) {
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int q = qb + u * BLOCK + (int)threadIdx.x;
+        v[u] = q < nq ? raw4[q] : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int q = qb + u * BLOCK + (int)threadIdx.x;
+        uint32_t m = 0u;
+        bool have = false;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (q < nq && valid(4 * q + c)) {
+            m = max(m, P::key(comp(v[u], c)));
+            have = true;
+          }
+        }
+        hist_add_runs(sm.hist, have ? m >> 21 : 0xFFFFFFFFu);
+      }
+    }
+    uint32_t b, kr;
+    cluster_pick<BLOCK>(sm, 2048, (uint32_t)K, b, kr);
+    g = b;
+  }
+
+  // ---- candidate lists: warp w lists, in order, the slots of its groups whose key has a
+  // first digit >= g or that are forced
+  const int per = (nq + NW - 1) / NW;
+  const int q0 = min(nq, warp * per), q1 = min(nq, q0 + per);
+  int32_t* L = sm.list + warp * LW;
+  {
+    uint32_t lc = 0;
+    bool over = false;
+    for (int qb = q0; qb < q1 && !over; qb += 32 * U) {
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int q = qb + 32 * u + lane;
+        v[u] = q < q1 ? raw4[q] : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int q = qb + 32 * u + lane;
+        uint32_t cm = 0u;   // candidate components of this lane's group
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t r = comp(v[u], c);
+          if (q < q1 && valid(4 * q + c) && (P::forced(r) || (P::key(r) >> 21) >= g))
+            cm |= 1u << c;
+        }
+        const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, cm & 1u);
+        const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, cm & 2u);
+        const uint32_t b2 = __ballot_sync(0xFFFFFFFFu, cm & 4u);
+        const uint32_t b3 = __ballot_sync(0xFFFFFFFFu, cm & 8u);
+        const uint32_t tot = __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
+        if (lc + tot > (uint32_t)LW) {
+          over = true;   // the same in every lane
+        } else if (!over) {
+          uint32_t o = lc + __popc(b0 & below) + __popc(b1 & below) + __popc(b2 & below) +
+                       __popc(b3 & below);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (cm & (1u << c)) L[o++] = 4 * q + c;
+          lc += tot;
+        }
+      }
+    }
+    if (lane == 0) {
+      sm.lcount[warp] = lc;
+      if (over) sm.lover = 1u;
+    }
+  }
+  __syncthreads();
+  const bool listed = sm.lover == 0u;   // the same in every thread of the CTA
+  const int cw = listed ? (int)sm.lcount[warp] : 0;
+  auto keyat = [&](int slot) { return P::key(raw[slot]); };
+
+  // ---- exact digits (the first over keys with first digit >= g: tau's is among them)
+  uint32_t prefix = 0, mask = 0, krem = any ? (uint32_t)K : 0u;
+  if (any) {
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+      const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+      const int nb = pass == 2 ? 1024 : 2048;
+      for (int i = threadIdx.x; i < nb; i += BLOCK) sm.hist[i] = 0u;
+      __syncthreads();
+      auto add = [&](uint32_t k, bool ok) {
+        const bool in = ok && (pass == 0 ? (k >> 21) >= g : (k & mask) == prefix);
+        hist_add_runs(sm.hist, in ? (k >> sh) & (uint32_t)(nb - 1) : 0xFFFFFFFFu);
+      };
+      if (listed) {
+        for (int b = 0; b < cw; b += 32 * 8) {
+          uint32_t kk[8];
+          bool ok[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int idx = b + 32 * u + lane;
+            ok[u] = idx < cw;
+            kk[u] = ok[u] ? keyat(L[idx]) : 0u;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) add(kk[u], ok[u]);
+        }
+      } else {
+        for (int b0 = s0; b0 < s1; b0 += 8 * BLOCK) {
+          uint32_t kk[8];
+          bool ok[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int i = b0 + k * BLOCK + (int)threadIdx.x;
+            ok[k] = i < s1;
+            kk[k] = ok[k] ? keyat(i) : 0u;
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) add(kk[k], ok[k]);
+        }
+      }
+      uint32_t b, kr;
+      cluster_pick<BLOCK>(sm, nb, krem, b, kr);
+      prefix |= b << sh;
+      mask |= (uint32_t)(nb - 1) << sh;
+      krem = kr;
+    }
+  }
+  const uint32_t tau = any ? prefix : 0xFFFFFFFFu;   // no key equals 0xFFFFFFFF
+  const uint32_t keq = any ? krem : 0u;
+
+  // ---- ordered selection: per-warp counts, cluster offsets, then each warp emits in order.
+  // Unlisted CTAs walk their slots in warp slices of whole 32-position words.
+  const int n = s1 - s0;
+  const int wper = (((n + NW - 1) / NW) + 31) & ~31;
+  const int w0 = min(s1, s0 + warp * wper), w1 = min(s1, w0 + wper);
+  uint32_t nkeep = 0, neq = 0;
+  auto tally = [&](int slot) {
+    const uint32_t r = raw[slot];
+    const bool f = P::forced(r);
+    const uint32_t k = P::key(r);
+    nkeep += (f || k > tau) ? 1u : 0u;
+    neq += (!f && k == tau) ? 1u : 0u;
+  };
+  if (listed) {
+    for (int idx = lane; idx < cw; idx += 32) tally(L[idx]);
+  } else {
+    for (int i = w0 + lane; i < w1; i += 32) tally(i);
+  }
+  nkeep = warp_sum_u(nkeep);
+  neq = warp_sum_u(neq);
+  if (lane == 0) {
+    sm.scr[warp] = nkeep;
+    sm.scr[32 + warp] = neq;
+  }
+  if (BITS && listed) {
+    // the CTA's words start clear; kept bits are then set one by one
+    const int p0 = s0 - shift, p1 = s1 - shift;
+    for (int wd = p0 / 32 + (int)threadIdx.x; wd < (p1 + 31) / 32; wd += BLOCK) bits[wd] = 0u;
+  }
+  const uint32_t total = cluster_order_offsets<BLOCK>(sm, keq);
+  uint32_t eqc = sm.scr[64 + warp], outc = sm.scr[96 + warp];
+  auto emit = [&](int slot, bool in) {
+    const uint32_t r = in ? raw[slot] : 0u;
+    const bool f = in && P::forced(r);
+    const uint32_t k = P::key(r);
+    const int j = slot - shift;
+    const bool iseq = in && !f && k == tau;
+    bool keep = in && (f || k > tau);
+    const uint32_t meq = __ballot_sync(0xFFFFFFFFu, iseq);
+    if (iseq && eqc + __popc(meq & below) < keq) keep = true;
+    const uint32_t mk = __ballot_sync(0xFFFFFFFFu, keep);
+    if (BITS) {
+      if (listed) {
+        if (keep) atomicOr(bits + (j >> 5), 1u << (j & 31));
+      } else if (lane == 0) {
+        bits[j >> 5] = mk;   // lane 0 holds the word's first position
+      }
+    } else if (keep) {
+      const int64_t row = base + outc + __popc(mk & below);
+      if (row < cap) kept[row] = j;
+    }
+    eqc += __popc(meq);
+    outc += __popc(mk);
+  };
+  if (listed) {
+    for (int b = 0; b < cw; b += 32) {
+      const int idx = b + lane;
+      emit(idx < cw ? L[idx] : 0, idx < cw);
+    }
+  } else {
+    for (int ib = w0; ib < w1; ib += 32) emit(ib + lane, ib + lane < w1);
   }
   __syncthreads();   // lists and scr are reused by the next call
   return total;
