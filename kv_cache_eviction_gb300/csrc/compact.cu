@@ -110,26 +110,48 @@ compact_select(const float* __restrict__ scores, const float* __restrict__ crit,
   float* sv = reinterpret_cast<float*>(stage4);
   int shift = 0;   // sv[i + shift] holds S[i] for i in [p0, p1)
   if (STAGED) {
+    // rank 0's cluster histogram starts clear: cleared here, published by the cluster barrier
+    // whose wait comes after the staging
+    if (rank == 0)
+      for (int i = threadIdx.x; i < 2048; i += kSelThreads) rs.ghist[i] = 0u;
+    auto arrived = cl.barrier_arrive();
+    for (int i = threadIdx.x; i < 2048; i += kSelThreads) rs.hist[i] = 0u;
     const int64_t f0 = h * (int64_t)C + p0, f1 = h * (int64_t)C + p1;
     const int64_t a0 = f0 & ~(int64_t)3;            // aligned start (inside the array)
     const int64_t a1 = f1 > a0 ? (f1 & ~(int64_t)3) : a0;
     shift = (int)(f0 - a0) - p0;
+    const int sl0 = p0 + shift, sl1 = p1 + shift;   // the span's slots
+    auto valid = [&](int slot) { return (unsigned)(slot - sl0) < (unsigned)(sl1 - sl0); };
     const float4* src = reinterpret_cast<const float4*>(scores + a0);
     const int nv = (int)((a1 - a0) >> 2);
+    __syncthreads();   // hist clear
+    // copy, and the group-max histogram of the first digit on the way (Ada-KV scores: the
+    // key of a score is its score_key)
     constexpr int U = 4;
-    for (int j0 = threadIdx.x; j0 < nv; j0 += U * kSelThreads) {
+    for (int jb = 0; jb < nv; jb += U * kSelThreads) {
       float4 x[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int j = j0 + u * kSelThreads;
+        const int j = jb + u * kSelThreads + (int)threadIdx.x;
         x[u] = j < nv ? src[j] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (j0 + u * kSelThreads < nv) stage4[j0 + u * kSelThreads] = x[u];
+      for (int u = 0; u < U; ++u) {
+        const int j = jb + u * kSelThreads + (int)threadIdx.x;
+        if (j < nv) stage4[j] = x[u];
+        const uint4 r = make_uint4(__float_as_uint(x[u].x), __float_as_uint(x[u].y),
+                                   __float_as_uint(x[u].z), __float_as_uint(x[u].w));
+        add_group_max<ScoreKeys>(rs, r, j, j < nv, valid);
+      }
     }
     for (int64_t f = a1 + threadIdx.x; f < f1; f += kSelThreads) sv[f - a0] = scores[f];
     __syncthreads();
+    if (a1 < f1 && threadIdx.x < 32) {   // the group of the scalar tail
+      const int q = nv;
+      add_group_max<ScoreKeys>(rs, reinterpret_cast<const uint4*>(sv)[q], q, threadIdx.x == 0,
+                               valid);
+    }
+    cl.barrier_wait(std::move(arrived));
   }
   auto sval = [&](int64_t i) -> float { return STAGED ? sv[i + shift] : S[i]; };
   const uint32_t* raw = reinterpret_cast<const uint32_t*>(sv);
@@ -138,7 +160,7 @@ compact_select(const float* __restrict__ scores, const float* __restrict__ crit,
     auto key = [&](int j) { return score_key(sval(j)); };
     const uint32_t n =
         STAGED ? cluster_topk_select_staged<kSelThreads, false, ScoreKeys>(
-                     raw, s0, s1, shift, Bg, kept, base, cap, nullptr, rs)
+                     raw, s0, s1, shift, Bg, kept, base, cap, nullptr, rs, true)
                : cluster_topk_select<kSelThreads, false>(p0, p1, Bg, key, no, kept, base, cap,
                                                          nullptr, rs);
     if (rank == 0 && threadIdx.x == 0 && n != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
@@ -151,7 +173,7 @@ compact_select(const float* __restrict__ scores, const float* __restrict__ crit,
     // stage-1 membership bits (each CTA writes and later reads the words of its own span)
     if (STAGED)
       cluster_topk_select_staged<kSelThreads, true, ScoreKeys>(raw, s0, s1, shift, K1, nullptr, 0,
-                                                                0, F, rs);
+                                                                0, F, rs, true);
     else
       cluster_topk_select<kSelThreads, true>(p0, p1, K1, key1, no, nullptr, 0, 0, F, rs);
     auto in1 = [&](int64_t i) { return ((F[i >> 5] >> (i & 31)) & 1u) != 0u; };
@@ -170,7 +192,7 @@ compact_select(const float* __restrict__ scores, const float* __restrict__ crit,
     auto forced2 = [&](int j) { return STAGED ? sk[j + shift] == 0u : in1(j); };
     const uint32_t n =
         STAGED ? cluster_topk_select_staged<kSelThreads, false, StoredKeys>(
-                     raw, s0, s1, shift, K2, kept, base, cap, nullptr, rs)
+                     raw, s0, s1, shift, K2, kept, base, cap, nullptr, rs, false)
                : cluster_topk_select<kSelThreads, false>(p0, p1, K2, key2, forced2, kept, base,
                                                          cap, nullptr, rs);
     if (rank == 0 && threadIdx.x == 0 && n != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
