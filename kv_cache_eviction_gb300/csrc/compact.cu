@@ -5,9 +5,20 @@
 // every head of a layer into one tensor (cu_seqlens-style offsets), filled by a
 // cache-update kernel.  CriticalKV: two-stage greedy selection, stage 1 by the
 // attention score, stage 2 by (A + eps) * ||(V W^O)_j||_1.
+//
+// The selection is one CTA per head and two streaming passes over the head's keys, through
+// a ring of bulk copies.  Pass A histograms the first digit (top 11 bits) of the largest key
+// of every aligned group of 4 positions; the bin g holding the K-th largest group maximum has
+// at least K groups at or above it, so at least K keys have a first digit >= g and tau, the
+// K-th largest key, has one too.  Pass B, walking the head backwards (its first chunks are
+// the ones pass A left in L2), collects every key with a first digit >= g (and every forced
+// position) into shared memory in position order.  The exact radix select and the ordered
+// emission then work on that short union alone.  A union that would not fit falls back to
+// the radix select over the whole head (a cluster of one CTA, keys read from global memory).
 #include <cstdlib>
 #include <cstring>
 
+#include "bulk_ring.cuh"
 #include "kv_internal.cuh"
 #include "radix_select.cuh"
 
@@ -16,8 +27,12 @@ namespace kv {
 namespace {
 constexpr int kScanThreads = 1024;
 constexpr int kSelThreads = 512;
-constexpr int kSelCl = 8;       // CTAs (one cluster) per head
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelStages = 4;
+constexpr int kSelStage = 16384;   // bytes per ring stage
+constexpr int kUnion = 4096;       // candidate (position, key) pairs a CTA can hold
 constexpr int kGatherThreads = 256;
+constexpr uint32_t kNoBin = 0xFFFFFFFFu;
 }
 
 // 64-bit inclusive block scan (one value per thread).
@@ -80,129 +95,413 @@ compact_offsets(const int32_t* __restrict__ head_budget, int64_t H, int Hkv, int
 }
 
 
-// One thread-block cluster of kSelCl CTAs per head: threshold(s), ordered kept positions,
-// window and reserve rows.  CTA r of the cluster owns candidate positions
-// [r * span, (r + 1) * span), span a multiple of 32 (whole words of the stage-1 bits).
-// STAGED: the CTA first copies its span of scores into shared memory (16-byte loads, the
-// copy aligned like the source) and every pass of the selection reads it from there, so the
-// scores cross HBM once; CriticalKV's stage-2 keys then replace the staged scores in place
-// (0 marks a stage-1 position).  Otherwise every pass reads the scores from global memory.
-template <bool STAGED>
+// Keys of a head in aligned groups of 4 flat positions: pos0 is the head position of the
+// group's first value (negative or >= C outside the head; the caller masks those).
+struct ScoreSrc {            // Ada-KV / LAVa scores; CriticalKV stage 1
+  static constexpr bool kTwo = false;
+  const float* S;            // the head's scores
+  __device__ void keys(const float4& x, const float4&, int, uint32_t (&k)[4], bool (&f)[4]) const {
+    k[0] = score_key(x.x); k[1] = score_key(x.y); k[2] = score_key(x.z); k[3] = score_key(x.w);
+    f[0] = f[1] = f[2] = f[3] = false;
+  }
+  __device__ uint32_t key_at(int i) const { return score_key(S[i]); }
+  __device__ bool forced_at(int) const { return false; }
+  // the largest key of a group whose four values all lie in the head (score_key is
+  // monotonic, and fmaxf skips a NaN as score_key maps it to the smallest key)
+  __device__ uint32_t full_max(const float4& x, const float4&, int) const {
+    return score_key(fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)));
+  }
+  // the values of a group whose key has a first digit >= g (1 <= g < 1024): for x > 0 the
+  // key is x's bit pattern, so the test is x >= the float whose bit pattern is g << 21
+  __device__ uint32_t cand_mask(const float4& x, const float4&, int, uint32_t g) const {
+    if (g == 0u) return 0xFu;
+    if (g >= 1024u) return 0u;
+    const float t = __uint_as_float(g << 21);
+    if (!(fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)) >= t)) return 0u;
+    return (x.x >= t ? 1u : 0u) | (x.y >= t ? 2u : 0u) | (x.z >= t ? 4u : 0u) |
+           (x.w >= t ? 8u : 0u);
+  }
+};
+struct KappaSrc {            // CriticalKV stage 2: stage-1 positions are forced, key 0
+  static constexpr bool kTwo = true;
+  const float* S;            // the head's scores
+  const float* Cn;           // the head's ||(V W^O)_j||_1
+  const uint32_t* F;         // the head's stage-1 bits
+  float eps;
+  int C;
+  __device__ bool in1(int p) const {
+    return p >= 0 && p < C && ((__ldcg(F + (p >> 5)) >> (p & 31)) & 1u) != 0u;
+  }
+  __device__ uint32_t kappa_key(float s, float c) const {
+    return score_key(__fmul_rn(__fadd_rn(s, eps), c)) + 1u;
+  }
+  __device__ void keys(const float4& x, const float4& y, int pos0, uint32_t (&k)[4],
+                       bool (&f)[4]) const {
+    const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      f[c] = in1(pos0 + c);
+      k[c] = f[c] ? 0u : kappa_key(xs[c], ys[c]);
+    }
+  }
+  __device__ uint32_t key_at(int i) const { return in1(i) ? 0u : kappa_key(S[i], Cn[i]); }
+  __device__ bool forced_at(int i) const { return in1(i); }
+  __device__ uint32_t full_max(const float4& x, const float4& y, int pos0) const {
+    uint32_t k[4];
+    bool f[4];
+    keys(x, y, pos0, k, f);
+    return max(max(k[0], k[1]), max(k[2], k[3]));
+  }
+  __device__ uint32_t cand_mask(const float4& x, const float4& y, int pos0, uint32_t g) const {
+    uint32_t k[4];
+    bool f[4];
+    keys(x, y, pos0, k, f);
+    uint32_t cm = 0u;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) cm |= (f[c] || (k[c] >> 21) >= g) ? 1u << c : 0u;
+    return cm;
+  }
+};
+
+struct HeadSelSmem {
+  uint32_t hist[2048];
+  uint32_t scr[2 * 32 + 8];
+  uint32_t res[2];
+  int32_t upos[kUnion];       // the union, in position order, fills [fill, kUnion)
+  uint32_t ukey[kUnion];
+  uint64_t full[kSelStages];
+};
+using SelRing = BulkRing<kSelStages, kSelStage>;
+
+// Ordered selection of one head's positions [0, C), keys and forced positions from `src`
+// (staged values from stream base pointers s0 / s1 = flat index 0 of the arrays).  keep(j)
+// = forced(j) || key(j) > tau || (key(j) == tau && j is among the keq lowest tau-equal
+// positions), tau the K-th largest key.  Kept positions go in ascending order to
+// kept[base + r] (rows >= cap skipped) or, BITS, as bits of bits[] (the head's words).
+// Returns the number kept; ok turns false (the same in every thread) if a wait gave up.
+template <bool BITS, class Src>
+__device__ uint32_t select_head(SelRing& R, HeadSelSmem& sm, unsigned char* ring_mem,
+                                const Src& src, const float* s0, const float* s1, int64_t flat0,
+                                int C, int64_t K, int32_t* kept, int64_t base, int64_t cap,
+                                uint32_t* bits, bool streaming, bool& ok) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t below = (1u << lane) - 1u;
+  const bool any = K > 0;
+  if (!any && !Src::kTwo) {   // nothing to select and nothing forced
+    if (BITS)
+      for (int wd = threadIdx.x; wd < (C + 31) / 32; wd += kSelThreads) bits[wd] = 0u;
+    __syncthreads();
+    return 0;
+  }
+  if (streaming) {
+    // the aligned window [a0, a1) of flat indices goes through the ring; the < 4 keys of
+    // the head past a1 (the tail) are read directly
+    const int64_t a0 = flat0 & ~(int64_t)3;
+    const int64_t a1 = max(a0, (flat0 + C) & ~(int64_t)3);
+    const int64_t tail0 = max(a1, flat0), tailn = flat0 + C - tail0;
+    const int64_t nbytes = (a1 - a0) * 4;
+    const unsigned char* w0 = reinterpret_cast<const unsigned char*>(s0 + a0);
+    const unsigned char* w1 = Src::kTwo ? reinterpret_cast<const unsigned char*>(s1 + a0) : nullptr;
+    constexpr int kGroups = kSelStage / 16 / (Src::kTwo ? 2 : 1);   // per chunk
+    // group j of a chunk at byte offset off: its keys, and which of them lie in the head
+    auto group = [&](const unsigned char* st0, const unsigned char* st1, int64_t off, int j,
+                     bool in, uint32_t (&k)[4], bool (&f)[4]) -> uint32_t {
+      const float4 x = in ? reinterpret_cast<const float4*>(st0)[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 y = (Src::kTwo && in) ? reinterpret_cast<const float4*>(st1)[j]
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+      const int pos0 = (int)(a0 + off / 4 + 4 * j - flat0);
+      src.keys(x, y, pos0, k, f);
+      uint32_t vm = 0u;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) vm |= (in && (unsigned)(pos0 + c) < (unsigned)C) ? 1u << c : 0u;
+      return vm;
+    };
+
+    // ---- pass A: first digit of every group's largest key
+    uint32_t g = 2048u;   // with K == 0 only forced positions are candidates
+    if (any) {
+      for (int i = threadIdx.x; i < 2048; i += kSelThreads) sm.hist[i] = 0u;
+      __syncthreads();
+      ok = ring_pass(R, w0, w1, nbytes, false,
+                     [&](const unsigned char* st0, const unsigned char* st1, int64_t off,
+                         uint32_t bytes) {
+        const int ng = (int)(bytes / 16);
+        for (int jb = 0; jb < kGroups; jb += kSelThreads) {
+          const int j = jb + (int)threadIdx.x;
+          const int pos0 = (int)(a0 + off / 4 + 4 * j - flat0);
+          uint32_t bin = kNoBin;
+          if (j < ng) {
+            const float4 x = reinterpret_cast<const float4*>(st0)[j];
+            const float4 y = Src::kTwo ? reinterpret_cast<const float4*>(st1)[j] : x;
+            if (pos0 >= 0 && pos0 + 3 < C) {
+              bin = src.full_max(x, y, pos0) >> 21;
+            } else {   // the head's first or last group
+              uint32_t k[4];
+              bool f[4];
+              src.keys(x, y, pos0, k, f);
+              uint32_t m = 0u;
+              bool have = false;
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                if ((unsigned)(pos0 + c) < (unsigned)C) {
+                  m = max(m, k[c]);
+                  have = true;
+                }
+              bin = have ? m >> 21 : kNoBin;
+            }
+          }
+          hist_add_runs(sm.hist, bin);
+        }
+      });
+      if (!ok) return 0;
+      if (warp == 0) {   // the tail's keys form one more group
+        uint32_t m = 0u;
+        for (int64_t i = tail0; i < tail0 + tailn; ++i) m = max(m, src.key_at((int)(i - flat0)));
+        hist_add_runs(sm.hist, (lane == 0 && tailn > 0) ? m >> 21 : kNoBin);
+      }
+      __syncthreads();
+      block_pick<kSelThreads>(sm.hist, 2048, (uint32_t)K, sm.scr, sm.res);
+      __syncthreads();
+      g = sm.res[0];
+      __syncthreads();
+    }
+
+    // ---- pass B: the union of keys with first digit >= g and forced positions, filled from
+    // the end of the buffer backwards (chunks come last to first), so it ends up ascending
+    uint32_t fill = kUnion;
+    bool over = false;
+    if (threadIdx.x == 0) {
+      uint32_t fl = kUnion;
+      for (int64_t i = tail0 + tailn - 1; i >= tail0; --i) {
+        const int p = (int)(i - flat0);
+        const uint32_t k = src.key_at(p);
+        if (src.forced_at(p) || (k >> 21) >= g) {
+          --fl;
+          sm.upos[fl] = p;
+          sm.ukey[fl] = k;
+        }
+      }
+      sm.res[0] = fl;
+    }
+    __syncthreads();
+    fill = sm.res[0];
+    __syncthreads();
+    constexpr int kPerWarp = kGroups / kSelWarps;   // groups of a chunk per warp, in order
+    ok = ring_pass(R, w0, w1, nbytes, true,
+                   [&](const unsigned char* st0, const unsigned char* st1, int64_t off,
+                       uint32_t bytes) {
+      const int ng = (int)(bytes / 16);
+      auto cand = [&](int j) -> uint32_t {
+        if (j >= ng) return 0u;
+        const float4 x = reinterpret_cast<const float4*>(st0)[j];
+        const float4 y = Src::kTwo ? reinterpret_cast<const float4*>(st1)[j] : x;
+        const int pos0 = (int)(a0 + off / 4 + 4 * j - flat0);
+        uint32_t cm = src.cand_mask(x, y, pos0, g);
+        if (pos0 < 0 || pos0 + 3 >= C) {   // the head's first or last group
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if ((unsigned)(pos0 + c) >= (unsigned)C) cm &= ~(1u << c);
+        }
+        return cm;
+      };
+      uint32_t cmu[kPerWarp / 32];   // candidate masks of this lane's groups
+      uint32_t wc = 0;                // this warp's candidates in the chunk
+#pragma unroll
+      for (int u = 0; u < kPerWarp / 32; ++u) {
+        cmu[u] = cand(warp * kPerWarp + u * 32 + lane);
+        wc += __popc(cmu[u]);
+      }
+      wc = warp_sum_u(wc);
+      if (lane == 0) sm.scr[warp] = wc;
+      __syncthreads();
+      // the warps' counts, scanned across the lanes of every warp
+      uint32_t c = lane < kSelWarps ? sm.scr[lane] : 0u, ci = c;
+#pragma unroll
+      for (int d = 1; d < kSelWarps; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, ci, d);
+        if (lane >= d) ci += y;
+      }
+      const uint32_t T = __shfl_sync(0xFFFFFFFFu, ci, kSelWarps - 1);
+      const uint32_t before = __shfl_sync(0xFFFFFFFFu, ci - c, warp);
+      if (T == 0u) return;   // the same in every thread
+      if (over || T > fill) {
+        over = true;         // the same in every thread
+        return;
+      }
+      uint32_t o = fill - T + before;
+#pragma unroll
+      for (int u = 0; u < kPerWarp / 32; ++u) {
+        const int j = warp * kPerWarp + u * 32 + lane;
+        const uint32_t n = __popc(cmu[u]);
+        uint32_t incl = n;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+          if (lane >= d) incl += y;
+        }
+        if (cmu[u]) {
+          uint32_t k[4];
+          bool f[4];
+          (void)group(st0, st1, off, j, true, k, f);
+          uint32_t q = o + incl - n;
+          const int pos0 = (int)(a0 + off / 4 + 4 * j - flat0);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            if ((cmu[u] >> c) & 1u) {
+              sm.upos[q] = pos0 + c;
+              sm.ukey[q] = k[c];
+              ++q;
+            }
+          }
+        }
+        o += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+      fill -= T;
+    });
+    if (!ok) return 0;
+    if (!over) {
+      const int u0 = (int)fill, nu = kUnion - (int)fill;
+      // ---- tau and keq over the union (every key above tau, and tau's first digit, is in it)
+      uint32_t prefix = 0, mask = 0, krem = any ? (uint32_t)K : 0u;
+      if (any) {
+#pragma unroll 1
+        for (int pass = 0; pass < 3; ++pass) {
+          const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+          const int nb = pass == 2 ? 1024 : 2048;
+          for (int i = threadIdx.x; i < nb; i += kSelThreads) sm.hist[i] = 0u;
+          __syncthreads();
+          for (int b0 = 0; b0 < nu; b0 += kSelThreads) {
+            const int t = b0 + (int)threadIdx.x;
+            const uint32_t k = t < nu ? sm.ukey[u0 + t] : 0u;
+            // (forced positions have key 0: counted like every key, as in the full select)
+            const bool in = t < nu && (pass == 0 ? (k >> 21) >= g : (k & mask) == prefix);
+            hist_add_runs(sm.hist, in ? (k >> sh) & (uint32_t)(nb - 1) : kNoBin);
+          }
+          __syncthreads();
+          block_pick<kSelThreads>(sm.hist, nb, krem, sm.scr, sm.res);
+          __syncthreads();
+          prefix |= sm.res[0] << sh;
+          mask |= (uint32_t)(nb - 1) << sh;
+          krem = sm.res[1];
+          __syncthreads();
+        }
+      }
+      const uint32_t tau = any ? prefix : 0xFFFFFFFFu;   // no key equals 0xFFFFFFFF
+      const uint32_t keq = any ? krem : 0u;
+      // ---- ordered emission: warp w takes a contiguous slice of the union
+      const int per = (nu + kSelWarps - 1) / kSelWarps;
+      const int e0 = u0 + min(nu, warp * per), e1 = u0 + min(nu, warp * per + per);
+      uint32_t nkeep = 0, neq = 0;
+      for (int t = e0 + lane; t < e1; t += 32) {
+        const uint32_t k = sm.ukey[t];
+        const bool f = src.forced_at(sm.upos[t]);
+        nkeep += (f || k > tau) ? 1u : 0u;
+        neq += (!f && k == tau) ? 1u : 0u;
+      }
+      nkeep = warp_sum_u(nkeep);
+      neq = warp_sum_u(neq);
+      if (lane == 0) {
+        sm.scr[warp] = nkeep;
+        sm.scr[32 + warp] = neq;
+      }
+      if (BITS)
+        for (int wd = threadIdx.x; wd < (C + 31) / 32; wd += kSelThreads) bits[wd] = 0u;
+      __syncthreads();
+      uint32_t eqc = 0, outc = 0, total = 0;
+      {
+        uint32_t eq = 0;
+        for (int w = 0; w < kSelWarps; ++w) {
+          const uint32_t e = sm.scr[32 + w];
+          const uint32_t take = eq >= keq ? 0u : (keq - eq < e ? keq - eq : e);
+          if (w == warp) {
+            eqc = eq;
+            outc = total;
+          }
+          total += sm.scr[w] + take;
+          eq += e;
+        }
+      }
+      for (int tb = e0; tb < e1; tb += 32) {
+        const int t = tb + lane;
+        const bool in = t < e1;
+        const uint32_t k = in ? sm.ukey[t] : 0u;
+        const int j = in ? sm.upos[t] : 0;
+        const bool f = in && src.forced_at(j);
+        const bool iseq = in && !f && k == tau;
+        bool keep = in && (f || k > tau);
+        const uint32_t meq = __ballot_sync(0xFFFFFFFFu, iseq);
+        if (iseq && eqc + __popc(meq & below) < keq) keep = true;
+        const uint32_t mk = __ballot_sync(0xFFFFFFFFu, keep);
+        if (BITS) {
+          if (keep) atomicOr(bits + (j >> 5), 1u << (j & 31));
+        } else if (keep) {
+          const int64_t row = base + outc + __popc(mk & below);
+          if (row < cap) kept[row] = j;
+        }
+        eqc += __popc(meq);
+        outc += __popc(mk);
+      }
+      __syncthreads();   // the union and scr are reused by the next selection
+      return total;
+    }
+  }
+  // ---- the radix select over the whole head, keys read from global memory; the ring's
+  // memory (no copy in flight) holds its state
+  ClusterSelectSmem& cs = *reinterpret_cast<ClusterSelectSmem*>(ring_mem);
+  const uint32_t total = cluster_topk_select<kSelThreads, BITS>(
+      0, C, K, [&](int j) { return src.key_at(j); }, [&](int j) { return src.forced_at(j); },
+      kept, base, cap, bits, cs);
+  __syncthreads();
+  return total;
+}
+
+// One CTA per head: threshold(s), ordered kept positions, window and reserve rows.
+template <bool CRIT>
 __global__ void __launch_bounds__(kSelThreads, 2)
-compact_select(const float* __restrict__ scores, const float* __restrict__ crit, uint32_t can,
-               uint32_t cad, float ceps, const int32_t* __restrict__ lens,
-               const int64_t* __restrict__ cu, int Hkv, int C, int w, int reserve,
-               int32_t* __restrict__ kept, int64_t cap, uint32_t* __restrict__ flags,
-               int64_t words, WsHeader* hdr) {
-  __shared__ ClusterSelectSmem rs;
-  extern __shared__ float4 stage4[];
-  cg::cluster_group cl = cg::this_cluster();
-  const int rank = (int)cl.block_rank(), ncta = (int)cl.num_blocks();
-  const int64_t h = blockIdx.y;
+head_select(const float* __restrict__ scores, const float* __restrict__ crit, uint32_t can,
+            uint32_t cad, float ceps, const int32_t* __restrict__ lens,
+            const int64_t* __restrict__ cu, int Hkv, int C, int w, int reserve,
+            int32_t* __restrict__ kept, int64_t cap, uint32_t* __restrict__ flags, int64_t words,
+            int streaming, WsHeader* hdr) {
+  __shared__ HeadSelSmem sm;
+  extern __shared__ __align__(128) unsigned char ring_mem[];
+  const int64_t h = blockIdx.x;
   const int64_t seg = h / Hkv;
   const int g = (int)(h - seg * Hkv);
   const int64_t base = cu[seg * (Hkv + 1) + g];
   const int64_t Bg = (int64_t)lens[h] - w;   // lens was clamped to [w, n]
-  const float* S = scores + h * (int64_t)C;
-  const int span = ((C + ncta - 1) / ncta + 31) & ~31;
-  const int p0 = min(C, rank * span), p1 = min(C, p0 + span);
-  auto no = [](int) { return false; };
-  float* sv = reinterpret_cast<float*>(stage4);
-  int shift = 0;   // sv[i + shift] holds S[i] for i in [p0, p1)
-  if (STAGED) {
-    // rank 0's cluster histogram starts clear: cleared here, published by the cluster barrier
-    // whose wait comes after the staging
-    if (rank == 0)
-      for (int i = threadIdx.x; i < 2048; i += kSelThreads) rs.ghist[i] = 0u;
-    auto arrived = cl.barrier_arrive();
-    for (int i = threadIdx.x; i < 2048; i += kSelThreads) rs.hist[i] = 0u;
-    const int64_t f0 = h * (int64_t)C + p0, f1 = h * (int64_t)C + p1;
-    const int64_t a0 = f0 & ~(int64_t)3;            // aligned start (inside the array)
-    const int64_t a1 = f1 > a0 ? (f1 & ~(int64_t)3) : a0;
-    shift = (int)(f0 - a0) - p0;
-    const int sl0 = p0 + shift, sl1 = p1 + shift;   // the span's slots
-    auto valid = [&](int slot) { return (unsigned)(slot - sl0) < (unsigned)(sl1 - sl0); };
-    const float4* src = reinterpret_cast<const float4*>(scores + a0);
-    const int nv = (int)((a1 - a0) >> 2);
-    __syncthreads();   // hist clear
-    // copy, and the group-max histogram of the first digit on the way (Ada-KV scores: the
-    // key of a score is its score_key)
-    constexpr int U = 4;
-    for (int jb = 0; jb < nv; jb += U * kSelThreads) {
-      float4 x[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int j = jb + u * kSelThreads + (int)threadIdx.x;
-        x[u] = j < nv ? src[j] : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int j = jb + u * kSelThreads + (int)threadIdx.x;
-        if (j < nv) stage4[j] = x[u];
-        const uint4 r = make_uint4(__float_as_uint(x[u].x), __float_as_uint(x[u].y),
-                                   __float_as_uint(x[u].z), __float_as_uint(x[u].w));
-        add_group_max<ScoreKeys>(rs, r, j, j < nv, valid);
-      }
-    }
-    for (int64_t f = a1 + threadIdx.x; f < f1; f += kSelThreads) sv[f - a0] = scores[f];
-    __syncthreads();
-    if (a1 < f1 && threadIdx.x < 32) {   // the group of the scalar tail
-      const int q = nv;
-      add_group_max<ScoreKeys>(rs, reinterpret_cast<const uint4*>(sv)[q], q, threadIdx.x == 0,
-                               valid);
-    }
-    cl.barrier_wait(std::move(arrived));
-  }
-  auto sval = [&](int64_t i) -> float { return STAGED ? sv[i + shift] : S[i]; };
-  const uint32_t* raw = reinterpret_cast<const uint32_t*>(sv);
-  const int s0 = p0 + shift, s1 = p1 + shift;   // the span's slots when staged
-  if (crit == nullptr) {
-    auto key = [&](int j) { return score_key(sval(j)); };
-    const uint32_t n =
-        STAGED ? cluster_topk_select_staged<kSelThreads, false, ScoreKeys>(
-                     raw, s0, s1, shift, Bg, kept, base, cap, nullptr, rs, true)
-               : cluster_topk_select<kSelThreads, false>(p0, p1, Bg, key, no, kept, base, cap,
-                                                         nullptr, rs);
-    if (rank == 0 && threadIdx.x == 0 && n != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
+  const int64_t flat0 = h * (int64_t)C;
+  SelRing R;
+  R.init(ring_mem, sm.full);
+  __syncthreads();
+  bool ok = true;
+  uint32_t n = 0;
+  if (!CRIT) {
+    const ScoreSrc src{scores + flat0};
+    n = select_head<false>(R, sm, ring_mem, src, scores, nullptr, flat0, C, Bg, kept, base, cap,
+                           nullptr, streaming != 0, ok);
   } else {
-    const float* Cn = crit + h * (int64_t)C;
     uint32_t* F = flags + h * words;
     const int64_t K1 = ((int64_t)can * Bg) / cad;
     const int64_t K2 = Bg - K1;
-    auto key1 = [&](int j) { return score_key(sval(j)); };
-    // stage-1 membership bits (each CTA writes and later reads the words of its own span)
-    if (STAGED)
-      cluster_topk_select_staged<kSelThreads, true, ScoreKeys>(raw, s0, s1, shift, K1, nullptr, 0,
-                                                                0, F, rs, true);
-    else
-      cluster_topk_select<kSelThreads, true>(p0, p1, K1, key1, no, nullptr, 0, 0, F, rs);
-    auto in1 = [&](int64_t i) { return ((F[i >> 5] >> (i & 31)) & 1u) != 0u; };
-    auto key2g = [&](int64_t i) -> uint32_t {
-      if (in1(i)) return 0u;
-      const float kap = __fmul_rn(__fadd_rn(sval(i), ceps), Cn[i]);
-      return score_key(kap) + 1u;
-    };
-    uint32_t* sk = reinterpret_cast<uint32_t*>(sv);
-    if (STAGED) {
-      // the bits were written by this CTA before the barrier that ends the selection
-      for (int i = p0 + threadIdx.x; i < p1; i += kSelThreads) sk[i + shift] = key2g(i);
-      __syncthreads();
+    const ScoreSrc src1{scores + flat0};
+    (void)select_head<true>(R, sm, ring_mem, src1, scores, nullptr, flat0, C, K1, nullptr, 0, 0,
+                            F, streaming != 0, ok);
+    __syncthreads();   // the stage-1 bits are complete
+    if (ok) {
+      const KappaSrc src2{scores + flat0, crit + flat0, F, ceps, C};
+      n = select_head<false>(R, sm, ring_mem, src2, scores, crit, flat0, C, K2, kept, base, cap,
+                             nullptr, streaming != 0, ok);
     }
-    auto key2 = [&](int j) -> uint32_t { return STAGED ? sk[j + shift] : key2g(j); };
-    auto forced2 = [&](int j) { return STAGED ? sk[j + shift] == 0u : in1(j); };
-    const uint32_t n =
-        STAGED ? cluster_topk_select_staged<kSelThreads, false, StoredKeys>(
-                     raw, s0, s1, shift, K2, kept, base, cap, nullptr, rs, false)
-               : cluster_topk_select<kSelThreads, false>(p0, p1, K2, key2, forced2, kept, base,
-                                                         cap, nullptr, rs);
-    if (rank == 0 && threadIdx.x == 0 && n != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
   }
-  for (int t = rank * kSelThreads + threadIdx.x; t < w + reserve; t += ncta * kSelThreads) {
+  if (threadIdx.x == 0) {
+    if (!ok) raise_dev(hdr, DEV_WAIT_TIMEOUT, 0x800u + (unsigned)(h & 0xFF));
+    else if (n != (uint32_t)Bg) raise_dev(hdr, DEV_SELECT, (unsigned)h);
+  }
+  for (int t = threadIdx.x; t < w + reserve; t += kSelThreads) {
     const int64_t row = base + Bg + t;
     if (row < cap) kept[row] = t < w ? C + t : -1;
   }
-  // rank 0's shared memory was read by the other CTAs: none leaves before all are done
-  cl.sync();
 }
 
 // Copy the kept rows of K and V into the flat buffers, 16 bytes per thread.
@@ -235,8 +534,9 @@ compact_gather(const char* __restrict__ k, const char* __restrict__ v,
   }
 }
 
-// KVEVICT_SELECT_PATH=global forces the selection that reads the scores from global memory
-// on every pass (the one spans too long for shared memory take); tests compare the two.
+// KVEVICT_SELECT_PATH=global forces the radix select over the whole head with the keys read
+// from global memory (the path a candidate union too long for shared memory takes); tests
+// compare the two.
 static bool global_select_forced() {
   const char* e = std::getenv("KVEVICT_SELECT_PATH");
   return e != nullptr && std::strcmp(e, "global") == 0;
@@ -261,39 +561,38 @@ cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const f
   const int64_t H = s.units();
   compact_offsets<<<1, kScanThreads, 0, st>>>(head_budget, H, s.Hkv, s.w, s.n, reserve, cap, cu,
                                                lens, hdr);
-  {
+  if (H > 0) {
+    const int C = s.C();
+    // the bulk copies need 16-byte aligned score (and norm) arrays
+    const bool streaming = C > 0 && !global_select_forced() &&
+                           (reinterpret_cast<uintptr_t>(scores) & 15u) == 0 &&
+                           (crit == nullptr || (reinterpret_cast<uintptr_t>(crit) & 15u) == 0);
+    const size_t ring_bytes = (size_t)kSelStages * kSelStage;
+    auto kern = crit ? head_select<true> : head_select<false>;
+    static bool opted[2] = {false, false};
+    if (!opted[crit ? 1 : 0]) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)ring_bytes);
+      if (e != cudaSuccess) return e;
+      opted[crit ? 1 : 0] = true;
+    }
+    // a cluster of one CTA: the whole-head fallback's cluster barriers are the block's own
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(kSelCl, (unsigned)H);
+    cfg.gridDim = dim3((unsigned)H);
     cfg.blockDim = dim3(kSelThreads);
+    cfg.dynamicSmemBytes = ring_bytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kSelCl;
+    attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // staged when a span (plus the alignment slack) fits next to the selection's own state
-    const int C = s.C();
-    const int span = ((C + kSelCl - 1) / kSelCl + 31) & ~31;
-    const size_t stage_bytes = align_up(((size_t)span + 8) * sizeof(float), 16);
-    const bool staged = C > 0 && !global_select_forced() &&
-                        stage_bytes + sizeof(ClusterSelectSmem) + 1024 <= max_smem_optin();
-    auto kern = staged ? compact_select<true> : compact_select<false>;
-    if (staged) {
-      static size_t opted = 0;   // the largest size opted in so far
-      if (stage_bytes > opted) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)stage_bytes);
-        if (e != cudaSuccess) return e;
-        opted = stage_bytes;
-      }
-      cfg.dynamicSmemBytes = stage_bytes;
-    }
     cudaError_t e = cudaLaunchKernelEx(
-        &cfg, kern, scores, crit, can, cad, ceps, (const int32_t*)lens,
-        (const int64_t*)cu, s.Hkv, C, s.w, reserve, kept, cap,
-        reinterpret_cast<uint32_t*>(ws + p.off_flags), p.flag_words, hdr);
+        &cfg, kern, scores, crit, can, cad, ceps, (const int32_t*)lens, (const int64_t*)cu, s.Hkv,
+        C, s.w, reserve, kept, cap, reinterpret_cast<uint32_t*>(ws + p.off_flags), p.flag_words,
+        streaming ? 1 : 0, hdr);
     if (e != cudaSuccess) return e;
   }
   const int row_bytes = s.d * s.esize();
