@@ -6,85 +6,54 @@
 // layer budgets: each layer's share of the sequence's total is proportional to the entropy
 // of its normalised scores.
 //
-// The layer-wide top-B' is a radix select on the fp32 bit patterns (no sort): three
-// passes of 11/11/10 bits, each a histogram over every layer at once (many CTAs per layer,
-// shared-memory counts merged into per-layer global bins), then a sweep that counts, per
-// head, the keys above the threshold and the keys equal to it.  Each sweep is one wave of
-// CTAs reading 16-byte vectors; the last CTA of a layer to finish picks the digit of the
-// pass (or, after the count, blends the head budgets), so no launch is spent on per-layer
-// bookkeeping.  Consecutive sweeps walk their chunks in opposite directions, so each one
-// starts on the part of the scores the previous one left in L2.
+// Two sweeps over the scores, each one wave of CTAs streaming its chunk of a layer through a
+// ring of bulk copies, and no sort:
+//  1. per layer, a histogram of the first digit (top 11 bits of the fp32 bit pattern) of the
+//     largest key of every aligned group of 4, and (LAVa) the partial sums of s and s ln s;
+//  2. after the layer budgets, the bin g holding the B'-th largest group maximum bounds tau,
+//     the B'-th largest key, from below: at least B' groups, so at least B' keys, have a
+//     first digit >= g.  The second sweep lists every key with a first digit >= g, in
+//     position order, per CTA.  The last CTA of the layer to finish finds tau and the
+//     tau-equal quota with an exact radix select (11/11/10 bits) over that union, counts
+//     each head's keys above and at tau from it, and blends the head budgets.
+// A union longer than its capacity (large budgets) makes that CTA run the radix select over
+// every key of the layer instead.  Consecutive sweeps walk their chunks in opposite
+// directions, so the second starts on the part of the scores the first left in L2.
+#include "bulk_ring.cuh"
 #include "kv_internal.cuh"
+#include "radix_select.cuh"
 
 namespace kv {
 
 namespace {
 constexpr int kThreads = 256;
-constexpr int kMinBlocks = 6;    // resident CTAs per SM the sweeps are sized for
-constexpr int kU = 4;            // 16-byte loads in flight per thread per step
+constexpr int kWarps = kThreads / 32;
+constexpr int kMinBlocks = 3;        // resident CTAs per SM the sweeps are sized for
+constexpr int kRingStages = 4;
+constexpr int kRingStage = 12288;    // bytes per ring stage (768 groups of 4 keys)
+constexpr int kRingBytes = kRingStages * kRingStage;
+constexpr int kGroups = kRingStage / 16;   // 4-key groups per ring stage
+using SweepRing = BulkRing<kRingStages, kRingStage>;
 constexpr int kBins = 2048;
 constexpr int kMaxHeads = 256;
-
-struct RadixState {          // one per (sequence, layer)
-  uint32_t prefix, mask;     // resolved high bits of the threshold key
-  uint32_t krem;             // keys still to take from the current prefix class
-  uint32_t active;           // 0 when B' == 0 (nothing to select)
-};
-
-__device__ __forceinline__ int pass_shift(int pass) { return pass == 0 ? 21 : (pass == 1 ? 10 : 0); }
-__device__ __forceinline__ int pass_bins(int pass) { return pass == 2 ? 1024 : 2048; }
-
-// Visits the keys x[i0, i1): fn(value, ok, i) is called the same number of times by every
-// thread of the block (warp votes inside fn stay convergent); ok is false for padding, i is
-// the key's index.  The
-// 16-byte aligned middle is read as float4, kU vectors in flight per thread; `rev` walks
-// the steps from the end of the range.
-template <typename Fn>
-__device__ __forceinline__ void sweep_keys(const float* __restrict__ x, int64_t i0, int64_t i1,
-                                           bool rev, Fn&& fn) {
-  const uintptr_t addr = reinterpret_cast<uintptr_t>(x + i0);
-  int64_t a = i0 + (int64_t)(((16u - (uint32_t)(addr & 15u)) & 15u) >> 2);
-  if (a > i1) a = i1;
-  const int64_t nv = (i1 - a) >> 2;
-  const int64_t b = a + nv * 4;
-  {
-    const int64_t ih = i0 + threadIdx.x, it = b + threadIdx.x;
-    const bool okh = ih < a, okt = it < i1;
-    const float xh = okh ? x[ih] : 0.0f, xt = okt ? x[it] : 0.0f;
-    fn(xh, okh, ih);
-    fn(xt, okt, it);
-  }
-  const float4* xv = reinterpret_cast<const float4*>(x + a);
-  const int64_t step = (int64_t)kU * blockDim.x;
-  const int64_t nsteps = cdiv(nv, step);
-  for (int64_t s = 0; s < nsteps; ++s) {
-    const int64_t base = (rev ? nsteps - 1 - s : s) * step + threadIdx.x;
-    float4 v[kU];
-#pragma unroll
-    for (int k = 0; k < kU; ++k) {
-      const int64_t j = base + (int64_t)k * blockDim.x;
-      v[k] = j < nv ? xv[j] : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int k = 0; k < kU; ++k) {
-      const int64_t j = base + (int64_t)k * blockDim.x;
-      const bool ok = j < nv;
-      const int64_t i = a + 4 * j;
-      fn(v[k].x, ok, i);
-      fn(v[k].y, ok, i + 1);
-      fn(v[k].z, ok, i + 2);
-      fn(v[k].w, ok, i + 3);
-    }
-  }
-}
+constexpr int kMaxChunks = 512;      // CTAs per layer
+constexpr int64_t kUnionPerLayer = 65536;   // candidate keys a layer's union can hold
+constexpr uint32_t kNoBin = 0xFFFFFFFFu;
 
 // Keys per CTA of a layer: a multiple of 4, so the chunks of an aligned layer are aligned.
-__device__ __forceinline__ int64_t chunk_len(int64_t N, int nch) {
+__host__ __device__ __forceinline__ int64_t chunk_len(int64_t N, int nch) {
   return cdiv(cdiv(N, nch), 4) * 4;
 }
 
+// The index a >= i0 of x's first 16-byte aligned key at or after x + i0 (at most i1).
+__device__ __forceinline__ int64_t aligned_from(const float* x, int64_t i0, int64_t i1) {
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(x + i0);
+  const int64_t a = i0 + (int64_t)(((16u - (uint32_t)(addr & 15u)) & 15u) >> 2);
+  return a < i1 ? a : i1;
+}
+
 // True in every thread of the CTA that is the n-th and last of its layer to get here; its
-// reads of the other CTAs' atomics come after a fence.  The counter is left at zero.
+// reads of the other CTAs' results come after a fence.  The counter is left at zero.
 __device__ __forceinline__ bool last_of_layer(uint32_t* done, uint32_t n, uint32_t* flag) {
   __threadfence();
   __syncthreads();
@@ -97,58 +66,6 @@ __device__ __forceinline__ bool last_of_layer(uint32_t* done, uint32_t n, uint32
   const bool last = *flag != 0u;
   if (last) __threadfence();
   return last;
-}
-
-// The digit of pass `pass` that holds the krem-th largest key of the layer (bins counted
-// from the top) and krem's rank inside it; G is the layer's global histogram, which is
-// cleared for the next pass.  All threads call it; scr holds >= 34 words.
-__device__ void pick_digit(uint32_t* G, int pass, uint32_t krem, uint32_t* scr, WsHeader* hdr,
-                           unsigned seg, uint32_t& bin_out, uint32_t& kr_out) {
-  const int nb = pass_bins(pass);
-  const int per = nb / (int)blockDim.x;   // 8 or 4
-  uint32_t c[kBins / kThreads];
-  uint32_t local = 0;
-#pragma unroll
-  for (int q = 0; q < kBins / kThreads; ++q) {
-    c[q] = q < per ? __ldcg(G + nb - 1 - ((int)threadIdx.x * per + q)) : 0u;
-    local += c[q];
-  }
-  if (threadIdx.x == 0) { scr[32] = 0u; scr[33] = 0u; }
-  uint32_t total;
-  const uint32_t incl = block_incl_scan(local, scr, &total);   // ends with a barrier
-  const uint32_t excl = incl - local;
-  if (excl < krem && krem <= incl) {
-    uint32_t acc = excl;
-#pragma unroll
-    for (int q = 0; q < kBins / kThreads; ++q) {
-      if (q < per && acc < krem) {
-        if (acc + c[q] >= krem) {
-          scr[32] = (uint32_t)(nb - 1 - ((int)threadIdx.x * per + q));
-          scr[33] = krem - acc;
-        }
-        acc += c[q];
-      }
-    }
-  }
-  if (threadIdx.x == 0 && krem > total) raise_dev(hdr, DEV_SELECT, seg);
-  for (int i = threadIdx.x; i < nb; i += blockDim.x) G[i] = 0u;
-  __syncthreads();
-  bin_out = scr[32];
-  kr_out = scr[33];
-  __syncthreads();
-}
-
-__device__ __forceinline__ void advance(RadixState& r, int pass, uint32_t bin, uint32_t kr) {
-  r.prefix |= bin << pass_shift(pass);
-  r.mask |= (uint32_t)(pass_bins(pass) - 1) << pass_shift(pass);
-  r.krem = kr;
-}
-
-__device__ __forceinline__ void merge_hist(const uint32_t* hist, uint32_t* G, int nb) {
-  for (int i = threadIdx.x; i < nb; i += blockDim.x) {
-    const uint32_t c = hist[i];
-    if (c) atomicAdd(&G[i], c);
-  }
 }
 
 // Block-wide sums; every thread gets the total (the same order for every thread).
@@ -173,70 +90,133 @@ __device__ __forceinline__ long long block_sum_ll(long long v, long long* red) {
 }
 }  // namespace
 
-// LAVa entropy mode, first sweep: the first digit's histogram (it does not depend on B', so
-// it is taken before the layer budgets exist) and per-CTA partial sums of s and s*ln(s)
-// (float terms, float runs of 16 added into fp64).
+// ---------------------------------------------------------------------------------------
+// Sweep 1: first digit of every group's largest key; (LAVa) partial sums of s, s ln s
+// ---------------------------------------------------------------------------------------
+
+// Grid (chunks, layers).  The chunk's aligned middle streams through the ring; the < 4 keys
+// on either side are read directly by thread 0 as one more group each.  LAVa: s ln s in
+// float, float runs of 16 keys added into fp64.
+template <bool ENTROPY>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
-entropy_hist(const float* __restrict__ scores, int64_t N, int nch, double2* __restrict__ part,
-             uint32_t* __restrict__ ghist) {
+alloc_sweep1(const float* __restrict__ scores, int64_t N, int nch, double2* __restrict__ part,
+             uint32_t* __restrict__ ghist, WsHeader* hdr) {
   __shared__ uint32_t hist[kBins];
-  __shared__ double sa[kThreads / 32], sb[kThreads / 32];
+  __shared__ double sa[kWarps], sb[kWarps];
+  __shared__ uint64_t rfull[kRingStages];
+  extern __shared__ __align__(128) unsigned char ring_mem[];
   const int64_t seg = blockIdx.y;
-  for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0u;
+  SweepRing R;
+  R.init(ring_mem, rfull);
+  for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0u;
   __syncthreads();
+  const float* x = scores + seg * N;
   const int64_t per = chunk_len(N, nch);
-  const int64_t i0 = min(N, blockIdx.x * per), i1 = min(N, i0 + per);
-  double a = 0.0, b = 0.0;
+  const int64_t i0 = min(N, (int64_t)blockIdx.x * per), i1 = min(N, i0 + per);
+  const int64_t a = aligned_from(x, i0, i1);
+  const int64_t nv = (i1 - a) >> 2, b = a + 4 * nv;
+  double sA = 0.0, sB = 0.0;
   float ra = 0.f, rb = 0.f;
-  int terms = 0;
-  sweep_keys(scores + seg * N, i0, i1, false, [&](float x, bool ok, int64_t) {
-    hist_add_runs(hist, ok ? (score_key(x) >> 21) : 0xFFFFFFFFu);
-    if (ok && x > 0.0f) {
-      ra += x;
-      rb += x * (__log2f(x) * 0.69314718055994531f);
+  int groups = 0;
+  // one group: the four values v, bit c of vm set when value c is a key of the chunk
+  auto visit = [&](const float4& v, uint32_t vm) {
+    const float xs[4] = {v.x, v.y, v.z, v.w};
+    uint32_t m = 0u;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if ((vm >> c) & 1u) {
+        m = max(m, score_key(xs[c]));
+        if (ENTROPY && xs[c] > 0.0f) {
+          ra += xs[c];
+          rb += xs[c] * (__log2f(xs[c]) * 0.69314718055994531f);
+        }
+      }
     }
-    if (++terms == 16) {
-      a += (double)ra;
-      b += (double)rb;
+    hist_add_runs(hist, vm ? m >> 21 : kNoBin);
+    if (ENTROPY && ++groups == 4) {
+      sA += (double)ra;
+      sB += (double)rb;
       ra = rb = 0.f;
-      terms = 0;
+      groups = 0;
+    }
+  };
+  // the partial groups on either side: keys [i0, a) and [b, i1)
+  {
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    uint32_t vm = 0u;
+    if (threadIdx.x == 0)
+      for (int64_t i = i0; i < a; ++i) {
+        (&v.x)[i - i0] = x[i];
+        vm |= 1u << (i - i0);
+      }
+    visit(v, vm);
+    v = make_float4(0.f, 0.f, 0.f, 0.f);
+    vm = 0u;
+    if (threadIdx.x == 0)
+      for (int64_t i = b; i < i1; ++i) {
+        (&v.x)[i - b] = x[i];
+        vm |= 1u << (i - b);
+      }
+    visit(v, vm);
+  }
+  const bool ok = ring_pass(R, reinterpret_cast<const unsigned char*>(x + a), nullptr, nv * 16,
+                            false, [&](const unsigned char* st, const unsigned char*, int64_t,
+                                       uint32_t bytes) {
+    const int ng = (int)(bytes / 16);
+    const float4* v4 = reinterpret_cast<const float4*>(st);
+    for (int jb = 0; jb < kGroups; jb += kThreads) {
+      const int j = jb + (int)threadIdx.x;
+      visit(j < ng ? v4[j] : make_float4(0.f, 0.f, 0.f, 0.f), j < ng ? 0xFu : 0u);
     }
   });
-  a += (double)ra;
-  b += (double)rb;
-  a = warp_sum_d(a);
-  b = warp_sum_d(b);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) { sa[warp] = a; sb[warp] = b; }
+  if (!ok && threadIdx.x == 0) raise_dev(hdr, DEV_WAIT_TIMEOUT, 0xA00u);
+  if (ENTROPY) {
+    sA += (double)ra;
+    sB += (double)rb;
+    sA = warp_sum_d(sA);
+    sB = warp_sum_d(sB);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+      sa[warp] = sA;
+      sb[warp] = sB;
+    }
+  }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (ENTROPY && threadIdx.x == 0) {
     double ta = 0.0, tb = 0.0;
-    for (int i = 0; i < kThreads / 32; ++i) { ta += sa[i]; tb += sb[i]; }
+    for (int i = 0; i < kWarps; ++i) {
+      ta += sa[i];
+      tb += sb[i];
+    }
     part[seg * nch + blockIdx.x] = make_double2(ta, tb);
   }
-  merge_hist(hist, ghist + seg * kBins, kBins);
+  uint32_t* G = ghist + seg * kBins;
+  for (int i = threadIdx.x; i < kBins; i += kThreads) {
+    const uint32_t c = hist[i];
+    if (c) atomicAdd(&G[i], c);
+  }
 }
 
-// One CTA per (sequence, layer): e_l of every layer of the sequence, the capped
-// proportional split of R = total - L*w*Hkv with floors and largest remainders (ties to the
-// lower layer), then this layer's first digit from the histogram of the entropy sweep.  The
-// split is the same in every CTA of a sequence (same inputs, same order); each thread owns
-// the layers l = tid (mod blockDim), sums over the active layers are block reductions and
-// the largest remainders are ranks every thread counts for its own layers.
+// ---------------------------------------------------------------------------------------
+// Layer budgets (B' of every layer) and the bound g of every layer
+// ---------------------------------------------------------------------------------------
+
+// LAVa: the capped proportional split of R = total - L*w*Hkv over the L layers of sequence
+// b, with floors and largest remainders (ties to the lower layer); returns B' of layer lme.
+// Every thread owns the layers l = tid (mod blockDim); sums over the active layers are block
+// reductions and the largest remainders are ranks each thread counts for its own layers.
+// Every CTA of a sequence computes the same split (same inputs, same order).
 constexpr int kMaxLayers = 1024;
-__global__ void __launch_bounds__(kThreads)
-layer_budgets(const double2* __restrict__ part, int nch, int L, int Hkv, int n, int w, int C,
-              const int64_t* __restrict__ total, int32_t* __restrict__ layer_budget,
-              int64_t* __restrict__ bprime, RadixState* __restrict__ st,
-              uint32_t* __restrict__ ghist, WsHeader* hdr) {
-  __shared__ double e[kMaxLayers], frac[kMaxLayers];
-  __shared__ int64_t sel[kMaxLayers];   // -1: active; >= 0: capped at that value
-  __shared__ double red_d[kThreads / 32];
-  __shared__ long long red_i[kThreads / 32];
-  __shared__ uint32_t scr[34];
-  __shared__ int64_t mine;
-  const int64_t seg = blockIdx.x;
-  const int b = (int)(seg / L), lme = (int)(seg - (int64_t)b * L);
+struct SplitSmem {
+  double e[kMaxLayers], frac[kMaxLayers];
+  int64_t sel[kMaxLayers];   // -1: active; >= 0: capped at that value
+  double red_d[kWarps];
+  long long red_i[kWarps];
+  int64_t mine;
+};
+__device__ int64_t lava_layer_share(SplitSmem& sm, const double2* part, int nch, int L, int Hkv,
+                                    int n, int w, int C, int64_t total, int b, int lme,
+                                    WsHeader* hdr) {
   for (int l = threadIdx.x; l < L; l += blockDim.x) {
     double S = 0.0, T = 0.0;
     const double2* p = part + ((int64_t)b * L + l) * nch;
@@ -247,11 +227,11 @@ layer_budgets(const double2* __restrict__ part, int nch, int L, int Hkv, int n, 
     }
     double el = 0.0;
     if (S > 0.0) el = (log(S) - T / S) / ((double)Hkv * (double)n);
-    e[l] = el > 0.0 ? el : 0.0;
-    sel[l] = -1;
+    sm.e[l] = el > 0.0 ? el : 0.0;
+    sm.sel[l] = -1;
   }
   const int64_t cap = (int64_t)Hkv * C;
-  int64_t R = total[b] - (int64_t)L * w * Hkv;
+  int64_t R = total - (int64_t)L * w * Hkv;
   if (R < 0 || R > (int64_t)L * cap) {
     if (threadIdx.x == 0 && lme == 0) raise_dev(hdr, DEV_BUDGET_RANGE, (unsigned)b);
     R = R < 0 ? 0 : (int64_t)L * cap;
@@ -262,222 +242,391 @@ layer_budgets(const double2* __restrict__ part, int nch, int L, int Hkv, int n, 
     double es = 0.0;
     long long na = 0;
     for (int l = threadIdx.x; l < L; l += blockDim.x)
-      if (sel[l] < 0) { es += e[l]; ++na; }
-    const double esum = block_sum_dbl(es, red_d);
-    const long long active = block_sum_ll(na, red_i);
+      if (sm.sel[l] < 0) {
+        es += sm.e[l];
+        ++na;
+      }
+    const double esum = block_sum_dbl(es, sm.red_d);
+    const long long active = block_sum_ll(na, sm.red_i);
     long long nover = 0;
     for (int l = threadIdx.x; l < L; l += blockDim.x) {
-      if (sel[l] >= 0) continue;
-      const double q = esum > 0.0 ? (double)rem * e[l] / esum : (double)rem / (double)active;
-      frac[l] = q;
+      if (sm.sel[l] >= 0) continue;
+      const double q = esum > 0.0 ? (double)rem * sm.e[l] / esum : (double)rem / (double)active;
+      sm.frac[l] = q;
       if (q > (double)cap) ++nover;
     }
-    nover = block_sum_ll(nover, red_i);
+    nover = block_sum_ll(nover, sm.red_i);
     if (nover == 0 || active == 0) break;
     for (int l = threadIdx.x; l < L; l += blockDim.x)
-      if (sel[l] < 0 && frac[l] > (double)cap) sel[l] = cap;
+      if (sm.sel[l] < 0 && sm.frac[l] > (double)cap) sm.sel[l] = cap;
     rem -= (int64_t)nover * cap;
   }
   long long used = 0;
   for (int l = threadIdx.x; l < L; l += blockDim.x) {
-    if (sel[l] >= 0) continue;
-    const double f = floor(frac[l]);
-    frac[l] -= f;                  // keep only the fractional part
-    sel[l] = -2 - (int64_t)f;      // active: the floor is stored as -2 - floor
+    if (sm.sel[l] >= 0) continue;
+    const double f = floor(sm.frac[l]);
+    sm.frac[l] -= f;                 // keep only the fractional part
+    sm.sel[l] = -2 - (int64_t)f;     // active: the floor is stored as -2 - floor
     used += (long long)f;
   }
-  const int64_t left = rem - (int64_t)block_sum_ll(used, red_i);   // also a barrier
+  const int64_t left = rem - (int64_t)block_sum_ll(used, sm.red_i);   // also a barrier
   // largest remainders: an active layer gets one more unit when fewer than `left` active
   // layers precede it in (fraction desc, layer asc) order
-  if (lme % blockDim.x == threadIdx.x) {
-    int64_t v = sel[lme];
+  if (lme % (int)blockDim.x == (int)threadIdx.x) {
+    int64_t v = sm.sel[lme];
     if (v <= -2) {
-      const double fl = frac[lme];
+      const double fl = sm.frac[lme];
       int64_t before = 0;
       for (int m = 0; m < L; ++m)
-        if (sel[m] <= -2 && (frac[m] > fl || (frac[m] == fl && m < lme))) ++before;
+        if (sm.sel[m] <= -2 && (sm.frac[m] > fl || (sm.frac[m] == fl && m < lme))) ++before;
       v = (-2 - v) + (before < left ? 1 : 0);
     }
-    bprime[seg] = v;
-    layer_budget[seg] = (int32_t)(v + (int64_t)w * Hkv);
-    mine = v;
+    sm.mine = v;
   }
   __syncthreads();
-  const int64_t Bp = mine;
-  RadixState r{0u, 0u, (uint32_t)Bp, Bp > 0 ? 1u : 0u};
-  uint32_t bin, kr;
-  pick_digit(ghist + seg * kBins, 0, r.krem, scr, hdr, (unsigned)seg, bin, kr);
-  if (threadIdx.x == 0) {
-    if (r.active) advance(r, 0, bin, kr);
-    st[seg] = r;
-  }
+  return sm.mine;
 }
 
-// Histogram of the pass's digit over the keys that match the resolved prefix; the last CTA
-// of the layer picks the digit.  Pass 0 without the entropy sweep also takes B' from the
-// per-layer budget (range-checked) and sets up the layer's state.
-__global__ void __launch_bounds__(kThreads, kMinBlocks)
-radix_hist(const float* __restrict__ scores, int64_t N, int nch, int pass,
-           const int64_t* __restrict__ budget, int Hkv, int w, int32_t* __restrict__ layer_budget,
-           int64_t* __restrict__ bprime, RadixState* __restrict__ st,
-           uint32_t* __restrict__ ghist, uint32_t* __restrict__ done, WsHeader* hdr) {
-  __shared__ uint32_t hist[kBins];
-  __shared__ uint32_t scr[34];
-  __shared__ uint32_t flag;
-  const int64_t seg = blockIdx.y;
-  RadixState r{0u, 0u, 0u, 1u};
-  if (pass > 0) {
-    r = st[seg];
-    if (!r.active) return;   // no CTA of this layer takes part
-  }
-  const int sh = pass_shift(pass), nb = pass_bins(pass);
-  for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0u;
-  __syncthreads();
-  const int64_t per = chunk_len(N, nch);
-  const int64_t i0 = min(N, blockIdx.x * per), i1 = min(N, i0 + per);
-  sweep_keys(scores + seg * N, i0, i1, (pass & 1) != 0, [&](float x, bool ok, int64_t) {
-    uint32_t bin = 0xFFFFFFFFu;
-    if (ok) {
-      const uint32_t key = score_key(x);
-      if ((key & r.mask) == r.prefix) bin = (key >> sh) & (uint32_t)(nb - 1);
-    }
-    hist_add_runs(hist, bin);
-  });
-  __syncthreads();
-  uint32_t* G = ghist + seg * kBins;
-  merge_hist(hist, G, nb);
-  if (!last_of_layer(done + seg, (uint32_t)nch, &flag)) return;
-  if (pass == 0) {
-    int64_t Bp = budget[seg] - (int64_t)w * Hkv;
+// One CTA per (sequence, layer): B' (LAVa split, or the given layer budget less the window,
+// range-checked), then g, the bin of the group-maximum histogram holding the B'-th largest
+// group maximum (2048 when B' == 0: no candidates).
+__global__ void __launch_bounds__(kThreads)
+alloc_bound(const double2* __restrict__ part, int nch, int L, int Hkv, int n, int w, int C,
+            const int64_t* __restrict__ budget, int entropy, int32_t* __restrict__ layer_budget,
+            int64_t* __restrict__ bprime, const uint32_t* __restrict__ ghist,
+            uint32_t* __restrict__ gbin, WsHeader* hdr) {
+  __shared__ SplitSmem sm;
+  __shared__ uint32_t scr[40], res[2];
+  const int64_t seg = blockIdx.x;
+  const int64_t N = (int64_t)Hkv * C;
+  int64_t Bp;
+  if (entropy) {
+    const int b = (int)(seg / L), lme = (int)(seg - (int64_t)b * L);
+    Bp = lava_layer_share(sm, part, nch, L, Hkv, n, w, C, budget[b], b, lme, hdr);
+  } else {
+    Bp = budget[seg] - (int64_t)w * Hkv;
     if (Bp < 0 || Bp > N) {
       if (threadIdx.x == 0) raise_dev(hdr, DEV_BUDGET_RANGE, (unsigned)seg);
       Bp = Bp < 0 ? 0 : N;
     }
-    r.krem = (uint32_t)Bp;
-    r.active = Bp > 0 ? 1u : 0u;
-    if (threadIdx.x == 0) {
-      bprime[seg] = Bp;
-      layer_budget[seg] = (int32_t)(Bp + (int64_t)w * Hkv);
-    }
   }
-  uint32_t bin, kr;
-  pick_digit(G, pass, r.krem, scr, hdr, (unsigned)seg, bin, kr);
+  block_pick<kThreads>(ghist + seg * kBins, kBins, (uint32_t)(Bp > 0 ? Bp : 1), scr, res);
+  __syncthreads();
   if (threadIdx.x == 0) {
-    if (r.active) advance(r, pass, bin, kr);
-    st[seg] = r;
+    bprime[seg] = Bp;
+    layer_budget[seg] = (int32_t)(Bp + (int64_t)w * Hkv);
+    gbin[seg] = Bp > 0 ? res[0] : 2048u;
   }
 }
 
-// Thread 0 of the last CTA of a layer: f_g from the per-head counts (tau-equal keys in head
-// order), each head's floor of the blend in sBg and its remainder in srem; returns the units
-// left for the largest remainders.  The counts are left zeroed for the next call.
-__device__ __noinline__ int64_t blend_floors(int64_t left_eq, uint32_t* Cg, int Hkv, int64_t Bp,
-                                             uint32_t an, uint32_t ad, int32_t* sBg,
-                                             int64_t* srem, WsHeader* hdr, unsigned seg) {
-  const int64_t den = (int64_t)ad * Hkv;
-  int64_t fsum = 0, flo = 0;
-  for (int g = 0; g < Hkv; ++g) {
-    const int64_t eqg = __ldcg(Cg + 2 * g + 1);
-    const int64_t take = left_eq < eqg ? left_eq : eqg;
-    left_eq -= take;
-    const int64_t f = (int64_t)__ldcg(Cg + 2 * g) + take;
-    Cg[2 * g] = 0u;
-    Cg[2 * g + 1] = 0u;
-    fsum += f;
-    const int64_t X = (int64_t)an * Bp + (int64_t)(ad - an) * Hkv * f;
-    sBg[g] = (int32_t)(X / den);
-    srem[g] = X % den;
-    flo += sBg[g];
-  }
-  if (fsum != Bp) raise_dev(hdr, DEV_SELECT, seg);
-  return Bp - flo;
-}
+// ---------------------------------------------------------------------------------------
+// Sweep 2: the union of keys with first digit >= g; the last CTA of a layer finishes it
+// ---------------------------------------------------------------------------------------
 
-// Per-head counts of keys above the threshold and equal to it; the last CTA of the layer
-// then forms f_g (keys above tau in head g, plus tau-equal keys in (head, position) order)
-// and the safeguard blend in exact integers.
-__global__ void __launch_bounds__(kThreads, kMinBlocks)
-radix_count(const float* __restrict__ scores, int Hkv, int C, int nch,
-            const RadixState* __restrict__ st, const int64_t* __restrict__ bprime,
-            uint32_t* __restrict__ counts /*[S][Hkv][2]*/, uint32_t* __restrict__ done, int w,
-            uint32_t an, uint32_t ad, int32_t* __restrict__ head_budget, WsHeader* hdr) {
-  __shared__ uint32_t cnt[2 * kMaxHeads];
-  __shared__ int64_t srem[kMaxHeads];
-  __shared__ int32_t sBg[kMaxHeads];
-  __shared__ int64_t sleft;
-  __shared__ uint32_t flag;
-  const int64_t seg = blockIdx.y;
-  const RadixState r = st[seg];
-  const int64_t N = (int64_t)Hkv * C;
-  uint32_t* Cg = counts + seg * 2 * Hkv;
-  if (r.active) {
-    const uint32_t tau = r.prefix;
-    for (int i = threadIdx.x; i < 2 * Hkv; i += blockDim.x) cnt[i] = 0u;
+struct FinishSmem {
+  union {
+    uint32_t hist[kBins];          // the radix passes
+    struct {                       // then the blend
+      int64_t srem[kMaxHeads];
+      int32_t sBg[kMaxHeads];
+    } b;
+  };
+  uint32_t scr[40], res[2];
+  uint32_t cnt[2 * kMaxHeads];     // per head: keys above tau, keys equal to tau
+  uint32_t cstart[kMaxChunks + 1]; // the union's chunk regions, concatenated
+  int64_t sleft;
+  uint32_t flag;
+};
+
+// Radix select of the Bp-th largest key over a sequence of keys visited by each(fn), where
+// each(fn) calls fn(key, ok) the same number of times in every thread; pass 0 counts only
+// first digits >= g.  Leaves (tau, keq) in res[0..1].
+template <typename Each>
+__device__ void radix_tau(FinishSmem& sm, uint32_t Bp, uint32_t g, Each&& each) {
+  uint32_t prefix = 0, mask = 0, krem = Bp;
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const int nb = pass == 2 ? 1024 : 2048;
+    for (int i = threadIdx.x; i < nb; i += kThreads) sm.hist[i] = 0u;
     __syncthreads();
-    const int64_t per = chunk_len(N, nch);
-    const int64_t i0 = min(N, blockIdx.x * per), i1 = min(N, i0 + per);
-    // one sub-sweep per head the chunk meets (walked from the last, like the steps)
-    const float* S = scores + seg * N;
-    if (i1 > i0) {
-      const int h0 = (int)(i0 / C), h1 = (int)((i1 - 1) / C);
-      for (int h = h1; h >= h0; --h) {
-        const int64_t a = max(i0, (int64_t)h * C), b = min(i1, (int64_t)(h + 1) * C);
-        uint32_t gt = 0, eq = 0;
-        sweep_keys(S, a, b, true, [&](float x, bool ok, int64_t) {
-          const uint32_t key = score_key(x);
-          gt += (ok && key > tau) ? 1u : 0u;
-          eq += (ok && key == tau) ? 1u : 0u;
-        });
-        gt = warp_sum_u(gt);
-        eq = warp_sum_u(eq);
-        if ((threadIdx.x & 31) == 0) {
-          if (gt) atomicAdd(&cnt[2 * h], gt);
-          if (eq) atomicAdd(&cnt[2 * h + 1], eq);
+    each([&](uint32_t k, bool ok) {
+      const bool in = ok && (pass == 0 ? (k >> 21) >= g : (k & mask) == prefix);
+      hist_add_runs(sm.hist, in ? (k >> sh) & (uint32_t)(nb - 1) : kNoBin);
+    });
+    __syncthreads();
+    block_pick<kThreads>(sm.hist, nb, krem, sm.scr, sm.res);
+    __syncthreads();
+    prefix |= sm.res[0] << sh;
+    mask |= (uint32_t)(nb - 1) << sh;
+    krem = sm.res[1];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    sm.res[0] = prefix;
+    sm.res[1] = krem;
+  }
+  __syncthreads();
+}
+
+// Grid (chunks, layers).  Walks the chunk backwards (the tail keys, the ring's chunks last to
+// first, the head keys) and fills the CTA's union region from its end, so the region
+// [fill, UC) lists the chunk's candidate positions in ascending order.
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
+alloc_sweep2(const float* __restrict__ scores, int Hkv, int C, int nch,
+             const uint32_t* __restrict__ gbin, const int64_t* __restrict__ bprime,
+             int32_t* __restrict__ upos, uint32_t* __restrict__ ukey, uint32_t* __restrict__ ufill,
+             uint32_t* __restrict__ uover, int64_t UC, uint32_t* __restrict__ done, int w,
+             uint32_t an, uint32_t ad, int32_t* __restrict__ head_budget, WsHeader* hdr) {
+  __shared__ FinishSmem sm;
+  __shared__ uint64_t rfull[kRingStages];
+  extern __shared__ __align__(128) unsigned char ring_mem[];
+  const int64_t seg = blockIdx.y;
+  const int64_t N = (int64_t)Hkv * C;
+  const uint32_t g = gbin[seg];
+  const int64_t Bp = bprime[seg];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* x = scores + seg * N;
+  const int64_t per = chunk_len(N, nch);
+  const int64_t i0 = min(N, (int64_t)blockIdx.x * per), i1 = min(N, i0 + per);
+  int32_t* P = upos + (seg * nch + blockIdx.x) * UC;
+  uint32_t* K = ukey + (seg * nch + blockIdx.x) * UC;
+  uint32_t fill = (uint32_t)UC;
+  bool over = false;
+  if (g < 2048u) {
+    SweepRing R;
+    R.init(ring_mem, rfull);
+    // a key is a candidate when its first digit is >= g: for x > 0 the key is x's bit
+    // pattern, so the test is x >= the float whose bit pattern is g << 21
+    const float t = __uint_as_float(min(g, 1023u) << 21);
+    auto is_cand = [&](float v) { return g == 0u || (g < 1024u && v >= t); };
+    const int64_t a = aligned_from(x, i0, i1);
+    const int64_t nv = (i1 - a) >> 2, b = a + 4 * nv;
+    // the keys outside the aligned middle, taken by thread 0 from the last down
+    auto side = [&](int64_t lo, int64_t hi) {
+      if (threadIdx.x == 0) {
+        uint32_t f = fill;
+        bool ov = over;
+        for (int64_t i = hi - 1; i >= lo && !ov; --i) {
+          const float v = x[i];
+          if (!is_cand(v)) continue;
+          if (f == 0u) {
+            ov = true;
+            break;
+          }
+          --f;
+          P[f] = (int32_t)i;
+          K[f] = score_key(v);
         }
+        sm.res[0] = f;
+        sm.res[1] = ov ? 1u : 0u;
+      }
+      __syncthreads();
+      fill = sm.res[0];
+      over = sm.res[1] != 0u;
+      __syncthreads();
+    };
+    side(b, i1);
+    constexpr int kPerWarp = kGroups / kWarps;   // groups of a ring chunk per warp, in order
+    const bool ok = ring_pass(R, reinterpret_cast<const unsigned char*>(x + a), nullptr, nv * 16,
+                              true, [&](const unsigned char* st, const unsigned char*,
+                                        int64_t off, uint32_t bytes) {
+      if (over) return;   // the same in every thread
+      const int ng = (int)(bytes / 16);
+      const float4* v4 = reinterpret_cast<const float4*>(st);
+      uint32_t cmu[kPerWarp / 32];
+      uint32_t wc = 0;
+#pragma unroll
+      for (int u = 0; u < kPerWarp / 32; ++u) {
+        const int j = warp * kPerWarp + u * 32 + lane;
+        uint32_t cm = 0u;
+        if (j < ng) {
+          const float4 v = v4[j];
+          if (is_cand(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w))))
+            cm = (is_cand(v.x) ? 1u : 0u) | (is_cand(v.y) ? 2u : 0u) |
+                 (is_cand(v.z) ? 4u : 0u) | (is_cand(v.w) ? 8u : 0u);
+        }
+        cmu[u] = cm;
+        wc += __popc(cm);
+      }
+      wc = warp_sum_u(wc);
+      if (lane == 0) sm.scr[warp] = wc;
+      __syncthreads();
+      uint32_t c = lane < kWarps ? sm.scr[lane] : 0u, ci = c;
+#pragma unroll
+      for (int d = 1; d < kWarps; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, ci, d);
+        if (lane >= d) ci += y;
+      }
+      const uint32_t T = __shfl_sync(0xFFFFFFFFu, ci, kWarps - 1);
+      const uint32_t before = __shfl_sync(0xFFFFFFFFu, ci - c, warp);
+      if (T == 0u) return;
+      if (T > fill) {
+        over = true;
+        return;
+      }
+      uint32_t o = fill - T + before;
+#pragma unroll
+      for (int u = 0; u < kPerWarp / 32; ++u) {
+        const int j = warp * kPerWarp + u * 32 + lane;
+        const uint32_t nc = __popc(cmu[u]);
+        uint32_t incl = nc;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+          if (lane >= d) incl += y;
+        }
+        if (cmu[u]) {
+          const float4 v = v4[j];
+          const float vs[4] = {v.x, v.y, v.z, v.w};
+          uint32_t q = o + incl - nc;
+          const int64_t i = a + off / 4 + 4 * (int64_t)j;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            if ((cmu[u] >> cc) & 1u) {
+              P[q] = (int32_t)(i + cc);
+              K[q] = score_key(vs[cc]);
+              ++q;
+            }
+        }
+        o += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+      fill -= T;
+    });
+    if (!ok) {
+      if (threadIdx.x == 0) raise_dev(hdr, DEV_WAIT_TIMEOUT, 0xA20u);
+      over = true;
+    }
+    if (!over) side(i0, a);
+  }
+  if (threadIdx.x == 0) {
+    ufill[seg * nch + blockIdx.x] = fill;
+    if (over) atomicOr(&uover[seg], 1u);
+  }
+  if (!last_of_layer(done + seg, (uint32_t)nch, &sm.flag)) return;
+
+  // ---- the last CTA of the layer: tau, keq and the per-head counts
+  for (int i = threadIdx.x; i < 2 * Hkv; i += kThreads) sm.cnt[i] = 0u;
+  const bool overflow = __ldcg(&uover[seg]) != 0u;
+  if (threadIdx.x == 0) {
+    uint32_t s0 = 0;
+    for (int c = 0; c < nch; ++c) {
+      sm.cstart[c] = s0;
+      s0 += (uint32_t)UC - __ldcg(&ufill[seg * nch + c]);
+    }
+    sm.cstart[nch] = s0;
+  }
+  __syncthreads();
+  uint32_t tau = 0xFFFFFFFFu, keq = 0u;   // no key equals 0xFFFFFFFF
+  if (Bp > 0) {
+    if (!overflow) {
+      // the union, chunk by chunk in position order
+      auto each = [&](auto&& fn) {
+        for (int c = 0; c < nch; ++c) {
+          const int64_t r0 = (seg * nch + c) * UC;
+          const int f = (int)(UC - (sm.cstart[c + 1] - sm.cstart[c]));
+          for (int tb = f; tb < (int)UC; tb += kThreads) {
+            const int tt = tb + (int)threadIdx.x;
+            fn(tt < (int)UC ? __ldcg(ukey + r0 + tt) : 0u, tt < (int)UC);
+          }
+        }
+      };
+      radix_tau(sm, (uint32_t)Bp, g, each);
+    } else {
+      // every key of the layer
+      auto each = [&](auto&& fn) {
+        for (int64_t ib = 0; ib < N; ib += kThreads) {
+          const int64_t i = ib + threadIdx.x;
+          fn(i < N ? score_key(x[i]) : 0u, i < N);
+        }
+      };
+      radix_tau(sm, (uint32_t)Bp, 0u, each);
+    }
+    tau = sm.res[0];
+    keq = sm.res[1];
+    // per head: keys above tau and keys equal to tau (every such key is in the union)
+    auto tally = [&](int64_t pos, uint32_t k) {
+      const int h = (int)(pos / C);
+      if (k > tau) atomicAdd(&sm.cnt[2 * h], 1u);
+      else if (k == tau) atomicAdd(&sm.cnt[2 * h + 1], 1u);
+    };
+    if (!overflow) {
+      for (int c = 0; c < nch; ++c) {
+        const int64_t r0 = (seg * nch + c) * UC;
+        for (int tt = (int)(UC - (sm.cstart[c + 1] - sm.cstart[c])) + threadIdx.x; tt < (int)UC;
+             tt += kThreads)
+          tally(__ldcg(upos + r0 + tt), __ldcg(ukey + r0 + tt));
+      }
+    } else {
+      for (int64_t i = threadIdx.x; i < N; i += kThreads) {
+        const uint32_t k = score_key(x[i]);
+        if (k >= tau) tally(i, k);
       }
     }
-    __syncthreads();
-    for (int i = threadIdx.x; i < 2 * Hkv; i += blockDim.x)
-      if (cnt[i]) atomicAdd(&Cg[i], cnt[i]);
   }
-  if (!last_of_layer(done + seg, (uint32_t)nch, &flag)) return;
-  const int64_t Bp = bprime[seg];
-  if (threadIdx.x == 0)
-    sleft = blend_floors(r.active ? (int64_t)r.krem : 0, Cg, Hkv, Bp, an, ad, sBg, srem, hdr,
-                         (unsigned)seg);
   __syncthreads();
-  // largest remainders (ties to the lower head): a head gets one more unit when fewer than
-  // `left` heads precede it in (remainder desc, head asc) order
-  for (int g = threadIdx.x; g < Hkv; g += blockDim.x) {
-    const int64_t rg = srem[g];
+  // f_g: keys above tau in head g, plus tau-equal keys in (head, position) order; then the
+  // safeguard blend in exact integers and the largest remainders (ties to the lower head)
+  if (threadIdx.x == 0) {
+    const int64_t den = (int64_t)ad * Hkv;
+    int64_t left_eq = (int64_t)keq, fsum = 0, flo = 0;
+    for (int h = 0; h < Hkv; ++h) {
+      const int64_t eqh = sm.cnt[2 * h + 1];
+      const int64_t take = left_eq < eqh ? left_eq : eqh;
+      left_eq -= take;
+      const int64_t f = (int64_t)sm.cnt[2 * h] + take;
+      fsum += f;
+      const int64_t X = (int64_t)an * Bp + (int64_t)(ad - an) * Hkv * f;
+      sm.b.sBg[h] = (int32_t)(X / den);
+      sm.b.srem[h] = X % den;
+      flo += sm.b.sBg[h];
+    }
+    if (fsum != Bp) raise_dev(hdr, DEV_SELECT, (unsigned)seg);
+    sm.sleft = Bp - flo;
+  }
+  __syncthreads();
+  for (int h = threadIdx.x; h < Hkv; h += kThreads) {
+    const int64_t rh = sm.b.srem[h];
     int64_t before = 0;
     for (int m = 0; m < Hkv; ++m)
-      if (srem[m] > rg || (srem[m] == rg && m < g)) ++before;
-    head_budget[seg * Hkv + g] = sBg[g] + (before < sleft ? 1 : 0) + w;
+      if (sm.b.srem[m] > rh || (sm.b.srem[m] == rh && m < h)) ++before;
+    head_budget[seg * Hkv + h] = sm.b.sBg[h] + (before < sm.sleft ? 1 : 0) + w;
   }
 }
+
+// ---------------------------------------------------------------------------------------
 
 AllocPlan alloc_plan(const Shape& s) {
   AllocPlan p{};
   const int64_t S = s.segments();
   const int64_t N = (int64_t)s.Hkv * (s.C() > 0 ? s.C() : 1);
-  // one wave of kMinBlocks CTAs per SM over all layers, at least one full step per CTA
+  // one wave of kMinBlocks CTAs per SM over all layers, at least one ring stage per CTA
   int64_t nch = (int64_t)num_sms() * kMinBlocks / (S > 0 ? S : 1);
-  const int64_t maxch = cdiv(N, (int64_t)kU * 4 * kThreads);
+  const int64_t maxch = cdiv(N, (int64_t)kRingStage / 4);
   if (nch > maxch) nch = maxch;
+  if (nch > kMaxChunks) nch = kMaxChunks;
   if (nch < 1) nch = 1;
+  nch = cdiv(N, chunk_len(N, (int)nch));   // no empty chunk
   p.nchunkE = (int)nch;
+  // a layer's union holds min(N, kUnionPerLayer) keys, split evenly over its CTAs
+  const int64_t ucap = N < kUnionPerLayer ? N : kUnionPerLayer;
+  p.union_per_cta = cdiv(ucap, nch) + 4;
   size_t off = kWsHeader;
   p.off_bprime = off;
   off += align_up((size_t)S * sizeof(int64_t), 256);
   p.off_epart = off;
-  off += align_up((size_t)S * p.nchunkE * sizeof(double2), 256);
-  p.off_e = off;
+  off += align_up((size_t)S * nch * sizeof(double2), 256);
+  p.off_gbin = off;
   off += align_up((size_t)S * sizeof(uint32_t), 256);
-  p.off_scratch = off;   // radix state, histograms, per-head counts
-  off += align_up((size_t)S * sizeof(RadixState), 256);
+  p.off_ufill = off;
+  off += align_up((size_t)S * nch * sizeof(uint32_t), 256);
+  p.off_zero = off;   // cleared by every call: done counters, overflow flags, histograms
+  off += align_up((size_t)S * sizeof(uint32_t), 256);
+  off += align_up((size_t)S * sizeof(uint32_t), 256);
   off += align_up((size_t)S * kBins * sizeof(uint32_t), 256);
-  off += align_up((size_t)S * 2 * kMaxHeads * sizeof(uint32_t), 256);
+  p.off_union = off;
+  off += align_up((size_t)S * nch * p.union_per_cta * sizeof(int32_t), 256);
+  off += align_up((size_t)S * nch * p.union_per_cta * sizeof(uint32_t), 256);
   p.off_end = off;
   return p;
 }
@@ -488,37 +637,48 @@ cudaError_t launch_allocate(const Shape& s, const float* scores, const int64_t* 
                             cudaStream_t st) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   const int64_t S = s.segments();
+  if (S <= 0) return cudaSuccess;
   const int C = s.C();
   const int64_t N = (int64_t)s.Hkv * C;
-  int64_t* bprime = reinterpret_cast<int64_t*>(ws + p.off_bprime);
-  uint32_t* done = reinterpret_cast<uint32_t*>(ws + p.off_e);
-  char* sc = ws + p.off_scratch;
-  RadixState* rst = reinterpret_cast<RadixState*>(sc);
-  sc += align_up((size_t)S * sizeof(RadixState), 256);
-  uint32_t* ghist = reinterpret_cast<uint32_t*>(sc);
-  sc += align_up((size_t)S * kBins * sizeof(uint32_t), 256);
-  uint32_t* counts = reinterpret_cast<uint32_t*>(sc);
-  // counters, histograms and counts start at zero; the kernels leave them zeroed behind them
-  cudaError_t e = cudaMemsetAsync(done, 0, p.off_end - p.off_e, st);
-  if (e != cudaSuccess) return e;
   const int nch = p.nchunkE;
-  const dim3 sweep((unsigned)nch, (unsigned)S);
-  if (entropy_mode) {
-    double2* part = reinterpret_cast<double2*>(ws + p.off_epart);
-    entropy_hist<<<sweep, kThreads, 0, st>>>(scores, N, nch, part, ghist);
-    layer_budgets<<<(unsigned)S, kThreads, 0, st>>>(part, nch, s.L, s.Hkv, s.n, s.w, C, budget,
-                                                    layer_budget, bprime, rst, ghist, hdr);
-    count_launches(2);
-  } else {
-    radix_hist<<<sweep, kThreads, 0, st>>>(scores, N, nch, 0, budget, s.Hkv, s.w, layer_budget,
-                                           bprime, rst, ghist, done, hdr);
-    count_launches(1);
+  const int64_t UC = p.union_per_cta;
+  int64_t* bprime = reinterpret_cast<int64_t*>(ws + p.off_bprime);
+  double2* part = reinterpret_cast<double2*>(ws + p.off_epart);
+  uint32_t* gbin = reinterpret_cast<uint32_t*>(ws + p.off_gbin);
+  uint32_t* ufill = reinterpret_cast<uint32_t*>(ws + p.off_ufill);
+  char* z = ws + p.off_zero;
+  uint32_t* done = reinterpret_cast<uint32_t*>(z);
+  z += align_up((size_t)S * sizeof(uint32_t), 256);
+  uint32_t* uover = reinterpret_cast<uint32_t*>(z);
+  z += align_up((size_t)S * sizeof(uint32_t), 256);
+  uint32_t* ghist = reinterpret_cast<uint32_t*>(z);
+  int32_t* upos = reinterpret_cast<int32_t*>(ws + p.off_union);
+  uint32_t* ukey = reinterpret_cast<uint32_t*>(
+      ws + p.off_union + align_up((size_t)S * nch * UC * sizeof(int32_t), 256));
+  // counters, flags and histograms start at zero
+  cudaError_t e = cudaMemsetAsync(ws + p.off_zero, 0, p.off_union - p.off_zero, st);
+  if (e != cudaSuccess) return e;
+  static bool opted = false;   // the sweeps' rings are dynamic shared memory above 48 KB
+  if (!opted) {
+    const void* ks[3] = {(const void*)alloc_sweep1<true>, (const void*)alloc_sweep1<false>,
+                         (const void*)alloc_sweep2};
+    for (const void* k : ks) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+      if (e != cudaSuccess) return e;
+    }
+    opted = true;
   }
-  for (int pass = 1; pass < 3; ++pass)
-    radix_hist<<<sweep, kThreads, 0, st>>>(scores, N, nch, pass, budget, s.Hkv, s.w,
-                                           layer_budget, bprime, rst, ghist, done, hdr);
-  radix_count<<<sweep, kThreads, 0, st>>>(scores, s.Hkv, C, nch, rst, bprime, counts, done, s.w,
-                                          an, ad, head_budget, hdr);
+  const dim3 sweep((unsigned)nch, (unsigned)S);
+  if (entropy_mode)
+    alloc_sweep1<true><<<sweep, kThreads, kRingBytes, st>>>(scores, N, nch, part, ghist, hdr);
+  else
+    alloc_sweep1<false><<<sweep, kThreads, kRingBytes, st>>>(scores, N, nch, part, ghist, hdr);
+  alloc_bound<<<(unsigned)S, kThreads, 0, st>>>(part, nch, s.L, s.Hkv, s.n, s.w, C, budget,
+                                                entropy_mode, layer_budget, bprime, ghist, gbin,
+                                                hdr);
+  alloc_sweep2<<<sweep, kThreads, kRingBytes, st>>>(scores, s.Hkv, C, nch, gbin, bprime, upos,
+                                                    ukey, ufill, uover, UC, done, s.w, an, ad,
+                                                    head_budget, hdr);
   count_launches(3);
   return cudaGetLastError();
 }

@@ -206,9 +206,9 @@ __device__ uint32_t select_head(SelRing& R, HeadSelSmem& sm, unsigned char* ring
     // group j of a chunk at byte offset off: its keys, and which of them lie in the head
     auto group = [&](const unsigned char* st0, const unsigned char* st1, int64_t off, int j,
                      bool in, uint32_t (&k)[4], bool (&f)[4]) -> uint32_t {
-      const float4 x = in ? reinterpret_cast<const float4*>(st0)[j] : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 y = (Src::kTwo && in) ? reinterpret_cast<const float4*>(st1)[j]
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 x = in ? reinterpret_cast<const float4*>(st0)[j] : zero;
+      const float4 y = (Src::kTwo && in) ? reinterpret_cast<const float4*>(st1)[j] : zero;
       const int pos0 = (int)(a0 + off / 4 + 4 * j - flat0);
       src.keys(x, y, pos0, k, f);
       uint32_t vm = 0u;
