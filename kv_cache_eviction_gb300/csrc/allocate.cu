@@ -96,7 +96,8 @@ __device__ __forceinline__ long long block_sum_ll(long long v, long long* red) {
 
 // Grid (chunks, layers).  The chunk's aligned middle streams through the ring; the < 4 keys
 // on either side are read directly by thread 0 as one more group each.  LAVa: s ln s in
-// float, float runs of 16 keys added into fp64.
+// float; float runs of 16 keys are added into a compensated float sum (Kahan), which goes to
+// fp64 once per thread (fp64 arithmetic is scarce on this part).
 template <bool ENTROPY>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
 alloc_sweep1(const float* __restrict__ scores, int64_t N, int nch, double2* __restrict__ part,
@@ -115,9 +116,15 @@ alloc_sweep1(const float* __restrict__ scores, int64_t N, int nch, double2* __re
   const int64_t i0 = min(N, (int64_t)blockIdx.x * per), i1 = min(N, i0 + per);
   const int64_t a = aligned_from(x, i0, i1);
   const int64_t nv = (i1 - a) >> 2, b = a + 4 * nv;
-  double sA = 0.0, sB = 0.0;
+  float sA = 0.f, cA = 0.f, sB = 0.f, cB = 0.f;   // compensated sums and their corrections
   float ra = 0.f, rb = 0.f;
   int groups = 0;
+  auto kahan = [](float& sum, float& c, float v) {
+    const float y = v - c;
+    const float t = sum + y;
+    c = (t - sum) - y;
+    sum = t;
+  };
   // one group: the four values v, bit c of vm set when value c is a key of the chunk
   auto visit = [&](const float4& v, uint32_t vm) {
     const float xs[4] = {v.x, v.y, v.z, v.w};
@@ -134,8 +141,8 @@ alloc_sweep1(const float* __restrict__ scores, int64_t N, int nch, double2* __re
     }
     hist_add_runs(hist, vm ? m >> 21 : kNoBin);
     if (ENTROPY && ++groups == 4) {
-      sA += (double)ra;
-      sB += (double)rb;
+      kahan(sA, cA, ra);
+      kahan(sB, cB, rb);
       ra = rb = 0.f;
       groups = 0;
     }
@@ -171,14 +178,14 @@ alloc_sweep1(const float* __restrict__ scores, int64_t N, int nch, double2* __re
   });
   if (!ok && threadIdx.x == 0) raise_dev(hdr, DEV_WAIT_TIMEOUT, 0xA00u);
   if (ENTROPY) {
-    sA += (double)ra;
-    sB += (double)rb;
-    sA = warp_sum_d(sA);
-    sB = warp_sum_d(sB);
+    kahan(sA, cA, ra);
+    kahan(sB, cB, rb);
+    const double dA = warp_sum_d((double)sA - (double)cA);
+    const double dB = warp_sum_d((double)sB - (double)cB);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) {
-      sa[warp] = sA;
-      sb[warp] = sB;
+      sa[warp] = dA;
+      sb[warp] = dB;
     }
   }
   __syncthreads();
@@ -519,19 +526,75 @@ alloc_sweep2(const float* __restrict__ scores, int Hkv, int C, int nch,
   __syncthreads();
   uint32_t tau = 0xFFFFFFFFu, keq = 0u;   // no key equals 0xFFFFFFFF
   if (Bp > 0) {
-    if (!overflow) {
-      // the union, chunk by chunk in position order
+    const uint32_t U = sm.cstart[nch];
+    // union entry t lives in chunk region c (cstart[c] <= t < cstart[c + 1]) at offset
+    // UC - (its region's length) + (t - cstart[c])
+    auto where = [&](uint32_t t) -> int64_t {
+      int lo = 0, hi = nch;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (sm.cstart[mid] <= t) lo = mid; else hi = mid;
+      }
+      return (seg * nch + lo) * UC + (UC - (int64_t)(sm.cstart[lo + 1] - sm.cstart[lo])) +
+             (int64_t)(t - sm.cstart[lo]);
+    };
+    auto tally = [&](int64_t pos, uint32_t k) {
+      const int h = (int)(pos / C);
+      if (k > tau) atomicAdd(&sm.cnt[2 * h], 1u);
+      else if (k == tau) atomicAdd(&sm.cnt[2 * h + 1], 1u);
+    };
+    if (!overflow && U <= (uint32_t)(kRingBytes / 4)) {
+      // the union's keys, gathered into the (idle) ring memory, 4 loads in flight per thread
+      uint32_t* Ub = reinterpret_cast<uint32_t*>(ring_mem);
+      for (uint32_t tb = 0; tb < U; tb += 4 * kThreads) {
+        uint32_t kk[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t t = tb + u * kThreads + threadIdx.x;
+          kk[u] = t < U ? __ldcg(ukey + where(t)) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t t = tb + u * kThreads + threadIdx.x;
+          if (t < U) Ub[t] = kk[u];
+        }
+      }
+      __syncthreads();
       auto each = [&](auto&& fn) {
-        for (int c = 0; c < nch; ++c) {
-          const int64_t r0 = (seg * nch + c) * UC;
-          const int f = (int)(UC - (sm.cstart[c + 1] - sm.cstart[c]));
-          for (int tb = f; tb < (int)UC; tb += kThreads) {
-            const int tt = tb + (int)threadIdx.x;
-            fn(tt < (int)UC ? __ldcg(ukey + r0 + tt) : 0u, tt < (int)UC);
-          }
+        for (uint32_t tb = 0; tb < U; tb += kThreads) {
+          const uint32_t t = tb + threadIdx.x;
+          fn(t < U ? Ub[t] : 0u, t < U);
         }
       };
       radix_tau(sm, (uint32_t)Bp, g, each);
+      tau = sm.res[0];
+      keq = sm.res[1];
+      for (uint32_t t = threadIdx.x; t < U; t += kThreads) {
+        const uint32_t k = Ub[t];
+        if (k >= tau) tally(__ldcg(upos + where(t)), k);
+      }
+    } else if (!overflow) {
+      // a union longer than the ring memory: read from L2, 8 keys per thread in flight
+      auto each = [&](auto&& fn) {
+        for (uint32_t tb = 0; tb < U; tb += 8 * kThreads) {
+          uint32_t kk[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint32_t t = tb + u * kThreads + threadIdx.x;
+            kk[u] = t < U ? __ldcg(ukey + where(t)) : 0u;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) fn(kk[u], tb + u * kThreads + threadIdx.x < U);
+        }
+      };
+      radix_tau(sm, (uint32_t)Bp, g, each);
+      tau = sm.res[0];
+      keq = sm.res[1];
+      for (uint32_t t = threadIdx.x; t < U; t += kThreads) {
+        const int64_t e = where(t);
+        const uint32_t k = __ldcg(ukey + e);
+        if (k >= tau) tally(__ldcg(upos + e), k);
+      }
     } else {
       // every key of the layer
       auto each = [&](auto&& fn) {
@@ -541,23 +604,8 @@ alloc_sweep2(const float* __restrict__ scores, int Hkv, int C, int nch,
         }
       };
       radix_tau(sm, (uint32_t)Bp, 0u, each);
-    }
-    tau = sm.res[0];
-    keq = sm.res[1];
-    // per head: keys above tau and keys equal to tau (every such key is in the union)
-    auto tally = [&](int64_t pos, uint32_t k) {
-      const int h = (int)(pos / C);
-      if (k > tau) atomicAdd(&sm.cnt[2 * h], 1u);
-      else if (k == tau) atomicAdd(&sm.cnt[2 * h + 1], 1u);
-    };
-    if (!overflow) {
-      for (int c = 0; c < nch; ++c) {
-        const int64_t r0 = (seg * nch + c) * UC;
-        for (int tt = (int)(UC - (sm.cstart[c + 1] - sm.cstart[c])) + threadIdx.x; tt < (int)UC;
-             tt += kThreads)
-          tally(__ldcg(upos + r0 + tt), __ldcg(ukey + r0 + tt));
-      }
-    } else {
+      tau = sm.res[0];
+      keq = sm.res[1];
       for (int64_t i = threadIdx.x; i < N; i += kThreads) {
         const uint32_t k = score_key(x[i]);
         if (k >= tau) tally(i, k);
