@@ -13,12 +13,13 @@
 //  2. after the layer budgets, the bin g holding the B'-th largest group maximum bounds tau,
 //     the B'-th largest key, from below: at least B' groups, so at least B' keys, have a
 //     first digit >= g.  The second sweep lists every key with a first digit >= g, in
-//     position order, per CTA.  The last CTA of the layer to finish finds tau and the
-//     tau-equal quota with an exact radix select (11/11/10 bits) over that union, counts
-//     each head's keys above and at tau from it, and blends the head budgets.
-// A union longer than its capacity (large budgets) makes that CTA run the radix select over
-// every key of the layer instead.  Consecutive sweeps walk their chunks in opposite
-// directions, so the second starts on the part of the scores the first left in L2.
+//     position order, per CTA (a region as long as the CTA's chunk: it cannot overflow,
+//     whatever the budget).  The layer's CTAs then find tau and the tau-equal quota with an
+//     exact radix select (11/11/10 bits) over their lists, waiting for one another at
+//     bounded barriers (the launch is cooperative), count each head's keys above and at tau,
+//     and the layer's first CTA blends the head budgets.
+// Consecutive sweeps walk their chunks in opposite directions, so the second starts on the
+// part of the scores the first left in L2.
 #include "bulk_ring.cuh"
 #include "kv_internal.cuh"
 #include "radix_select.cuh"
@@ -37,7 +38,6 @@ using SweepRing = BulkRing<kRingStages, kRingStage>;
 constexpr int kBins = 2048;
 constexpr int kMaxHeads = 256;
 constexpr int kMaxChunks = 512;      // CTAs per layer
-constexpr int64_t kUnionPerLayer = 65536;   // candidate keys a layer's union can hold
 constexpr uint32_t kNoBin = 0xFFFFFFFFu;
 
 // Keys per CTA of a layer: a multiple of 4, so the chunks of an aligned layer are aligned.
@@ -50,22 +50,6 @@ __device__ __forceinline__ int64_t aligned_from(const float* x, int64_t i0, int6
   const uintptr_t addr = reinterpret_cast<uintptr_t>(x + i0);
   const int64_t a = i0 + (int64_t)(((16u - (uint32_t)(addr & 15u)) & 15u) >> 2);
   return a < i1 ? a : i1;
-}
-
-// True in every thread of the CTA that is the n-th and last of its layer to get here; its
-// reads of the other CTAs' results come after a fence.  The counter is left at zero.
-__device__ __forceinline__ bool last_of_layer(uint32_t* done, uint32_t n, uint32_t* flag) {
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const uint32_t t = atomicAdd(done, 1u);
-    *flag = t == n - 1 ? 1u : 0u;
-    if (t == n - 1) *done = 0u;
-  }
-  __syncthreads();
-  const bool last = *flag != 0u;
-  if (last) __threadfence();
-  return last;
 }
 
 // Block-wide sums; every thread gets the total (the same order for every thread).
@@ -327,10 +311,11 @@ alloc_bound(const double2* __restrict__ part, int nch, int L, int Hkv, int n, in
 }
 
 // ---------------------------------------------------------------------------------------
-// Sweep 2: the union of keys with first digit >= g; the last CTA of a layer finishes it
+// Sweep 2: the union of keys with first digit >= g, then the exact select over it by all
+// the CTAs of the layer
 // ---------------------------------------------------------------------------------------
 
-struct FinishSmem {
+struct Sweep2Smem {
   union {
     uint32_t hist[kBins];          // the radix passes
     struct {                       // then the blend
@@ -339,56 +324,53 @@ struct FinishSmem {
     } b;
   };
   uint32_t scr[40], res[2];
-  uint32_t cnt[2 * kMaxHeads];     // per head: keys above tau, keys equal to tau
-  uint32_t cstart[kMaxChunks + 1]; // the union's chunk regions, concatenated
-  int64_t sleft;
-  uint32_t flag;
+  uint32_t cnt[2 * kMaxHeads];     // this CTA's per-head counts: above tau, equal to tau
+  uint32_t ok;
 };
 
-// Radix select of the Bp-th largest key over a sequence of keys visited by each(fn), where
-// each(fn) calls fn(key, ok) the same number of times in every thread; pass 0 counts only
-// first digits >= g.  Leaves (tau, keq) in res[0..1].
-template <typename Each>
-__device__ void radix_tau(FinishSmem& sm, uint32_t Bp, uint32_t g, Each&& each) {
-  uint32_t prefix = 0, mask = 0, krem = Bp;
-#pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
-    const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const int nb = pass == 2 ? 1024 : 2048;
-    for (int i = threadIdx.x; i < nb; i += kThreads) sm.hist[i] = 0u;
-    __syncthreads();
-    each([&](uint32_t k, bool ok) {
-      const bool in = ok && (pass == 0 ? (k >> 21) >= g : (k & mask) == prefix);
-      hist_add_runs(sm.hist, in ? (k >> sh) & (uint32_t)(nb - 1) : kNoBin);
-    });
-    __syncthreads();
-    block_pick<kThreads>(sm.hist, nb, krem, sm.scr, sm.res);
-    __syncthreads();
-    prefix |= sm.res[0] << sh;
-    mask |= (uint32_t)(nb - 1) << sh;
-    krem = sm.res[1];
-    __syncthreads();
-  }
+// Barrier of the CTAs of one layer (co-resident: the kernel is a cooperative launch): the
+// call's k-th barrier completes when the layer's counter reaches k * nch.  Writes before it
+// (fenced) are visible after it.  The wait is bounded (1 s); a CTA that gives up records
+// DEV_WAIT_TIMEOUT and waits no more (its layer's results are then invalid).
+__device__ void layer_barrier(uint32_t* ctr, uint32_t target, uint32_t* ok, WsHeader* hdr) {
+  __syncthreads();
   if (threadIdx.x == 0) {
-    sm.res[0] = prefix;
-    sm.res[1] = krem;
+    __threadfence();
+    atomicAdd(ctr, 1u);
+    if (*ok) {
+      const uint64_t t0 = ptx::globaltimer();
+      while (ptx::ld_acquire_u32(ctr) < target) {
+        if (ptx::globaltimer() - t0 > 1000000000ull) {
+          raise_dev(hdr, DEV_WAIT_TIMEOUT, 0xA30u);
+          *ok = 0u;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
   }
   __syncthreads();
 }
 
-// Grid (chunks, layers).  Walks the chunk backwards (the tail keys, the ring's chunks last to
-// first, the head keys) and fills the CTA's union region from its end, so the region
-// [fill, UC) lists the chunk's candidate positions in ascending order.
+// Grid (chunks, layers of this launch), a cooperative launch (every CTA resident).  Each CTA
+// walks its chunk backwards (the tail keys, the ring's chunks last to first, the head keys),
+// listing its candidates from the end of its own region, so [fill, UC) holds them in
+// ascending position order; UC is the chunk's length, so a region cannot overflow.  Then
+// the layer's CTAs run three radix passes over their regions (each pass: shared-memory
+// histogram, added into the layer's global histogram of that pass, a layer barrier, the
+// pick repeated in every CTA), count their keys above and at tau per head into the layer's
+// counters, and after a last barrier the layer's first CTA blends the head budgets.
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
-alloc_sweep2(const float* __restrict__ scores, int Hkv, int C, int nch,
+alloc_sweep2(const float* __restrict__ scores, int Hkv, int C, int nch, int64_t seg0,
              const uint32_t* __restrict__ gbin, const int64_t* __restrict__ bprime,
-             int32_t* __restrict__ upos, uint32_t* __restrict__ ukey, uint32_t* __restrict__ ufill,
-             uint32_t* __restrict__ uover, int64_t UC, uint32_t* __restrict__ done, int w,
-             uint32_t an, uint32_t ad, int32_t* __restrict__ head_budget, WsHeader* hdr) {
-  __shared__ FinishSmem sm;
+             int32_t* __restrict__ upos, uint32_t* __restrict__ ukey, int64_t UC,
+             uint32_t* __restrict__ lhist /*[S][3][kBins]*/, uint32_t* __restrict__ hcnt,
+             uint32_t* __restrict__ lbar, int w, uint32_t an, uint32_t ad,
+             int32_t* __restrict__ head_budget, WsHeader* hdr) {
+  __shared__ Sweep2Smem sm;
   __shared__ uint64_t rfull[kRingStages];
   extern __shared__ __align__(128) unsigned char ring_mem[];
-  const int64_t seg = blockIdx.y;
+  const int64_t seg = seg0 + blockIdx.y;
   const int64_t N = (int64_t)Hkv * C;
   const uint32_t g = gbin[seg];
   const int64_t Bp = bprime[seg];
@@ -399,7 +381,7 @@ alloc_sweep2(const float* __restrict__ scores, int Hkv, int C, int nch,
   int32_t* P = upos + (seg * nch + blockIdx.x) * UC;
   uint32_t* K = ukey + (seg * nch + blockIdx.x) * UC;
   uint32_t fill = (uint32_t)UC;
-  bool over = false;
+  if (threadIdx.x == 0) sm.ok = 1u;
   if (g < 2048u) {
     SweepRing R;
     R.init(ring_mem, rfull);
@@ -413,24 +395,17 @@ alloc_sweep2(const float* __restrict__ scores, int Hkv, int C, int nch,
     auto side = [&](int64_t lo, int64_t hi) {
       if (threadIdx.x == 0) {
         uint32_t f = fill;
-        bool ov = over;
-        for (int64_t i = hi - 1; i >= lo && !ov; --i) {
+        for (int64_t i = hi - 1; i >= lo; --i) {
           const float v = x[i];
           if (!is_cand(v)) continue;
-          if (f == 0u) {
-            ov = true;
-            break;
-          }
           --f;
           P[f] = (int32_t)i;
           K[f] = score_key(v);
         }
         sm.res[0] = f;
-        sm.res[1] = ov ? 1u : 0u;
       }
       __syncthreads();
       fill = sm.res[0];
-      over = sm.res[1] != 0u;
       __syncthreads();
     };
     side(b, i1);
@@ -438,7 +413,6 @@ alloc_sweep2(const float* __restrict__ scores, int Hkv, int C, int nch,
     const bool ok = ring_pass(R, reinterpret_cast<const unsigned char*>(x + a), nullptr, nv * 16,
                               true, [&](const unsigned char* st, const unsigned char*,
                                         int64_t off, uint32_t bytes) {
-      if (over) return;   // the same in every thread
       const int ng = (int)(bytes / 16);
       const float4* v4 = reinterpret_cast<const float4*>(st);
       uint32_t cmu[kPerWarp / 32];
@@ -467,11 +441,7 @@ alloc_sweep2(const float* __restrict__ scores, int Hkv, int C, int nch,
       }
       const uint32_t T = __shfl_sync(0xFFFFFFFFu, ci, kWarps - 1);
       const uint32_t before = __shfl_sync(0xFFFFFFFFu, ci - c, warp);
-      if (T == 0u) return;
-      if (T > fill) {
-        over = true;
-        return;
-      }
+      if (T == 0u) return;   // the same in every thread
       uint32_t o = fill - T + before;
 #pragma unroll
       for (int u = 0; u < kPerWarp / 32; ++u) {
@@ -500,121 +470,79 @@ alloc_sweep2(const float* __restrict__ scores, int Hkv, int C, int nch,
       }
       fill -= T;
     });
-    if (!ok) {
-      if (threadIdx.x == 0) raise_dev(hdr, DEV_WAIT_TIMEOUT, 0xA20u);
-      over = true;
+    if (!ok && threadIdx.x == 0) {
+      raise_dev(hdr, DEV_WAIT_TIMEOUT, 0xA20u);
+      sm.ok = 0u;
     }
-    if (!over) side(i0, a);
+    side(i0, a);
   }
-  if (threadIdx.x == 0) {
-    ufill[seg * nch + blockIdx.x] = fill;
-    if (over) atomicOr(&uover[seg], 1u);
-  }
-  if (!last_of_layer(done + seg, (uint32_t)nch, &sm.flag)) return;
 
-  // ---- the last CTA of the layer: tau, keq and the per-head counts
+  // ---- the exact select over the layer's union (every CTA of the layer takes part)
   for (int i = threadIdx.x; i < 2 * Hkv; i += kThreads) sm.cnt[i] = 0u;
-  const bool overflow = __ldcg(&uover[seg]) != 0u;
-  if (threadIdx.x == 0) {
-    uint32_t s0 = 0;
-    for (int c = 0; c < nch; ++c) {
-      sm.cstart[c] = s0;
-      s0 += (uint32_t)UC - __ldcg(&ufill[seg * nch + c]);
-    }
-    sm.cstart[nch] = s0;
-  }
-  __syncthreads();
+  const int nu = (int)(UC - fill);   // this CTA's candidates: P/K[fill, UC)
+  uint32_t* bar = lbar + seg;
   uint32_t tau = 0xFFFFFFFFu, keq = 0u;   // no key equals 0xFFFFFFFF
   if (Bp > 0) {
-    const uint32_t U = sm.cstart[nch];
-    // union entry t lives in chunk region c (cstart[c] <= t < cstart[c + 1]) at offset
-    // UC - (its region's length) + (t - cstart[c])
-    auto where = [&](uint32_t t) -> int64_t {
-      int lo = 0, hi = nch;
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (sm.cstart[mid] <= t) lo = mid; else hi = mid;
-      }
-      return (seg * nch + lo) * UC + (UC - (int64_t)(sm.cstart[lo + 1] - sm.cstart[lo])) +
-             (int64_t)(t - sm.cstart[lo]);
-    };
-    auto tally = [&](int64_t pos, uint32_t k) {
-      const int h = (int)(pos / C);
-      if (k > tau) atomicAdd(&sm.cnt[2 * h], 1u);
-      else if (k == tau) atomicAdd(&sm.cnt[2 * h + 1], 1u);
-    };
-    if (!overflow && U <= (uint32_t)(kRingBytes / 4)) {
-      // the union's keys, gathered into the (idle) ring memory, 4 loads in flight per thread
-      uint32_t* Ub = reinterpret_cast<uint32_t*>(ring_mem);
-      for (uint32_t tb = 0; tb < U; tb += 4 * kThreads) {
-        uint32_t kk[4];
+    uint32_t prefix = 0, mask = 0, krem = (uint32_t)Bp;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+      const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+      const int nb = pass == 2 ? 1024 : 2048;
+      for (int i = threadIdx.x; i < nb; i += kThreads) sm.hist[i] = 0u;
+      __syncthreads();
+      for (int tb = 0; tb < nu; tb += 8 * kThreads) {
+        uint32_t kk[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t t = tb + u * kThreads + threadIdx.x;
-          kk[u] = t < U ? __ldcg(ukey + where(t)) : 0u;
+        for (int u = 0; u < 8; ++u) {
+          const int tt = tb + u * kThreads + (int)threadIdx.x;
+          kk[u] = tt < nu ? K[fill + tt] : 0u;
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t t = tb + u * kThreads + threadIdx.x;
-          if (t < U) Ub[t] = kk[u];
+        for (int u = 0; u < 8; ++u) {
+          const bool in = tb + u * kThreads + (int)threadIdx.x < nu &&
+                          (pass == 0 ? (kk[u] >> 21) >= g : (kk[u] & mask) == prefix);
+          hist_add_runs(sm.hist, in ? (kk[u] >> sh) & (uint32_t)(nb - 1) : kNoBin);
         }
       }
       __syncthreads();
-      auto each = [&](auto&& fn) {
-        for (uint32_t tb = 0; tb < U; tb += kThreads) {
-          const uint32_t t = tb + threadIdx.x;
-          fn(t < U ? Ub[t] : 0u, t < U);
-        }
-      };
-      radix_tau(sm, (uint32_t)Bp, g, each);
-      tau = sm.res[0];
-      keq = sm.res[1];
-      for (uint32_t t = threadIdx.x; t < U; t += kThreads) {
-        const uint32_t k = Ub[t];
-        if (k >= tau) tally(__ldcg(upos + where(t)), k);
+      uint32_t* G = lhist + (seg * 3 + pass) * kBins;
+      for (int i = threadIdx.x; i < nb; i += kThreads) {
+        const uint32_t c = sm.hist[i];
+        if (c) atomicAdd(&G[i], c);
       }
-    } else if (!overflow) {
-      // a union longer than the ring memory: read from L2, 8 keys per thread in flight
-      auto each = [&](auto&& fn) {
-        for (uint32_t tb = 0; tb < U; tb += 8 * kThreads) {
-          uint32_t kk[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint32_t t = tb + u * kThreads + threadIdx.x;
-            kk[u] = t < U ? __ldcg(ukey + where(t)) : 0u;
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) fn(kk[u], tb + u * kThreads + threadIdx.x < U);
-        }
-      };
-      radix_tau(sm, (uint32_t)Bp, g, each);
-      tau = sm.res[0];
-      keq = sm.res[1];
-      for (uint32_t t = threadIdx.x; t < U; t += kThreads) {
-        const int64_t e = where(t);
-        const uint32_t k = __ldcg(ukey + e);
-        if (k >= tau) tally(__ldcg(upos + e), k);
-      }
-    } else {
-      // every key of the layer
-      auto each = [&](auto&& fn) {
-        for (int64_t ib = 0; ib < N; ib += kThreads) {
-          const int64_t i = ib + threadIdx.x;
-          fn(i < N ? score_key(x[i]) : 0u, i < N);
-        }
-      };
-      radix_tau(sm, (uint32_t)Bp, 0u, each);
-      tau = sm.res[0];
-      keq = sm.res[1];
-      for (int64_t i = threadIdx.x; i < N; i += kThreads) {
-        const uint32_t k = score_key(x[i]);
-        if (k >= tau) tally(i, k);
-      }
+      layer_barrier(bar, (uint32_t)(pass + 1) * (uint32_t)nch, &sm.ok, hdr);
+      for (int i = threadIdx.x; i < nb; i += kThreads) sm.hist[i] = __ldcg(G + i);
+      __syncthreads();
+      block_pick<kThreads>(sm.hist, nb, krem, sm.scr, sm.res);
+      __syncthreads();
+      prefix |= sm.res[0] << sh;
+      mask |= (uint32_t)(nb - 1) << sh;
+      krem = sm.res[1];
+      __syncthreads();
     }
+    tau = prefix;
+    keq = krem;
+    // this CTA's keys above and at tau, per head (every such key is a candidate)
+    for (int tt = threadIdx.x; tt < nu; tt += kThreads) {
+      const uint32_t k = K[fill + tt];
+      if (k < tau) continue;
+      const int h = (int)(P[fill + tt] / C);
+      atomicAdd(&sm.cnt[2 * h + (k > tau ? 0 : 1)], 1u);
+    }
+    __syncthreads();
+    uint32_t* Hc = hcnt + seg * 2 * Hkv;
+    for (int i = threadIdx.x; i < 2 * Hkv; i += kThreads)
+      if (sm.cnt[i]) atomicAdd(&Hc[i], sm.cnt[i]);
+    layer_barrier(bar, 4u * (uint32_t)nch, &sm.ok, hdr);
+    if (blockIdx.x != 0) return;
+    for (int i = threadIdx.x; i < 2 * Hkv; i += kThreads) sm.cnt[i] = __ldcg(Hc + i);
+    __syncthreads();
+  } else if (blockIdx.x != 0) {
+    return;
   }
-  __syncthreads();
-  // f_g: keys above tau in head g, plus tau-equal keys in (head, position) order; then the
-  // safeguard blend in exact integers and the largest remainders (ties to the lower head)
+  // ---- the layer's first CTA: f_g = keys above tau in head g plus tau-equal keys in (head,
+  // position) order; the safeguard blend in exact integers and the largest remainders (ties
+  // to the lower head)
   if (threadIdx.x == 0) {
     const int64_t den = (int64_t)ad * Hkv;
     int64_t left_eq = (int64_t)keq, fsum = 0, flo = 0;
@@ -630,35 +558,51 @@ alloc_sweep2(const float* __restrict__ scores, int Hkv, int C, int nch,
       flo += sm.b.sBg[h];
     }
     if (fsum != Bp) raise_dev(hdr, DEV_SELECT, (unsigned)seg);
-    sm.sleft = Bp - flo;
+    sm.scr[0] = (uint32_t)(Bp - flo);
   }
   __syncthreads();
+  const int64_t left = sm.scr[0];
   for (int h = threadIdx.x; h < Hkv; h += kThreads) {
     const int64_t rh = sm.b.srem[h];
     int64_t before = 0;
     for (int m = 0; m < Hkv; ++m)
       if (sm.b.srem[m] > rh || (sm.b.srem[m] == rh && m < h)) ++before;
-    head_budget[seg * Hkv + h] = sm.b.sBg[h] + (before < sm.sleft ? 1 : 0) + w;
+    head_budget[seg * Hkv + h] = sm.b.sBg[h] + (before < left ? 1 : 0) + w;
   }
 }
 
 // ---------------------------------------------------------------------------------------
 
+// CTAs of alloc_sweep2 that can be resident at once (its cooperative launch needs them all).
+static int64_t sweep2_resident() {
+  static int64_t cached = 0;
+  if (cached == 0) {
+    int occ = 0;
+    if (cudaFuncSetAttribute(alloc_sweep2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kRingBytes) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, alloc_sweep2, kThreads,
+                                                      kRingBytes) != cudaSuccess ||
+        occ < 1)
+      occ = 1;
+    cached = (int64_t)occ * num_sms();
+  }
+  return cached;
+}
+
 AllocPlan alloc_plan(const Shape& s) {
   AllocPlan p{};
   const int64_t S = s.segments();
   const int64_t N = (int64_t)s.Hkv * (s.C() > 0 ? s.C() : 1);
-  // one wave of kMinBlocks CTAs per SM over all layers, at least one ring stage per CTA
-  int64_t nch = (int64_t)num_sms() * kMinBlocks / (S > 0 ? S : 1);
+  // one wave over all layers (or, with more layers than resident CTAs, one CTA per layer and
+  // several launches), at least one ring stage per CTA
+  int64_t nch = sweep2_resident() / (S > 0 ? S : 1);
   const int64_t maxch = cdiv(N, (int64_t)kRingStage / 4);
   if (nch > maxch) nch = maxch;
   if (nch > kMaxChunks) nch = kMaxChunks;
   if (nch < 1) nch = 1;
   nch = cdiv(N, chunk_len(N, (int)nch));   // no empty chunk
   p.nchunkE = (int)nch;
-  // a layer's union holds min(N, kUnionPerLayer) keys, split evenly over its CTAs
-  const int64_t ucap = N < kUnionPerLayer ? N : kUnionPerLayer;
-  p.union_per_cta = cdiv(ucap, nch) + 4;
+  p.union_per_cta = chunk_len(N, (int)nch);   // a chunk's candidates fit in its region
   size_t off = kWsHeader;
   p.off_bprime = off;
   off += align_up((size_t)S * sizeof(int64_t), 256);
@@ -666,12 +610,11 @@ AllocPlan alloc_plan(const Shape& s) {
   off += align_up((size_t)S * nch * sizeof(double2), 256);
   p.off_gbin = off;
   off += align_up((size_t)S * sizeof(uint32_t), 256);
-  p.off_ufill = off;
-  off += align_up((size_t)S * nch * sizeof(uint32_t), 256);
-  p.off_zero = off;   // cleared by every call: done counters, overflow flags, histograms
-  off += align_up((size_t)S * sizeof(uint32_t), 256);
+  p.off_zero = off;   // cleared by every call: barriers, histograms, per-head counts
   off += align_up((size_t)S * sizeof(uint32_t), 256);
   off += align_up((size_t)S * kBins * sizeof(uint32_t), 256);
+  off += align_up((size_t)S * 3 * kBins * sizeof(uint32_t), 256);
+  off += align_up((size_t)S * 2 * s.Hkv * sizeof(uint32_t), 256);
   p.off_union = off;
   off += align_up((size_t)S * nch * p.union_per_cta * sizeof(int32_t), 256);
   off += align_up((size_t)S * nch * p.union_per_cta * sizeof(uint32_t), 256);
@@ -693,17 +636,18 @@ cudaError_t launch_allocate(const Shape& s, const float* scores, const int64_t* 
   int64_t* bprime = reinterpret_cast<int64_t*>(ws + p.off_bprime);
   double2* part = reinterpret_cast<double2*>(ws + p.off_epart);
   uint32_t* gbin = reinterpret_cast<uint32_t*>(ws + p.off_gbin);
-  uint32_t* ufill = reinterpret_cast<uint32_t*>(ws + p.off_ufill);
   char* z = ws + p.off_zero;
-  uint32_t* done = reinterpret_cast<uint32_t*>(z);
-  z += align_up((size_t)S * sizeof(uint32_t), 256);
-  uint32_t* uover = reinterpret_cast<uint32_t*>(z);
+  uint32_t* lbar = reinterpret_cast<uint32_t*>(z);
   z += align_up((size_t)S * sizeof(uint32_t), 256);
   uint32_t* ghist = reinterpret_cast<uint32_t*>(z);
+  z += align_up((size_t)S * kBins * sizeof(uint32_t), 256);
+  uint32_t* lhist = reinterpret_cast<uint32_t*>(z);
+  z += align_up((size_t)S * 3 * kBins * sizeof(uint32_t), 256);
+  uint32_t* hcnt = reinterpret_cast<uint32_t*>(z);
   int32_t* upos = reinterpret_cast<int32_t*>(ws + p.off_union);
   uint32_t* ukey = reinterpret_cast<uint32_t*>(
       ws + p.off_union + align_up((size_t)S * nch * UC * sizeof(int32_t), 256));
-  // counters, flags and histograms start at zero
+  // barriers, histograms and counts start at zero
   cudaError_t e = cudaMemsetAsync(ws + p.off_zero, 0, p.off_union - p.off_zero, st);
   if (e != cudaSuccess) return e;
   static bool opted = false;   // the sweeps' rings are dynamic shared memory above 48 KB
@@ -724,10 +668,28 @@ cudaError_t launch_allocate(const Shape& s, const float* scores, const int64_t* 
   alloc_bound<<<(unsigned)S, kThreads, 0, st>>>(part, nch, s.L, s.Hkv, s.n, s.w, C, budget,
                                                 entropy_mode, layer_budget, bprime, ghist, gbin,
                                                 hdr);
-  alloc_sweep2<<<sweep, kThreads, kRingBytes, st>>>(scores, s.Hkv, C, nch, gbin, bprime, upos,
-                                                    ukey, ufill, uover, UC, done, s.w, an, ad,
-                                                    head_budget, hdr);
-  count_launches(3);
+  count_launches(2);
+  // sweep 2 is a cooperative launch (the CTAs of a layer wait for one another), over as many
+  // layers at a time as can be resident
+  const int64_t per_launch = sweep2_resident() / nch > 0 ? sweep2_resident() / nch : 1;
+  for (int64_t s0 = 0; s0 < S; s0 += per_launch) {
+    const int64_t sb = S - s0 < per_launch ? S - s0 : per_launch;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)nch, (unsigned)sb);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kRingBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, alloc_sweep2, scores, s.Hkv, C, nch, s0,
+                           (const uint32_t*)gbin, (const int64_t*)bprime, upos, ukey, UC, lhist,
+                           hcnt, lbar, s.w, an, ad, head_budget, hdr);
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+  }
   return cudaGetLastError();
 }
 

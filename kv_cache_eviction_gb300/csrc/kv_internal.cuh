@@ -37,7 +37,7 @@ cudaError_t launch_score_fixup(const float* halo, const float* vbar, int64_t uni
 struct AllocPlan {
   int nchunkE;            // sweep CTAs per segment
   int64_t union_per_cta;  // candidate keys one sweep CTA can list
-  size_t off_bprime, off_epart, off_gbin, off_ufill, off_zero, off_union, off_end;
+  size_t off_bprime, off_epart, off_gbin, off_zero, off_union, off_end;
 };
 AllocPlan alloc_plan(const Shape& s);
 cudaError_t launch_allocate(const Shape& s, const float* scores, const int64_t* budget,
