@@ -13,8 +13,8 @@
 // K-th largest key, has one too.  Pass B, walking the head backwards (its first chunks are
 // the ones pass A left in L2), collects every key with a first digit >= g (and every forced
 // position) into shared memory in position order.  The exact radix select and the ordered
-// emission then work on that short union alone.  A union that would not fit falls back to
-// the radix select over the whole head (a cluster of one CTA, keys read from global memory).
+// emission then work on that short union alone.  A union that outgrows shared memory (large
+// budgets) moves to the head's region of the workspace, which has room for every key.
 #include <cstdlib>
 #include <cstring>
 
@@ -106,6 +106,7 @@ struct ScoreSrc {            // Ada-KV / LAVa scores; CriticalKV stage 1
   }
   __device__ uint32_t key_at(int i) const { return score_key(S[i]); }
   __device__ bool forced_at(int) const { return false; }
+  __device__ bool forced_key(uint32_t) const { return false; }
   // the largest key of a group whose four values all lie in the head (score_key is
   // monotonic, and fmaxf skips a NaN as score_key maps it to the smallest key)
   __device__ uint32_t full_max(const float4& x, const float4&, int) const {
@@ -126,11 +127,18 @@ struct KappaSrc {            // CriticalKV stage 2: stage-1 positions are forced
   static constexpr bool kTwo = true;
   const float* S;            // the head's scores
   const float* Cn;           // the head's ||(V W^O)_j||_1
-  const uint32_t* F;         // the head's stage-1 bits
+  const uint32_t* F;         // the head's stage-1 bits (bits_mode)
   float eps;
   int C;
-  __device__ bool in1(int p) const {
-    return p >= 0 && p < C && ((__ldcg(F + (p >> 5)) >> (p & 31)) & 1u) != 0u;
+  bool bits_mode;
+  uint32_t tau1;             // otherwise stage 1 kept key > tau1, and key == tau1 at
+  int pcut1;                 // positions <= pcut1
+  // stage-1 membership of position p with score s
+  __device__ bool in1(int p, float s) const {
+    if (p < 0 || p >= C) return false;
+    if (bits_mode) return ((__ldcg(F + (p >> 5)) >> (p & 31)) & 1u) != 0u;
+    const uint32_t k = score_key(s);
+    return k > tau1 || (k == tau1 && p <= pcut1);
   }
   __device__ uint32_t kappa_key(float s, float c) const {
     return score_key(__fmul_rn(__fadd_rn(s, eps), c)) + 1u;
@@ -140,12 +148,17 @@ struct KappaSrc {            // CriticalKV stage 2: stage-1 positions are forced
     const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      f[c] = in1(pos0 + c);
+      f[c] = in1(pos0 + c, xs[c]);
       k[c] = f[c] ? 0u : kappa_key(xs[c], ys[c]);
     }
   }
-  __device__ uint32_t key_at(int i) const { return in1(i) ? 0u : kappa_key(S[i], Cn[i]); }
-  __device__ bool forced_at(int i) const { return in1(i); }
+  __device__ uint32_t key_at(int i) const {
+    const float s = S[i];
+    return in1(i, s) ? 0u : kappa_key(s, Cn[i]);
+  }
+  __device__ bool forced_at(int i) const { return in1(i, S[i]); }
+  // a listed entry with key k is forced exactly when k is 0 (a kappa key is at least 1)
+  __device__ bool forced_key(uint32_t k) const { return k == 0u; }
   __device__ uint32_t full_max(const float4& x, const float4& y, int pos0) const {
     uint32_t k[4];
     bool f[4];
@@ -173,23 +186,36 @@ struct HeadSelSmem {
 };
 using SelRing = BulkRing<kSelStages, kSelStage>;
 
+// What select_head produces: the kept positions as rows, or as bits (the whole-head
+// select only), or only tau and the position of the last kept tau-equal key (the
+// streaming select only; CriticalKV stage 1).
+enum { kOutRows = 0, kOutBits = 1, kOutTau = 2 };
+
 // Ordered selection of one head's positions [0, C), keys and forced positions from `src`
 // (staged values from stream base pointers s0 / s1 = flat index 0 of the arrays).  keep(j)
 // = forced(j) || key(j) > tau || (key(j) == tau && j is among the keq lowest tau-equal
-// positions), tau the K-th largest key.  Kept positions go in ascending order to
-// kept[base + r] (rows >= cap skipped) or, BITS, as bits of bits[] (the head's words).
-// Returns the number kept; ok turns false (the same in every thread) if a wait gave up.
-template <bool BITS, class Src>
+// positions), tau the K-th largest key.  kOutRows: kept positions in ascending order to
+// kept[base + r] (rows >= cap skipped); kOutBits: bits of bits[] (the head's words);
+// kOutTau: *tau_out = tau and *pcut_out = the position of the keq-th tau-equal key (-1 when
+// keq is 0), so keep(j) = key(j) > tau || (key(j) == tau && j <= pcut).  Returns the number
+// kept; ok turns false (the same in every thread) if a wait gave up.
+template <int OUT, class Src>
 __device__ uint32_t select_head(SelRing& R, HeadSelSmem& sm, unsigned char* ring_mem,
                                 const Src& src, const float* s0, const float* s1, int64_t flat0,
                                 int C, int64_t K, int32_t* kept, int64_t base, int64_t cap,
-                                uint32_t* bits, bool streaming, bool& ok) {
+                                uint32_t* bits, int32_t* gpos, uint32_t* gkey, bool streaming,
+                                bool& ok, uint32_t* tau_out = nullptr, int* pcut_out = nullptr) {
+  constexpr bool BITS = OUT == kOutBits;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t below = (1u << lane) - 1u;
   const bool any = K > 0;
   if (!any && !Src::kTwo) {   // nothing to select and nothing forced
     if (BITS)
       for (int wd = threadIdx.x; wd < (C + 31) / 32; wd += kSelThreads) bits[wd] = 0u;
+    if (OUT == kOutTau && threadIdx.x == 0) {
+      *tau_out = 0xFFFFFFFFu;
+      *pcut_out = -1;
+    }
     __syncthreads();
     return 0;
   }
@@ -269,7 +295,7 @@ __device__ uint32_t select_head(SelRing& R, HeadSelSmem& sm, unsigned char* ring
     // ---- pass B: the union of keys with first digit >= g and forced positions, filled from
     // the end of the buffer backwards (chunks come last to first), so it ends up ascending
     uint32_t fill = kUnion;
-    bool over = false;
+    bool spilled = false;   // the union moved to the head's global region (C entries)
     if (threadIdx.x == 0) {
       uint32_t fl = kUnion;
       for (int64_t i = tail0 + tailn - 1; i >= tail0; --i) {
@@ -324,10 +350,19 @@ __device__ uint32_t select_head(SelRing& R, HeadSelSmem& sm, unsigned char* ring
       const uint32_t T = __shfl_sync(0xFFFFFFFFu, ci, kSelWarps - 1);
       const uint32_t before = __shfl_sync(0xFFFFFFFFu, ci - c, warp);
       if (T == 0u) return;   // the same in every thread
-      if (over || T > fill) {
-        over = true;         // the same in every thread
-        return;
+      if (!spilled && T > fill) {
+        // the shared-memory union is full: move it to the end of the head's global region
+        // (room for every key of the head) and go on there
+        const uint32_t n = kUnion - fill;
+        for (uint32_t t = threadIdx.x; t < n; t += kSelThreads) {
+          gpos[C - n + t] = sm.upos[fill + t];
+          gkey[C - n + t] = sm.ukey[fill + t];
+        }
+        fill = (uint32_t)C - n;
+        spilled = true;      // the same in every thread
       }
+      int32_t* UP = spilled ? gpos : sm.upos;
+      uint32_t* UK = spilled ? gkey : sm.ukey;
       uint32_t o = fill - T + before;
 #pragma unroll
       for (int u = 0; u < kPerWarp / 32; ++u) {
@@ -348,8 +383,8 @@ __device__ uint32_t select_head(SelRing& R, HeadSelSmem& sm, unsigned char* ring
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             if ((cmu[u] >> c) & 1u) {
-              sm.upos[q] = pos0 + c;
-              sm.ukey[q] = k[c];
+              UP[q] = pos0 + c;
+              UK[q] = k[c];
               ++q;
             }
           }
@@ -359,8 +394,11 @@ __device__ uint32_t select_head(SelRing& R, HeadSelSmem& sm, unsigned char* ring
       fill -= T;
     });
     if (!ok) return 0;
-    if (!over) {
-      const int u0 = (int)fill, nu = kUnion - (int)fill;
+    {
+      const int u0 = (int)fill, nu = (spilled ? C : kUnion) - (int)fill;
+      // the union's entries (written by this CTA before the last barrier of the pass)
+      auto ukey_at = [&](int t) -> uint32_t { return spilled ? gkey[t] : sm.ukey[t]; };
+      auto upos_at = [&](int t) -> int { return spilled ? gpos[t] : sm.upos[t]; };
       // ---- tau and keq over the union (every key above tau, and tau's first digit, is in it)
       uint32_t prefix = 0, mask = 0, krem = any ? (uint32_t)K : 0u;
       if (any) {
@@ -370,12 +408,21 @@ __device__ uint32_t select_head(SelRing& R, HeadSelSmem& sm, unsigned char* ring
           const int nb = pass == 2 ? 1024 : 2048;
           for (int i = threadIdx.x; i < nb; i += kSelThreads) sm.hist[i] = 0u;
           __syncthreads();
-          for (int b0 = 0; b0 < nu; b0 += kSelThreads) {
-            const int t = b0 + (int)threadIdx.x;
-            const uint32_t k = t < nu ? sm.ukey[u0 + t] : 0u;
-            // (forced positions have key 0: counted like every key, as in the full select)
-            const bool in = t < nu && (pass == 0 ? (k >> 21) >= g : (k & mask) == prefix);
-            hist_add_runs(sm.hist, in ? (k >> sh) & (uint32_t)(nb - 1) : kNoBin);
+          for (int b0 = 0; b0 < nu; b0 += 8 * kSelThreads) {
+            uint32_t kk[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int t = b0 + u * kSelThreads + (int)threadIdx.x;
+              kk[u] = t < nu ? ukey_at(u0 + t) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int t = b0 + u * kSelThreads + (int)threadIdx.x;
+              // (forced positions have key 0: counted like every key, as in the full select)
+              const bool in =
+                  t < nu && (pass == 0 ? (kk[u] >> 21) >= g : (kk[u] & mask) == prefix);
+              hist_add_runs(sm.hist, in ? (kk[u] >> sh) & (uint32_t)(nb - 1) : kNoBin);
+            }
           }
           __syncthreads();
           block_pick<kSelThreads>(sm.hist, nb, krem, sm.scr, sm.res);
@@ -393,8 +440,8 @@ __device__ uint32_t select_head(SelRing& R, HeadSelSmem& sm, unsigned char* ring
       const int e0 = u0 + min(nu, warp * per), e1 = u0 + min(nu, warp * per + per);
       uint32_t nkeep = 0, neq = 0;
       for (int t = e0 + lane; t < e1; t += 32) {
-        const uint32_t k = sm.ukey[t];
-        const bool f = src.forced_at(sm.upos[t]);
+        const uint32_t k = ukey_at(t);
+        const bool f = src.forced_key(k);
         nkeep += (f || k > tau) ? 1u : 0u;
         neq += (!f && k == tau) ? 1u : 0u;
       }
@@ -404,9 +451,32 @@ __device__ uint32_t select_head(SelRing& R, HeadSelSmem& sm, unsigned char* ring
         sm.scr[warp] = nkeep;
         sm.scr[32 + warp] = neq;
       }
-      if (BITS)
-        for (int wd = threadIdx.x; wd < (C + 31) / 32; wd += kSelThreads) bits[wd] = 0u;
       __syncthreads();
+      if (OUT == kOutTau) {
+        // the keq-th tau-equal entry of the union: the warp whose slice holds it finds it
+        uint32_t eqb = 0;
+        for (int w = 0; w < warp; ++w) eqb += sm.scr[32 + w];
+        const uint32_t mine = sm.scr[32 + warp];
+        if (keq > 0u && eqb < keq && keq <= eqb + mine) {
+          uint32_t seen = eqb;
+          for (int tb = e0; tb < e1; tb += 32) {
+            const int t = tb + lane;
+            const uint32_t k = t < e1 ? ukey_at(t) : 0u;
+            const bool iseq = t < e1 && !src.forced_key(k) && k == tau;
+            const uint32_t meq = __ballot_sync(0xFFFFFFFFu, iseq);
+            if (iseq && seen + __popc(meq & below) + 1u == keq) sm.res[0] = (uint32_t)upos_at(t);
+            seen += __popc(meq);
+            if (seen >= keq) break;   // the same in every lane
+          }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          *tau_out = tau;
+          *pcut_out = keq > 0u ? (int)sm.res[0] : -1;
+        }
+        __syncthreads();
+        return 0;
+      }
       uint32_t eqc = 0, outc = 0, total = 0;
       {
         uint32_t eq = 0;
@@ -424,17 +494,15 @@ __device__ uint32_t select_head(SelRing& R, HeadSelSmem& sm, unsigned char* ring
       for (int tb = e0; tb < e1; tb += 32) {
         const int t = tb + lane;
         const bool in = t < e1;
-        const uint32_t k = in ? sm.ukey[t] : 0u;
-        const int j = in ? sm.upos[t] : 0;
-        const bool f = in && src.forced_at(j);
+        const uint32_t k = in ? ukey_at(t) : 0u;
+        const int j = in ? upos_at(t) : 0;
+        const bool f = in && src.forced_key(k);
         const bool iseq = in && !f && k == tau;
         bool keep = in && (f || k > tau);
         const uint32_t meq = __ballot_sync(0xFFFFFFFFu, iseq);
         if (iseq && eqc + __popc(meq & below) < keq) keep = true;
         const uint32_t mk = __ballot_sync(0xFFFFFFFFu, keep);
-        if (BITS) {
-          if (keep) atomicOr(bits + (j >> 5), 1u << (j & 31));
-        } else if (keep) {
+        if (keep) {
           const int64_t row = base + outc + __popc(mk & below);
           if (row < cap) kept[row] = j;
         }
@@ -462,7 +530,8 @@ head_select(const float* __restrict__ scores, const float* __restrict__ crit, ui
             uint32_t cad, float ceps, const int32_t* __restrict__ lens,
             const int64_t* __restrict__ cu, int Hkv, int C, int w, int reserve,
             int32_t* __restrict__ kept, int64_t cap, uint32_t* __restrict__ flags, int64_t words,
-            int streaming, WsHeader* hdr) {
+            int32_t* __restrict__ gpos, uint32_t* __restrict__ gkey, int streaming,
+            WsHeader* hdr) {
   __shared__ HeadSelSmem sm;
   extern __shared__ __align__(128) unsigned char ring_mem[];
   const int64_t h = blockIdx.x;
@@ -478,21 +547,33 @@ head_select(const float* __restrict__ scores, const float* __restrict__ crit, ui
   uint32_t n = 0;
   if (!CRIT) {
     const ScoreSrc src{scores + flat0};
-    n = select_head<false>(R, sm, ring_mem, src, scores, nullptr, flat0, C, Bg, kept, base, cap,
-                           nullptr, streaming != 0, ok);
+    n = select_head<kOutRows>(R, sm, ring_mem, src, scores, nullptr, flat0, C, Bg, kept, base,
+                              cap, nullptr, gpos + flat0, gkey + flat0, streaming != 0, ok);
   } else {
     uint32_t* F = flags + h * words;
     const int64_t K1 = ((int64_t)can * Bg) / cad;
     const int64_t K2 = Bg - K1;
     const ScoreSrc src1{scores + flat0};
-    (void)select_head<true>(R, sm, ring_mem, src1, scores, nullptr, flat0, C, K1, nullptr, 0, 0,
-                            F, streaming != 0, ok);
-    __syncthreads();   // the stage-1 bits are complete
-    if (ok) {
-      const KappaSrc src2{scores + flat0, crit + flat0, F, ceps, C};
-      n = select_head<false>(R, sm, ring_mem, src2, scores, crit, flat0, C, K2, kept, base, cap,
-                             nullptr, streaming != 0, ok);
+    KappaSrc src2{scores + flat0, crit + flat0, F, ceps, C, false, 0u, -1};
+    if (streaming) {
+      // stage 1 yields its threshold and tie cut; stage 2 tests membership from the score
+      __shared__ uint32_t tau1;
+      __shared__ int pcut1;
+      (void)select_head<kOutTau>(R, sm, ring_mem, src1, scores, nullptr, flat0, C, K1, nullptr,
+                                 0, 0, nullptr, gpos + flat0, gkey + flat0, true, ok, &tau1,
+                                 &pcut1);
+      __syncthreads();
+      src2.tau1 = tau1;
+      src2.pcut1 = pcut1;
+    } else {
+      (void)select_head<kOutBits>(R, sm, ring_mem, src1, scores, nullptr, flat0, C, K1, nullptr,
+                                  0, 0, F, gpos + flat0, gkey + flat0, false, ok);
+      __syncthreads();   // the stage-1 bits are complete
+      src2.bits_mode = true;
     }
+    if (ok)
+      n = select_head<kOutRows>(R, sm, ring_mem, src2, scores, crit, flat0, C, K2, kept, base,
+                                cap, nullptr, gpos + flat0, gkey + flat0, streaming != 0, ok);
   }
   if (threadIdx.x == 0) {
     if (!ok) raise_dev(hdr, DEV_WAIT_TIMEOUT, 0x800u + (unsigned)(h & 0xFF));
@@ -548,6 +629,10 @@ CompactPlan compact_plan(const Shape& s, bool critical) {
   p.off_flags = off;
   p.flag_words = critical ? cdiv(s.C() > 0 ? s.C() : 1, 32) : 0;
   off += align_up((size_t)s.units() * p.flag_words * sizeof(uint32_t), 256);
+  // a head's candidate union, when it outgrows shared memory: room for every key
+  p.off_union = off;
+  off += align_up((size_t)s.units() * (s.C() > 0 ? s.C() : 0) * sizeof(int32_t), 256);
+  off += align_up((size_t)s.units() * (s.C() > 0 ? s.C() : 0) * sizeof(uint32_t), 256);
   p.off_end = off;
   return p;
 }
@@ -568,6 +653,9 @@ cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const f
                            (reinterpret_cast<uintptr_t>(scores) & 15u) == 0 &&
                            (crit == nullptr || (reinterpret_cast<uintptr_t>(crit) & 15u) == 0);
     const size_t ring_bytes = (size_t)kSelStages * kSelStage;
+    int32_t* gpos = reinterpret_cast<int32_t*>(ws + p.off_union);
+    uint32_t* gkey = reinterpret_cast<uint32_t*>(
+        ws + p.off_union + align_up((size_t)H * C * sizeof(int32_t), 256));
     auto kern = crit ? head_select<true> : head_select<false>;
     static bool opted[2] = {false, false};
     if (!opted[crit ? 1 : 0]) {
@@ -592,7 +680,7 @@ cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const f
     cudaError_t e = cudaLaunchKernelEx(
         &cfg, kern, scores, crit, can, cad, ceps, (const int32_t*)lens, (const int64_t*)cu, s.Hkv,
         C, s.w, reserve, kept, cap, reinterpret_cast<uint32_t*>(ws + p.off_flags), p.flag_words,
-        streaming ? 1 : 0, hdr);
+        gpos, gkey, streaming ? 1 : 0, hdr);
     if (e != cudaSuccess) return e;
   }
   const int row_bytes = s.d * s.esize();

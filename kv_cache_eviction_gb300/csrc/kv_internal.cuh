@@ -46,7 +46,7 @@ cudaError_t launch_allocate(const Shape& s, const float* scores, const int64_t* 
 
 // ----------------------------- compaction ----------------------------------
 struct CompactPlan {
-  size_t off_flags, off_end;
+  size_t off_flags, off_union, off_end;
   int64_t flag_words;   // per head, when CriticalKV stage-1 flags are needed
 };
 CompactPlan compact_plan(const Shape& s, bool critical);
