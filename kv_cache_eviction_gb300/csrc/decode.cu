@@ -1,4 +1,5 @@
-// One decode step of attention over the flat cache.
+// One decode step of attention over the flat cache (caches whose heads average more than a
+// thousand rows; shorter ones go to decode_head.cu).
 //
 // Ada-KV formal model: the new token's k, v are appended to its head's cache,
 // then A = softmax(q K^T / sqrt(d)) and o = A V per query head; the flat layout
@@ -22,6 +23,9 @@
 //   decode_attn     persistent CTAs (as many as fit), every warp a worker.
 //   decode_combine  heads that span several chunks: merges their partials.
 // The second and third kernels are programmatic dependents of the one before.
+#include <cstdlib>
+#include <cstring>
+
 #include "kv_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -611,13 +615,13 @@ static cudaError_t launch_attn(const Shape& s, const T* q, const void* kf, const
                                cudaStream_t st) {
   const size_t smem = sizeof(DecSmem);
   auto kern = decode_attn<T, GM, LPRT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
-  // resident CTAs per SM, looked up once per instantiation
+  // the shared-memory opt-in and the resident CTAs per SM, once per instantiation (host work
+  // on every call would delay the launches behind it)
   static const int per_sm = [&]() {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem) != cudaSuccess)
       return 0;
     return n;
   }();
@@ -687,12 +691,26 @@ static cudaError_t launch_attn_g(const Shape& s, const T* q, const void* kf, con
                             s.d, cap, C);
 }
 
+// KVEVICT_DECODE_PATH=rows forces the row-balanced split for every shape, =heads the
+// one-CTA-per-head kernel wherever its row size allows, whatever the head lengths (tests
+// compare the two decode paths).
+static int decode_path_forced() {
+  const char* e = std::getenv("KVEVICT_DECODE_PATH");
+  if (e == nullptr) return 0;
+  if (std::strcmp(e, "rows") == 0) return 1;
+  if (std::strcmp(e, "heads") == 0) return 2;
+  return 0;
+}
+
 cudaError_t launch_decode(const Shape& s, const void* q, const void* kn, const void* vn,
                           void* kf, void* vf, const int64_t* cu, int32_t* lens, int64_t cap,
                           float scale, void* out, char* ws, const DecodePlan& p,
                           cudaStream_t st) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   const int64_t H = s.units();
+  const int forced = decode_path_forced();
+  if (forced != 1 && decode_head_supported(s, forced == 2 ? 0 : cap))
+    return launch_decode_head(s, q, kn, vn, kf, vf, cu, lens, cap, scale, out, hdr, st);
   const int row_bytes = s.d * s.esize();
   const int Ct = kStageBytes / row_bytes;
   int64_t C = cdiv(cap, p.max_chunks);

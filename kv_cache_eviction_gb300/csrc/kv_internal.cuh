@@ -67,6 +67,16 @@ cudaError_t launch_decode(const Shape& s, const void* q, const void* kn, const v
                           float scale, void* out, char* ws, const DecodePlan& p,
                           cudaStream_t st);
 
+// Decode with one CTA per KV head (decode_head.cu): rows of 256 bytes, G <= 8, and at most
+// this many flat rows per head on average (beyond it the row-balanced split of decode.cu
+// evens out uneven heads better).
+constexpr int64_t kDecodeHeadRowsMax = 1024;
+bool decode_head_supported(const Shape& s, int64_t cap);
+cudaError_t launch_decode_head(const Shape& s, const void* q, const void* kn, const void* vn,
+                               void* kf, void* vf, const int64_t* cu, int32_t* lens,
+                               int64_t cap, float scale, void* out, WsHeader* hdr,
+                               cudaStream_t st);
+
 int num_sms();
 // Largest dynamic + static shared memory one CTA may opt in to.
 size_t max_smem_optin();

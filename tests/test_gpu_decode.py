@@ -1,14 +1,17 @@
 """flat_decode_attn against the oracle on hand-built flat caches.
 
 The caches are built directly (no scoring or compaction) so that the per-head lengths can
-be pushed to the cases the decode kernel has to get right: empty heads, one-row heads, heads
+be pushed to the cases the decode kernels have to get right: empty heads, one-row heads, heads
 longer than a whole row chunk (their partials are merged across CTAs), heads sharing a
 chunk, reserve rows exhausted, and every lane layout (16-byte slices per row of 1, 2, 4, 8,
-16 and 32) and group size 1, 2, 3, 4, 8.
+16 and 32) and group size 1, 2, 3, 4, 8.  Every case runs through both decode kernels (the
+one-CTA-per-head kernel takes the 256-byte-row cases; the others fall through to the
+row-balanced split either way).
 """
 from __future__ import annotations
 
 import math
+import os
 
 import numpy as np
 import pytest
@@ -20,6 +23,19 @@ import oracle as O
 from .kvpath import np64, workspace
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=["heads", "rows"], autouse=True)
+def decode_path(request):
+    """Every case through both decode kernels: one CTA per KV head (used for 256-byte rows
+    when heads are short) and the row-balanced split (the rest)."""
+    old = os.environ.get("KVEVICT_DECODE_PATH")
+    os.environ["KVEVICT_DECODE_PATH"] = request.param
+    yield request.param
+    if old is None:
+        os.environ.pop("KVEVICT_DECODE_PATH", None)
+    else:
+        os.environ["KVEVICT_DECODE_PATH"] = old
 
 
 def build_cache(B, L, hkv, G, d, lens, reserve, dtype, seed):
