@@ -1,5 +1,6 @@
-// One decode step of attention over the flat cache (caches whose heads average more than a
-// thousand rows; shorter ones go to decode_head.cu).
+// One decode step of attention over the flat cache: the entry point that picks one of three
+// kernels (one CTA per head in decode_head.cu, the one-launch split of decode_split.cu, or
+// the row-balanced split below, for many long heads).
 //
 // Ada-KV formal model: the new token's k, v are appended to its head's cache,
 // then A = softmax(q K^T / sqrt(d)) and o = A V per query head; the flat layout
@@ -589,13 +590,17 @@ DecodePlan decode_plan(const Shape& s) {
   int64_t target = (int64_t)num_sms() * 32;
   if (target < 4 * units) target = 4 * units;
   p.max_chunks = target;
+  p.part_slots = target + units;
   size_t off = kWsHeader;
   p.off_part = off;
-  off += align_up((size_t)(target + units) * (kPartHead + s.G() * s.d) * sizeof(float), 256);
+  off += align_up((size_t)p.part_slots * (kPartHead + s.G() * s.d) * sizeof(float), 256);
   p.off_map = off;
   off += align_up((size_t)target * sizeof(uint32_t), 256);
   p.off_work = off;
   off += 256;
+  // tickets of decode_split (zero between launches): CTAs past the scan, then one per head
+  p.off_tick = off;
+  off += align_up((size_t)(1 + units) * sizeof(uint32_t), 256);
   p.off_end = off;
   return p;
 }
@@ -691,14 +696,15 @@ static cudaError_t launch_attn_g(const Shape& s, const T* q, const void* kf, con
                             s.d, cap, C);
 }
 
-// KVEVICT_DECODE_PATH=rows forces the row-balanced split for every shape, =heads the
-// one-CTA-per-head kernel wherever its row size allows, whatever the head lengths (tests
-// compare the two decode paths).
+// KVEVICT_DECODE_PATH=rows forces the row-balanced split of this file for every shape,
+// =heads the one-CTA-per-head kernel and =split the one-launch split wherever their row size
+// and group allow, whatever the head lengths (tests compare the decode paths).
 static int decode_path_forced() {
   const char* e = std::getenv("KVEVICT_DECODE_PATH");
   if (e == nullptr) return 0;
   if (std::strcmp(e, "rows") == 0) return 1;
   if (std::strcmp(e, "heads") == 0) return 2;
+  if (std::strcmp(e, "split") == 0) return 3;
   return 0;
 }
 
@@ -709,7 +715,25 @@ cudaError_t launch_decode(const Shape& s, const void* q, const void* kn, const v
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   const int64_t H = s.units();
   const int forced = decode_path_forced();
-  if (forced != 1 && decode_head_supported(s, forced == 2 ? 0 : cap))
+  // Measured on GB300 (L2 flushed, log-normal head lengths): one CTA per head wins while
+  // the heads fit one wave and are short (every kernel is latency-bound there); the
+  // one-launch split wins from there to about 1.5K rows per head, and at any length when
+  // the heads are few; many long heads stream best through the row-balanced split here.
+  const int64_t rows_per_head = cap / H;
+  const bool few_heads = H <= 2 * (int64_t)num_sms();
+  if (forced == 0) {
+    if (few_heads && rows_per_head <= kDecodeHeadShortRows && decode_head_supported(s, cap))
+      return launch_decode_head(s, q, kn, vn, kf, vf, cu, lens, cap, scale, out, hdr, st);
+    if ((few_heads || rows_per_head <= kDecodeSplitRowsMax) && decode_split_supported(s, cap))
+      return launch_decode_split(s, q, kn, vn, kf, vf, cu, lens, cap, scale, out,
+                                 reinterpret_cast<float*>(ws + p.off_part), p.part_slots,
+                                 reinterpret_cast<uint32_t*>(ws + p.off_tick), hdr, st);
+  } else if (forced == 3 && decode_split_supported(s, cap)) {
+    return launch_decode_split(s, q, kn, vn, kf, vf, cu, lens, cap, scale, out,
+                               reinterpret_cast<float*>(ws + p.off_part), p.part_slots,
+                               reinterpret_cast<uint32_t*>(ws + p.off_tick), hdr, st);
+  }
+  if (forced != 1 && decode_head_supported(s, forced >= 2 ? 0 : cap))
     return launch_decode_head(s, q, kn, vn, kf, vf, cu, lens, cap, scale, out, hdr, st);
   const int row_bytes = s.d * s.esize();
   const int Ct = kStageBytes / row_bytes;

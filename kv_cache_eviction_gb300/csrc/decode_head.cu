@@ -11,57 +11,25 @@
 // token's row is read straight from k_new / v_new, the warps' (max, sum, o) are merged in
 // shared memory, and the CTA finally appends the new row and bumps the head's length.  One
 // launch, no partials in global memory.  Rows of 256 bytes (bf16 d = 128, fp32 d = 64):
-// 16 lanes per row, two rows per warp step.
-#include "kv_internal.cuh"
-#include "tc_ptx.cuh"
+// 16 lanes per row, tiles of 32 scores per warp (RowTileAttn).
+#include "decode_rows16.cuh"
 
 namespace kv {
 
 namespace {
+using namespace r16;
 constexpr int kHWarps = 4;
 constexpr int kHThreads = kHWarps * 32;
-constexpr int kHStages = 3;
-constexpr int kHRows = 16;                   // rows per ring stage
-constexpr int kHRowBytes = 256;
-constexpr int kHStageBytes = kHRows * kHRowBytes;
+constexpr int kHStages = kStages;
+constexpr int kHRows = kStageRows;
+constexpr int kHRowBytes = kRowBytes;
 
-// Every warp's stages start on a 128-byte boundary (bulk copies need 16-byte aligned shared
-// memory destinations; the barriers would otherwise leave warps 1..3 at an 8-byte offset).
-struct __align__(128) HeadWarpSmem {
-  unsigned char st[kHStages][2][kHStageBytes];   // [stage][K, V]
-  uint64_t full[kHStages];
-};
-static_assert(sizeof(HeadWarpSmem) % 128 == 0, "per-warp stages stay 128-byte aligned");
 struct HeadSmem {
-  HeadWarpSmem w[kHWarps];
+  WarpRing w[kHWarps];
 };
-
-__device__ __forceinline__ void unpack_row16(const uint4& r, float2 (&f)[4]) {   // bf16 x 8
-  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
-}
-__device__ __forceinline__ void unpack_row16(const uint4& r, float2 (&f)[2]) {   // fp32 x 4
-  f[0] = make_float2(__uint_as_float(r.x), __uint_as_float(r.y));
-  f[1] = make_float2(__uint_as_float(r.z), __uint_as_float(r.w));
-}
-__device__ __forceinline__ uint4 pack_row16(const float (&o)[8], __nv_bfloat16) {
-  uint32_t w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __nv_bfloat162 b = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
-    w[i] = *reinterpret_cast<const uint32_t*>(&b);
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
-__device__ __forceinline__ uint4 pack_row16(const float (&o)[4], float) {
-  return make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
-                    __float_as_uint(o[3]));
-}
 }  // namespace
 
-// GM: the group size rounded up to 1, 2, 4 or 8 (register arrays); G <= GM is the real one.
+// GM: the group size rounded up to 2, 4 or 8 (register arrays); G <= GM is the real one.
 template <typename T, int GM>
 __global__ void __launch_bounds__(kHThreads, 2)
 decode_head(const T* __restrict__ q, const T* __restrict__ kn, const T* __restrict__ vn,
@@ -74,7 +42,7 @@ decode_head(const T* __restrict__ q, const T* __restrict__ kn, const T* __restri
   extern __shared__ __align__(128) unsigned char dsm_raw[];
   HeadSmem& S = *reinterpret_cast<HeadSmem*>(dsm_raw);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  HeadWarpSmem& ws = S.w[warp];
+  WarpRing& ws = S.w[warp];
   const int half = lane >> 4, ci = lane & 15;
   const int64_t h = blockIdx.x;
   const int64_t seg = h / Hkv;
@@ -86,15 +54,12 @@ decode_head(const T* __restrict__ q, const T* __restrict__ kn, const T* __restri
     ptx::fence_mbar_init();
   }
   // this lane's slices of the G query rows, scaled into the exp2 domain
-  float2 qf[GM][V2];
-#pragma unroll
-  for (int g = 0; g < GM; ++g) {
-    float2 f[V2];
-    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-    if (g < G) raw = *reinterpret_cast<const uint4*>(q + h * GD + g * D + ci * VE);
-    unpack_row16(raw, f);
-#pragma unroll
-    for (int e = 0; e < V2; ++e) qf[g][e] = ptx::fmul2(f[e], make_float2(c2, c2));
+  using Att = RowTileAttn<T, GM>;
+  Att att;
+  {
+    uint4 qr[GM];
+    load_q<T, GM>(q, h, G, ci, qr);
+    att.begin(qr, c2);
   }
   const int64_t base = cu[seg * (Hkv + 1) + g0], end = cu[seg * (Hkv + 1) + g0 + 1];
   const int len = lens[h];
@@ -134,43 +99,6 @@ decode_head(const T* __restrict__ q, const T* __restrict__ kn, const T* __restri
   int issued = 0;   // items whose copies have been issued (the same in every lane)
   for (; issued < nitems && issued < kHStages; ++issued) issue(issued);
 
-  float mrun[GM], lrun[GM];
-  float2 o[GM][V2];
-#pragma unroll
-  for (int g = 0; g < GM; ++g) {
-    mrun[g] = -INFINITY;
-    lrun[g] = 0.f;
-#pragma unroll
-    for (int e2 = 0; e2 < V2; ++e2) o[g][e2] = make_float2(0.f, 0.f);
-  }
-  // two rows per step (one per half-warp): k, v slices of this lane's row, ok = row exists
-  auto step = [&](const uint4& kr, const uint4& vr, bool ok) {
-    float2 kfv[V2], vfv[V2];
-    unpack_row16(kr, kfv);
-    unpack_row16(vr, vfv);
-#pragma unroll
-    for (int g = 0; g < GM; ++g) {
-      float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int e2 = 0; e2 < V2; ++e2) a = ptx::ffma2(qf[g][e2], kfv[e2], a);
-      float sc = a.x + a.y;
-#pragma unroll
-      for (int off = 8; off > 0; off >>= 1) sc += __shfl_xor_sync(0xFFFFFFFFu, sc, off);
-      if (!ok) sc = -INFINITY;
-      const float so = __shfl_xor_sync(0xFFFFFFFFu, sc, 16);   // the other half's row
-      const float mn = fmaxf(mrun[g], fmaxf(sc, so));
-      const float mu = mn == -INFINITY ? 0.f : mn;
-      const float al = ptx::ex2(mrun[g] - mu);
-      const float p = ptx::ex2(sc - mu), po = ptx::ex2(so - mu);
-      mrun[g] = mn;
-      lrun[g] = lrun[g] * al + p + po;
-#pragma unroll
-      for (int e2 = 0; e2 < V2; ++e2)
-        o[g][e2] = ptx::ffma2(make_float2(p, p), vfv[e2],
-                              ptx::fmul2(o[g][e2], make_float2(al, al)));
-    }
-  };
-
   bool okw = true;
   int consumed = 0;   // items read (their stage may be reused)
   for (int it = 0; it < nitems && okw; ++it) {
@@ -183,19 +111,10 @@ decode_head(const T* __restrict__ q, const T* __restrict__ kn, const T* __restri
     }
     const int64_t rb = f0 + (int64_t)it * kHRows;
     const int nr = (int)((f1 - rb) < kHRows ? f1 - rb : kHRows);
-    {
-      const unsigned char* Ks = ws.st[s][0];
-      const unsigned char* Vs = ws.st[s][1];
-      for (int r = 0; r < nr; r += 2) {
-        const int row = r + half;
-        const bool ok = row < nr;
-        uint4 kr = make_uint4(0u, 0u, 0u, 0u), vr = kr;
-        if (ok) {
-          kr = *reinterpret_cast<const uint4*>(Ks + row * kHRowBytes + ci * 16);
-          vr = *reinterpret_cast<const uint4*>(Vs + row * kHRowBytes + ci * 16);
-        }
-        step(kr, vr, ok);
-      }
+    for (int b = 0; b < nr; b += Att::kRows) {
+      uint4 kr[Att::U], vr[Att::U];
+      load_tile<Att>(ws.st[s][0], ws.st[s][1], b, nr, kr, vr);
+      att.tile(kr, vr, nr - b, ws.red, ws.pbuf);
     }
     __syncwarp();   // every lane is done with stage s
     consumed = it + 1;
@@ -209,21 +128,20 @@ decode_head(const T* __restrict__ q, const T* __restrict__ kn, const T* __restri
   }
   // the new row, in the warp whose range holds it
   if (app && r0 <= nflat && nflat < r1) {
-    uint4 kr = make_uint4(0u, 0u, 0u, 0u), vr = kr;
-    if (half == 0) {
-      kr = *reinterpret_cast<const uint4*>(kn + h * D + ci * VE);
-      vr = *reinterpret_cast<const uint4*>(vn + h * D + ci * VE);
+    uint4 kr[Att::U], vr[Att::U];
+#pragma unroll
+    for (int u = 0; u < Att::U; ++u) {
+      kr[u] = make_uint4(0u, 0u, 0u, 0u);
+      vr[u] = kr[u];
     }
-    step(kr, vr, half == 0);
+    if (half == 0) {
+      kr[0] = *reinterpret_cast<const uint4*>(kn + h * D + ci * VE);
+      vr[0] = *reinterpret_cast<const uint4*>(vn + h * D + ci * VE);
+    }
+    att.tile(kr, vr, 1, ws.red, ws.pbuf);
   }
   // this warp's (max, sum, o): the two half-warps' o hold different rows' terms
-#pragma unroll
-  for (int g = 0; g < GM; ++g)
-#pragma unroll
-    for (int e2 = 0; e2 < V2; ++e2) {
-      o[g][e2].x += __shfl_xor_sync(0xFFFFFFFFu, o[g][e2].x, 16);
-      o[g][e2].y += __shfl_xor_sync(0xFFFFFFFFu, o[g][e2].y, 16);
-    }
+  att.finish();
   __syncthreads();   // every warp is done with its ring: its memory holds the partials now
   float* part = reinterpret_cast<float*>(dsm_raw);   // [warp][g][2 + D]
   const int pstride = 2 + D;
@@ -233,13 +151,13 @@ decode_head(const T* __restrict__ q, const T* __restrict__ kn, const T* __restri
       if (g < G) {
         float* P = part + (warp * GM + g) * pstride;
         if (ci == 0) {
-          P[0] = mrun[g];
-          P[1] = lrun[g];
+          P[0] = att.m[g];
+          P[1] = att.l[g];
         }
 #pragma unroll
         for (int e2 = 0; e2 < V2; ++e2) {
-          P[2 + ci * VE + 2 * e2] = o[g][e2].x;
-          P[2 + ci * VE + 2 * e2 + 1] = o[g][e2].y;
+          P[2 + ci * VE + 2 * e2] = att.o[g][e2].x;
+          P[2 + ci * VE + 2 * e2 + 1] = att.o[g][e2].y;
         }
       }
     }
@@ -310,19 +228,17 @@ cudaError_t launch_decode_head(const Shape& s, const void* q, const void* kn, co
                                cudaStream_t st) {
   const float c2 = scale * 1.4426950408889634f;
   const int G = s.G();
-  const int GM = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
+  const int GM = G <= 2 ? 2 : G <= 4 ? 4 : 8;   // tiles of 32 scores: GM >= 2
 #define KV_HEAD_CASE(T, M)                                                                 \
   return launch_head_t<T, M>(s, q, kn, vn, kf, vf, cu, lens, cap, c2, out, hdr, st)
   if (s.dtype == KV_BF16) {
     switch (GM) {
-      case 1: KV_HEAD_CASE(__nv_bfloat16, 1);
       case 2: KV_HEAD_CASE(__nv_bfloat16, 2);
       case 4: KV_HEAD_CASE(__nv_bfloat16, 4);
       default: KV_HEAD_CASE(__nv_bfloat16, 8);
     }
   }
   switch (GM) {
-    case 1: KV_HEAD_CASE(float, 1);
     case 2: KV_HEAD_CASE(float, 2);
     case 4: KV_HEAD_CASE(float, 4);
     default: KV_HEAD_CASE(float, 8);

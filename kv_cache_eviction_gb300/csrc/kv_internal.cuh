@@ -59,7 +59,8 @@ cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const f
 // ----------------------------- decode --------------------------------------
 struct DecodePlan {
   int64_t max_chunks;   // flat-row chunks (one CTA each) the launch may use
-  size_t off_part, off_map, off_work, off_end;
+  int64_t part_slots;   // partials the part region holds
+  size_t off_part, off_map, off_work, off_tick, off_end;
 };
 DecodePlan decode_plan(const Shape& s);
 cudaError_t launch_decode(const Shape& s, const void* q, const void* kn, const void* vn,
@@ -76,6 +77,20 @@ cudaError_t launch_decode_head(const Shape& s, const void* q, const void* kn, co
                                void* kf, void* vf, const int64_t* cu, int32_t* lens,
                                int64_t cap, float scale, void* out, WsHeader* hdr,
                                cudaStream_t st);
+
+// Decode with the used rows of all heads split evenly across CTAs (decode_split.cu): rows of
+// 256 bytes, G <= 4, at most kDecodeSplitHeadsMax heads and a flat capacity within int32.
+constexpr int64_t kDecodeSplitHeadsMax = 1024;
+// Flat rows per head up to which the default choice is one CTA per head (when the heads fit
+// one wave), and up to which it is the split (when they do not).
+constexpr int64_t kDecodeHeadShortRows = 256;
+constexpr int64_t kDecodeSplitRowsMax = 1536;
+bool decode_split_supported(const Shape& s, int64_t cap);
+cudaError_t launch_decode_split(const Shape& s, const void* q, const void* kn, const void* vn,
+                                void* kf, void* vf, const int64_t* cu, int32_t* lens,
+                                int64_t cap, float scale, void* out, float* part,
+                                int64_t part_slots, uint32_t* tick, WsHeader* hdr,
+                                cudaStream_t st);
 
 int num_sms();
 // Largest dynamic + static shared memory one CTA may opt in to.

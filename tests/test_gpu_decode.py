@@ -25,10 +25,12 @@ from .kvpath import np64, workspace
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["heads", "rows"], autouse=True)
+@pytest.fixture(params=["split", "heads", "rows"], autouse=True)
 def decode_path(request):
-    """Every case through both decode kernels: one CTA per KV head (used for 256-byte rows
-    when heads are short) and the row-balanced split (the rest)."""
+    """Every case through the three decode kernels: the one-launch split of the used rows
+    across CTAs (256-byte rows, G <= 4, short heads), one CTA per KV head (256-byte rows, the
+    other groups) and the row-balanced split (the rest).  A shape a forced kernel does not
+    take goes to the next one that does."""
     old = os.environ.get("KVEVICT_DECODE_PATH")
     os.environ["KVEVICT_DECODE_PATH"] = request.param
     yield request.param
@@ -175,6 +177,17 @@ def test_decode_many_small_heads_per_chunk():
     lens = rng.integers(0, 2, B * L * hkv)
     c = build_cache(B, L, hkv, G, d, lens, reserve=1, dtype="bf16", seed=6)
     check(c, B, L, hkv, G, d, "bf16", append=True)
+
+
+@pytest.mark.parametrize("lens", [[0, 1, 2, 5], [0, 0, 0, 0], [40, 0, 1, 0]])
+def test_decode_fewer_rows_than_ctas(lens):
+    """A cache of a few rows: most CTAs of a one-wave grid get no rows, and a head's pieces
+    skip them when they are merged."""
+    B, L, hkv, G, d = 1, 1, 4, 4, 128
+    c = build_cache(B, L, hkv, G, d, np.array(lens), reserve=2, dtype="bf16", seed=13)
+    check(c, B, L, hkv, G, d, "bf16", append=True)
+    c = build_cache(B, L, hkv, G, d, np.array(lens), reserve=2, dtype="bf16", seed=14)
+    check(c, B, L, hkv, G, d, "bf16", append=False)
 
 
 def test_decode_repeated_steps_match_single_oracle_run():
