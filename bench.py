@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--decode-steps", type=int, default=-1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time the step with eager launches only (no CUDA graph replay)")
     ap.add_argument("--no-decode-large", action="store_true",
                     help="skip the decode-only measurement on the large flat cache")
     return ap.parse_args()
@@ -384,27 +386,28 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
-    def step(ev=None):
+    def step(ev=None, st=None):
+        st = stream if st is None else st
         if ev is not None:
-            ev[0].record(stream)
+            ev[0].record(st)
         kv.kv_score(shape, mode, group, inp["q_win"], inp["k"],
                     inp["v"] if wl.mode != "ada" else None, inp["w_o"], wl.model_dim, scores,
-                    crit, w_s, stream)
+                    crit, w_s, st)
         if ev is not None:
-            ev[1].record(stream)
+            ev[1].record(st)
         kv.kv_allocate(shape, scores, budgets, entropy, wl.alpha[0], wl.alpha[1], lb, hb, w_a,
-                       stream)
+                       st)
         if ev is not None:
-            ev[2].record(stream)
+            ev[2].record(st)
         kv.kv_compact(shape, inp["k"], inp["v"], scores, crit, wl.crit_alpha[0],
                       wl.crit_alpha[1], wl.crit_eps, hb, wl.reserve, kept, cu, lens, kf, vf, cap,
-                      w_c, stream)
+                      w_c, st)
         if ev is not None:
-            ev[3].record(stream)
+            ev[3].record(st)
         kv.flat_decode_attn(shape, dec["q"], dec["k_new"], dec["v_new"], kf, vf, cu, lens, scale,
-                            out, w_d, stream)
+                            out, w_d, st)
         if ev is not None:
-            ev[4].record(stream)
+            ev[4].record(st)
 
     def barrier():
         if world > 1:
@@ -436,24 +439,68 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     barrier()
     launches = kv.kv_kernel_launches() - launches0
-    clk = clocks.stop() if clocks is not None else None
 
     stage_names = ["score", "allocate", "compact", "decode"]
     stage_ms = {nm: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1])
                                     for i in range(args.steps))
                 for j, nm in enumerate(stage_names)}
     if big_inputs:
-        ms_per_step = t_start.elapsed_time(t_end) / args.steps
+        eager_ms = t_start.elapsed_time(t_end) / args.steps
     else:
-        ms_per_step = statistics.mean(evs[i][0].elapsed_time(evs[i][4])
-                                      for i in range(args.steps))
-    t_local = max_over_ranks(ms_per_step, dev)
-    value = aggregate_value(world, B, wl.n, L, t_local)
-
+        eager_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][4])
+                                   for i in range(args.steps))
     for w_ in (w_s, w_a, w_c, w_d):
         code = kv.kv_check_device_status(w_, stream)
         if code:
             raise RuntimeError("device check %d in the timed region" % code)
+
+    # -------------------- the same step captured once as a CUDA graph --------------------
+    # The four calls enqueue every kernel on one stream with no host work between them, so
+    # the step can be captured and replayed: one graph launch per step instead of the
+    # library's host-side launches.  Only with inputs larger than L2 (no flush to interleave).
+    graph_ms, graph_note = None, None
+    if args.no_graph:
+        graph_note = "not run (--no-graph)"
+    elif not big_inputs:
+        graph_note = "not run (inputs fit in L2: the flush between steps is not in the graph)"
+    else:
+        try:
+            gs = torch.cuda.Stream(dev)
+            gs.wait_stream(stream)
+            torch.cuda.synchronize(dev)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=gs):
+                step(st=gs)
+            with torch.cuda.stream(gs):
+                for _ in range(max(args.warmup, 0)):
+                    graph.replay()
+                torch.cuda.synchronize(dev)
+                g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                barrier()
+                torch.cuda.synchronize(dev)
+                g0.record(gs)
+                for _ in range(args.steps):
+                    graph.replay()
+                g1.record(gs)
+                torch.cuda.synchronize(dev)
+            barrier()
+            graph_ms = g0.elapsed_time(g1) / args.steps
+            for w_ in (w_s, w_a, w_c, w_d):
+                code = kv.kv_check_device_status(w_, stream)
+                if code:
+                    raise RuntimeError("device check %d in the graph replays" % code)
+            graph_note = "one CUDA graph per step (captured once), replayed %d times" % args.steps
+            del graph
+        except RuntimeError as e:
+            if "device check" in str(e):
+                raise
+            graph_note = "capture failed: " + str(e).splitlines()[0][:160]
+            graph_ms = None
+            torch.cuda.synchronize(dev)
+    clk = clocks.stop() if clocks is not None else None
+    ms_per_step = graph_ms if graph_ms is not None else eager_ms
+    t_local = max_over_ranks(ms_per_step, dev)
+    value = aggregate_value(world, B, wl.n, L, t_local)
 
     # -------------------- decode alone, L2 flushed before each step --------------------
     hb_rows = int(hb.sum().item())
@@ -481,6 +528,77 @@ def run_ours(args):
         raise RuntimeError("device check in decode")
     peak, peak_kind = read_peaks()
     dec_gbs = sum(dbytes) / (sum(dts) / 1e3) / 1e9
+
+    # -------------------- decode alone, one launch per layer --------------------
+    # The serving loop's own shape: each layer's decode is its own call (one sequence, the
+    # layer's Hkv heads).  The L calls of a step are captured once as a CUDA graph and
+    # replayed (a launch loop in Python would time the host, not the GPU), with the step's
+    # inputs copied into the captured buffers and L2 flushed before each replay.
+    dec_pl = None
+    if B == 1 and L > 1:
+        shape1 = kv.KvShape.from_workload(wl.with_(layers=1))
+        w_d1 = torch.zeros(max(kv.kv_workspace_size(kv.KV_OP_DECODE, shape1), 256),
+                           dtype=torch.uint8, device=dev)
+        kv.kv_compact(shape, inp["k"], inp["v"], scores, crit, wl.crit_alpha[0], wl.crit_alpha[1],
+                      wl.crit_eps, hb, wl.reserve, kept, cu, lens, kf, vf, cap, w_c, stream)
+        # per-layer offset tables on 16-byte boundaries (the ABI's alignment rule)
+        cu_pl = torch.zeros(L, 16, dtype=torch.int64, device=dev)
+        cu_pl[:, :wl.hkv + 1] = cu[0]
+        d0 = W.make_decode_batch(wl, 1, inp["tau"], device=dev, seqs=seqs)
+        xq, xk, xv = d0["q"].clone(), d0["k_new"].clone(), d0["v_new"].clone()
+
+        def layer_calls(st):
+            for l in range(L):
+                kv.flat_decode_attn(shape1, xq[0, l], xk[0, l], xv[0, l], kf, vf, cu_pl[l],
+                                    lens[0, l], scale, out[0, l], w_d1, st,
+                                    flat_capacity_rows=cap)
+
+        gs = torch.cuda.Stream(dev)
+        gs.wait_stream(stream)
+        torch.cuda.synchronize(dev)
+        pl_graph, pl_note = None, None
+        try:
+            pl_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(pl_graph, stream=gs):
+                layer_calls(gs)
+        except RuntimeError as e:
+            pl_graph, pl_note = None, "capture failed: " + str(e).splitlines()[0][:160]
+            torch.cuda.synchronize(dev)
+        lens_pl0 = int(lens.sum().item())
+        pl = {"graph": ([], []), "eager": ([], [])}   # times, bytes
+        with torch.cuda.stream(gs):
+            for s_ in range(nd):
+                d_in = W.make_decode_batch(wl, 1 + s_, inp["tau"], device=dev, seqs=seqs)
+                xq.copy_(d_in["q"])
+                xk.copy_(d_in["k_new"])
+                xv.copy_(d_in["v_new"])
+                flush.zero_()
+                # the last step (or every step without a graph) launches eagerly
+                kind = "graph" if pl_graph is not None and s_ < nd - 1 else "eager"
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(gs)
+                if kind == "graph":
+                    pl_graph.replay()
+                else:
+                    layer_calls(gs)
+                e1.record(gs)
+                torch.cuda.synchronize(dev)
+                rows = lens_pl0 + (s_ + 1) * L * wl.hkv
+                pl[kind][0].append(e0.elapsed_time(e1))
+                pl[kind][1].append(algorithmic_bytes(wl, B, L, hb_rows, rows)["decode"])
+        if kv.kv_check_device_status(w_d1, stream):
+            raise RuntimeError("device check in the per-layer decode")
+        kind = "graph" if pl["graph"][0] else "eager"
+        timed, tbytes = pl[kind]
+        pl_gbs = sum(tbytes) / (sum(timed) / 1e3) / 1e9
+        dec_pl = {"value": pl_gbs, "unit": "GB/s", "frac": pl_gbs / peak, "steps": len(timed),
+                  "ms_per_step": statistics.mean(timed), "launches_per_step": L,
+                  "timing": ("CUDA graph of the %d per-layer calls, replayed" % L)
+                  if kind == "graph" else "eager per-layer calls (graph: %s)" % pl_note,
+                  "eager_us_per_call": statistics.mean(pl["eager"][0]) * 1e3 / L
+                  if pl["eager"][0] else None,
+                  "l2": "flushed before each step of %d per-layer calls" % L}
+        del pl_graph
     dec_large = (decode_large(kv, W, dev, stream, flush, args)
                  if rank == 0 and not args.no_decode_large else None)
 
@@ -604,12 +722,16 @@ def run_ours(args):
                 if big_inputs else "L2 flushed between steps",
                 "step": "kv_score + kv_allocate + kv_compact over all layers, then one "
                         "flat_decode_attn step over all layers",
+                "timing": graph_note if graph_ms is not None else
+                "eager launches (graph: %s)" % graph_note,
             },
+            "eager_ms_per_step": eager_ms,
             "stages_ms": stage_ms,
             "decode_attn": {"value": dec_gbs, "unit": "GB/s", "frac": dec_gbs / peak,
                             "peak": peak, "steps": nd, "ms_per_step": statistics.mean(dts),
                             "bytes_per_step": statistics.mean(dbytes),
                             "l2": "flushed before each step"},
+            "decode_attn_per_layer": dec_pl,
             "decode_attn_large": dict(dec_large, frac=dec_large["value"] / peak)
             if dec_large else None,
             "roofline": roofline,

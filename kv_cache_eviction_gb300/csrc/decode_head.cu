@@ -10,7 +10,8 @@
 // streams its rows through its own ring of bulk copies (3 stages, 16 rows each), the new
 // token's row is read straight from k_new / v_new, the warps' (max, sum, o) are merged in
 // shared memory, and the CTA finally appends the new row and bumps the head's length.  One
-// launch, no partials in global memory.  Rows of 256 bytes (bf16 d = 128, fp32 d = 64):
+// launch (a programmatic dependent of the call before it), no partials in global memory.
+// Rows of 256 bytes (bf16 d = 128, fp32 d = 64):
 // 16 lanes per row, tiles of 32 scores per warp (RowTileAttn).
 #include "decode_rows16.cuh"
 
@@ -53,6 +54,10 @@ decode_head(const T* __restrict__ q, const T* __restrict__ kn, const T* __restri
     for (int s = 0; s < kHStages; ++s) ptx::mbar_init(&ws.full[s], 1);
     ptx::fence_mbar_init();
   }
+  // a programmatic dependent launch: the next call on the stream may start launching, and
+  // nothing of the previous one is read or written before it is done
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   // this lane's slices of the G query rows, scaled into the exp2 domain
   using Att = RowTileAttn<T, GM>;
   Att att;
@@ -215,11 +220,19 @@ static cudaError_t launch_head_t(const Shape& s, const void* q, const void* kn, 
   static const cudaError_t opted = cudaFuncSetAttribute(
       decode_head<T, GM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (opted != cudaSuccess) return opted;
-  decode_head<T, GM><<<(unsigned)s.units(), kHThreads, smem, st>>>(
-      (const T*)q, (const T*)kn, (const T*)vn, (T*)kf, (T*)vf, cu, lens, cap, (T*)out, s.Hkv,
-      s.G(), c2, hdr);
-  count_launches(1);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)s.units());
+  cfg.blockDim = dim3(kHThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_head<T, GM>, (const T*)q, (const T*)kn,
+                                           (const T*)vn, (T*)kf, (T*)vf, cu, lens, cap, (T*)out,
+                                           s.Hkv, s.G(), c2, hdr);
+  if (e == cudaSuccess) count_launches(1);
+  return e;
 }
 
 cudaError_t launch_decode_head(const Shape& s, const void* q, const void* kn, const void* vn,

@@ -54,6 +54,15 @@ __device__ __forceinline__ uint4 pack_row16(const float (&o)[4], float) {
                     __float_as_uint(o[3]));
 }
 
+// Launch attribute of a programmatic dependent launch: the kernel may start while the one
+// before it on the stream finishes, and waits (griddepcontrol.wait) before touching memory.
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a{};
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 // Slice ci of the query rows g < G of KV head h (zeros for g >= G).
 template <typename T, int GM>
 __device__ __forceinline__ void load_q(const T* __restrict__ q, int64_t h, int G, int ci,

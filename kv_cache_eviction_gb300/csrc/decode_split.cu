@@ -16,6 +16,7 @@
 //      an eighth each.  A warp streams the flat rows of each head piece in its eighth
 //      through its own ring of bulk copies, in tiles of 2U rows, and reads the new row from
 //      k_new / v_new (appending it to the flat buffer);
+//   (a call with few rows uses only as many CTAs as give each kSplitMinRows rows);
 //   3. a head held by one warp is written out by it; the pieces of a head split between
 //      warps are merged in shared memory; a head that crosses CTA boundaries leaves one
 //      partial per CTA in global memory, and the last CTA to finish it (a per-head ticket)
@@ -34,6 +35,10 @@ constexpr int kSThreads = kSWarps * 32;
 constexpr int kSPer = (int)(kDecodeSplitHeadsMax / kSThreads);   // heads per thread, step 1
 static_assert(kSPer * kSThreads == kDecodeSplitHeadsMax, "scan covers every head");
 constexpr int kSCand = kSWarps + 1;   // heads a CTA may have to merge
+// Used rows per CTA at least (8 warps x 48 rows in flight): a small call, such as one
+// layer's heads, runs on as few CTAs as that allows instead of merging every head from
+// partials of a dozen CTAs.
+constexpr int64_t kSplitMinRows = 384;
 
 struct SplitSmem {
   WarpRing ring[kSWarps];   // after the stream: the warps' partials, slots 2k and 2k + 1
@@ -177,6 +182,10 @@ decode_split(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
     for (int s = 0; s < kStages; ++s) ptx::mbar_init(&ws.full[s], 1);
     ptx::fence_mbar_init();
   }
+  // a programmatic dependent launch: the next call on the stream may start launching, and
+  // nothing of the previous one is read or written before it is done
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
 
   // ---- 1. used rows of every head and their prefix (all loads first: nothing below may
   // be ordered before them)
@@ -260,7 +269,10 @@ decode_split(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
 
   // ---- 2. this CTA's rows, an eighth per warp
   const int64_t Tu = S.P[H];   // used rows of all heads
-  const int64_t b0 = cta_first(c, Tu, N), b1 = cta_first(c + 1, Tu, N);
+  const int64_t ne = (Tu + kSplitMinRows - 1) / kSplitMinRows;
+  const int Ne = (int)(ne < 1 ? 1 : ne > N ? N : ne);   // CTAs that take rows
+  if (c >= Ne) return;
+  const int64_t b0 = cta_first(c, Tu, Ne), b1 = cta_first(c + 1, Tu, Ne);
   const int64_t span = b1 - b0;
   const int64_t xs = b0 + span * warp / kSWarps, xe = b0 + span * (warp + 1) / kSWarps;
 
@@ -498,11 +510,11 @@ decode_split(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
     int won = 0;
     if (ic >= 0) {
       const int h = S.cand[ic];
-      const int64_t ca = cta_of(S.P[h], Tu, N), cb = cta_of(S.P[h + 1] - 1, Tu, N);
+      const int64_t ca = cta_of(S.P[h], Tu, Ne), cb = cta_of(S.P[h + 1] - 1, Tu, Ne);
       uint32_t npc = (uint32_t)(cb - ca + 1);   // the head's CTAs with rows
-      if (Tu < N) {
+      if (Tu < Ne) {
         npc = 0;
-        for (int64_t cc = ca; cc <= cb; ++cc) npc += cta_first(cc, Tu, N) < cta_first(cc + 1, Tu, N);
+        for (int64_t cc = ca; cc <= cb; ++cc) npc += cta_first(cc, Tu, Ne) < cta_first(cc + 1, Tu, Ne);
       }
       const uint32_t old = atomicAdd(&tick[1 + h], 1u);
       if (old + 1u == npc) {
@@ -522,13 +534,13 @@ decode_split(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
     const int g = sl0 / NSL, sl = sl0 - g * NSL;
     const int off = kPartHead + g * D + sl * VE;
     const int h = S.cand[ic];
-    const int64_t ca = cta_of(S.P[h], Tu, N), cb = cta_of(S.P[h + 1] - 1, Tu, N);
+    const int64_t ca = cta_of(S.P[h], Tu, Ne), cb = cta_of(S.P[h + 1] - 1, Tu, Ne);
     float M, L, acc[VE];
     merge_slice<true, 8, VE>(
         (int)(cb - ca + 1),
         [&](int i) -> const float* {
           const int64_t cc = ca + i;
-          if (!(cta_first(cc, Tu, N) < cta_first(cc + 1, Tu, N))) return nullptr;
+          if (!(cta_first(cc, Tu, Ne) < cta_first(cc + 1, Tu, Ne))) return nullptr;
           return part + (cc == ca ? 2 * cc + 1 : 2 * cc) * pstride;
         },
         g, off, M, L, acc);
@@ -564,11 +576,19 @@ static cudaError_t launch_split_t(const Shape& s, const void* q, const void* kn,
   int64_t grid = (int64_t)per_sm * num_sms();
   if (2 * grid > part_slots) grid = part_slots / 2;   // two partial slots per CTA
   if (grid < 1) return cudaErrorInvalidConfiguration;
-  decode_split<T, GM><<<(unsigned)grid, kSThreads, smem, st>>>(
-      (const T*)q, (const T*)kn, (const T*)vn, (T*)kf, (T*)vf, cu, lens, cap, (T*)out,
-      (int)s.units(), s.Hkv, s.G(), c2, part, tick, hdr);
-  count_launches(1);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kSThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split<T, GM>, (const T*)q, (const T*)kn,
+                                           (const T*)vn, (T*)kf, (T*)vf, cu, lens, cap, (T*)out,
+                                           (int)s.units(), s.Hkv, s.G(), c2, part, tick, hdr);
+  if (e == cudaSuccess) count_launches(1);
+  return e;
 }
 
 cudaError_t launch_decode_split(const Shape& s, const void* q, const void* kn, const void* vn,

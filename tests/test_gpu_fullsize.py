@@ -2,7 +2,7 @@
 
 The three multi-layer workloads run at their full sizes through the same calls bench.py
 times (kv_score, kv_allocate and kv_compact over every (sequence, layer) of the batch, then
-one flat_decode_attn step over all of them).  The oracle then checks a few (sequence,
+one flat_decode_attn step over all of them).  The oracle then checks four (sequence,
 layer) units, always including the first and the last:
 
 - scores within 1e-4 relative of the oracle's fp64 scores of that unit (CriticalKV: the
@@ -38,10 +38,15 @@ def built():
     kv.lib()
 
 
-def samples(B, L, seed):
+def samples(B, L, seed, n=4):
+    """n distinct (sequence, layer) units: the first, the last, and seeded interior layers."""
     rng = np.random.default_rng(seed)
-    pts = [(0, 0), (B - 1, L - 1), (int(rng.integers(B)), int(rng.integers(1, L - 1)))]
-    return list(dict.fromkeys(pts))
+    pts = [(0, 0), (B - 1, L - 1)]
+    while len(pts) < n:
+        p = (int(rng.integers(B)), int(rng.integers(1, L - 1)))
+        if p not in pts:
+            pts.append(p)
+    return pts
 
 
 @pytest.mark.parametrize("name", ["llama8b_32k_b4", "mistral7b_128k_lava",
