@@ -52,6 +52,9 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--decode-steps", type=int, default=-1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-batches", default="",
+                    help="comma-separated batch sizes: decode alone over that many replicas of "
+                         "the evicted sequence's flat cache (e.g. 1,8,32)")
     ap.add_argument("--no-graph", action="store_true",
                     help="time the step with eager launches only (no CUDA graph replay)")
     ap.add_argument("--no-decode-large", action="store_true",
@@ -294,6 +297,55 @@ def algorithmic_bytes(wl, B, L, head_budget_total_rows, decode_rows):
         compact += s_bytes
     decode = 2 * decode_rows * row + 2 * B * L * wl.hq * wl.d * e + 4 * B * L * wl.hkv * wl.d * e
     return {"score": score, "allocate": allocate, "compact": compact, "decode": decode}
+
+
+def decode_batches(kv, W, wl, dev, stream, flush, kf, vf, cu, lens, cap, batches, steps=3):
+    """flat_decode_attn alone over b copies of one evicted sequence's flat cache, for each b in
+    `batches`.  The copies sit at distinct addresses of one flat buffer (offsets shifted by
+    the sequence's capacity), with fresh q / k_new / v_new per sequence; L2 flushed before
+    each step.  Replicas stand in for b independently evicted sequences."""
+    import torch
+    res = []
+    L, hkv = wl.layers, wl.hkv
+    for b in batches:
+        shape_b = kv.KvShape.from_workload(wl.with_(batch=b))
+        kf_b = torch.empty(b * cap, wl.d, dtype=kf.dtype, device=dev)
+        vf_b = torch.empty_like(kf_b)
+        for i in range(b):
+            kf_b[i * cap:(i + 1) * cap].copy_(kf[:cap])
+            vf_b[i * cap:(i + 1) * cap].copy_(vf[:cap])
+        cu_b = torch.cat([cu[:1] + i * cap for i in range(b)]).contiguous()
+        lens_b = torch.cat([lens[:1]] * b).contiguous()
+        g = torch.Generator(device=dev).manual_seed(0xC0DE + b)
+        q = torch.randn(b, L, wl.hq, wl.d, device=dev, generator=g).to(kf.dtype)
+        kn = torch.randn(b, L, hkv, wl.d, device=dev, generator=g).to(kf.dtype)
+        vn = torch.randn(b, L, hkv, wl.d, device=dev, generator=g).to(kf.dtype)
+        out = torch.empty_like(q)
+        wsb = torch.zeros(max(kv.kv_workspace_size(kv.KV_OP_DECODE, shape_b), 256),
+                          dtype=torch.uint8, device=dev)
+        scale = 1.0 / math.sqrt(wl.d)
+        dts, byts = [], []
+        for i in range(steps + 1):
+            rows = int(lens_b.sum().item()) + b * L * hkv     # after this step's append
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            kv.flat_decode_attn(shape_b, q, kn, vn, kf_b, vf_b, cu_b, lens_b, scale, out, wsb,
+                                stream)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 1:
+                dts.append(e0.elapsed_time(e1))
+                byts.append(algorithmic_bytes(wl, b, L, 0, rows)["decode"])
+        if kv.kv_check_device_status(wsb, stream):
+            raise RuntimeError("device check in the batch-%d decode" % b)
+        gbs = sum(byts) / (sum(dts) / 1e3) / 1e9
+        res.append({"batch": b, "value": gbs, "unit": "GB/s", "steps": steps,
+                    "ms_per_step": statistics.mean(dts), "bytes_per_step": statistics.mean(byts),
+                    "cache": "%d replicas of sequence 0's flat cache at distinct addresses" % b})
+        del kf_b, vf_b, q, kn, vn, out, wsb
+        torch.cuda.empty_cache()
+    return res
 
 
 def decode_large(kv, W, dev, stream, flush, args):
@@ -599,6 +651,16 @@ def run_ours(args):
                   if pl["eager"][0] else None,
                   "l2": "flushed before each step of %d per-layer calls" % L}
         del pl_graph
+    dec_batches = None
+    if args.decode_batches and rank == 0:
+        kv.kv_compact(shape, inp["k"], inp["v"], scores, crit, wl.crit_alpha[0],
+                      wl.crit_alpha[1], wl.crit_eps, hb, wl.reserve, kept, cu, lens, kf, vf, cap,
+                      w_c, stream)
+        dec_batches = decode_batches(kv, W, wl, dev, stream, flush, kf, vf, cu, lens, cap,
+                                     [int(x) for x in args.decode_batches.split(",") if x])
+        peak_ = read_peaks()[0]
+        for r in dec_batches:
+            r["frac"] = r["value"] / peak_
     dec_large = (decode_large(kv, W, dev, stream, flush, args)
                  if rank == 0 and not args.no_decode_large else None)
 
@@ -732,6 +794,7 @@ def run_ours(args):
                             "bytes_per_step": statistics.mean(dbytes),
                             "l2": "flushed before each step"},
             "decode_attn_per_layer": dec_pl,
+            "decode_attn_batches": dec_batches,
             "decode_attn_large": dict(dec_large, frac=dec_large["value"] / peak)
             if dec_large else None,
             "roofline": roofline,

@@ -717,14 +717,18 @@ cudaError_t launch_decode(const Shape& s, const void* q, const void* kn, const v
   const int forced = decode_path_forced();
   // Measured on GB300 (L2 flushed, log-normal head lengths): one CTA per head wins while
   // the heads fit one wave and are short (every kernel is latency-bound there); the
-  // one-launch split wins from there to about 1.5K rows per head, and at any length when
-  // the heads are few; many long heads stream best through the row-balanced split here.
+  // one-launch split wins from there to about 1.5K rows per head, and to about 8K when the
+  // heads are few; heads longer still stream best through the row-balanced split, except
+  // in calls of a few heads (one layer at a time), where the split spreads them over SMs.
   const int64_t rows_per_head = cap / H;
   const bool few_heads = H <= 2 * (int64_t)num_sms();
+  const bool one_layer = H <= (int64_t)num_sms() / 4;
   if (forced == 0) {
     if (few_heads && rows_per_head <= kDecodeHeadShortRows && decode_head_supported(s, cap))
       return launch_decode_head(s, q, kn, vn, kf, vf, cu, lens, cap, scale, out, hdr, st);
-    if ((few_heads || rows_per_head <= kDecodeSplitRowsMax) && decode_split_supported(s, cap))
+    if ((rows_per_head <= kDecodeSplitRowsMax ||
+         (few_heads && rows_per_head <= kDecodeSplitFewRowsMax) || one_layer) &&
+        decode_split_supported(s, cap))
       return launch_decode_split(s, q, kn, vn, kf, vf, cu, lens, cap, scale, out,
                                  reinterpret_cast<float*>(ws + p.off_part), p.part_slots,
                                  reinterpret_cast<uint32_t*>(ws + p.off_tick), hdr, st);

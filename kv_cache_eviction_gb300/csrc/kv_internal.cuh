@@ -85,6 +85,7 @@ constexpr int64_t kDecodeSplitHeadsMax = 1024;
 // one wave), and up to which it is the split (when they do not).
 constexpr int64_t kDecodeHeadShortRows = 256;
 constexpr int64_t kDecodeSplitRowsMax = 1536;
+constexpr int64_t kDecodeSplitFewRowsMax = 8192;   // when the heads fit one wave
 bool decode_split_supported(const Shape& s, int64_t cap);
 cudaError_t launch_decode_split(const Shape& s, const void* q, const void* kn, const void* vn,
                                 void* kf, void* vf, const int64_t* cu, int32_t* lens,
