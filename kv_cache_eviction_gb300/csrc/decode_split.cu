@@ -21,8 +21,9 @@
 //      warps are merged in shared memory; a head that crosses CTA boundaries leaves one
 //      partial per CTA in global memory, and the last CTA to finish it (a per-head ticket)
 //      merges them.
-// The lengths are bumped by the last CTA to finish step 1 (every CTA has read them by
-// then).  The tickets return to zero at the end of every launch, so the workspace only has
+// CTA boundaries inside short heads move to the nearer head end, so only heads longer than
+// kSplitSnapRows ever cross CTAs.  The lengths are bumped by the last CTA to count itself
+// past step 1 (every CTA has read them by then), as it leaves.  The tickets return to zero at the end of every launch, so the workspace only has
 // to start zeroed.  No CTA waits for another: the grid needs no co-residency.
 #include "decode_rows16.cuh"
 
@@ -39,6 +40,10 @@ constexpr int kSCand = kSWarps + 1;   // heads a CTA may have to merge
 // layer's heads, runs on as few CTAs as that allows instead of merging every head from
 // partials of a dozen CTAs.
 constexpr int64_t kSplitMinRows = 384;
+// A CTA boundary that falls inside a head of at most this many used rows moves to the
+// nearer end of that head: short heads are never split between CTAs (no partials in global
+// memory, no ticket), and a CTA's range grows or shrinks by at most half such a head.
+constexpr int64_t kSplitSnapRows = 512;
 
 struct SplitSmem {
   WarpRing ring[kSWarps];   // after the stream: the warps' partials, slots 2k and 2k + 1
@@ -51,7 +56,6 @@ struct SplitSmem {
   uint32_t cslots[kSCand];                   // each) and counts, and whether they cross
   int32_t cn[kSCand], ccross[kSCand];        // the CTA's ends
   int32_t ncand, win[2];
-  int flag;
 };
 static_assert(sizeof(SplitSmem) <= 227 * 1024, "one CTA per SM");
 
@@ -255,24 +259,40 @@ decode_split(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
   if (tid == kSThreads - 1) S.P[H] = run;
   __syncthreads();
   // the last CTA past this point writes the new lengths: every CTA has read lens by then
-  if (tid == 0) {
-    __threadfence();
-    const uint32_t old = atomicAdd(&tick[0], 1u);
-    const bool last = old == (uint32_t)(N - 1);
-    if (last) atomicExch(&tick[0], 0u);
-    S.flag = last ? 1 : 0;
-  }
-  __syncthreads();
-  if (S.flag)
-    for (int h = tid; h < H; h += kSThreads)
+  // Every CTA has read lens once it is past this point; the last CTA to count itself here
+  // writes the new lengths when it leaves (warp 0 waits for the count only then, so the
+  // atomic's round trip overlaps the stream).
+  uint32_t scanned = 0;
+  if (tid == 0) scanned = atomicAdd(&tick[0], 1u);
+  auto leave = [&]() {
+    if (warp != 0) return;
+    const uint32_t old = __shfl_sync(0xFFFFFFFFu, scanned, 0);
+    if (old != (uint32_t)(N - 1)) return;
+    for (int h = lane; h < H; h += 32)
       if (S.app[h]) lens[h] = (int32_t)(S.P[h + 1] - S.P[h]);
+    if (lane == 0) atomicExch(&tick[0], 0u);
+  };
 
   // ---- 2. this CTA's rows, an eighth per warp
   const int64_t Tu = S.P[H];   // used rows of all heads
   const int64_t ne = (Tu + kSplitMinRows - 1) / kSplitMinRows;
   const int Ne = (int)(ne < 1 ? 1 : ne > N ? N : ne);   // CTAs that take rows
-  if (c >= Ne) return;
-  const int64_t b0 = cta_first(c, Tu, Ne), b1 = cta_first(c + 1, Tu, Ne);
+  if (c >= Ne) {
+    leave();
+    return;
+  }
+  // CTA k's first row: T k / Ne, moved to the nearer end of a short head it falls in.  Rows
+  // of a head longer than kSplitSnapRows are split at the unmoved boundaries, so cta_of and
+  // cta_first locate the pieces of such a head exactly.
+  auto bound = [&](int64_t k) -> int64_t {
+    const int64_t x = cta_first(k, Tu, Ne);
+    if (x <= 0 || x >= Tu) return x;
+    const int h = head_of(S.P, H, x);
+    const int64_t lo = S.P[h], hi = S.P[h + 1];
+    if (hi - lo > kSplitSnapRows) return x;
+    return x - lo <= hi - x ? lo : hi;
+  };
+  const int64_t b0 = bound(c), b1 = bound(c + 1);
   const int64_t span = b1 - b0;
   const int64_t xs = b0 + span * warp / kSWarps, xe = b0 + span * (warp + 1) / kSWarps;
 
@@ -437,7 +457,10 @@ decode_split(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
   };
   if (hasA) put(wp + (2 * warp) * pstride, am, al, ao);
   if (hasB) put(wp + (2 * warp + 1) * pstride, att.m, att.l, att.o);
-  if (span <= 0) return;   // no rows here (uniform in the CTA)
+  if (span <= 0) {   // no rows here (uniform in the CTA)
+    leave();
+    return;
+  }
   auto warp_first = [&](int k) { return b0 + span * k / kSWarps; };
   if (tid == 0) {
     // heads split between warps, or crossing the CTA's ends: each holds the first row of a
@@ -500,7 +523,10 @@ decode_split(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
   // heads crossing the CTA's ends (its first and last candidates): this CTA's partials are
   // out, and the last of each head's CTAs merges them
   const int nx = ncand == 0 ? 0 : (S.ccross[0] + (ncand > 1 ? S.ccross[ncand - 1] : 0));
-  if (nx == 0) return;   // uniform in the CTA
+  if (nx == 0) {   // uniform in the CTA
+    leave();
+    return;
+  }
   __threadfence();
   __syncthreads();
   if (tid < 2) {
@@ -525,7 +551,10 @@ decode_split(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
     S.win[tid] = won ? ic : -1;
   }
   __syncthreads();
-  if (S.win[0] < 0 && S.win[1] < 0) return;
+  if (S.win[0] < 0 && S.win[1] < 0) {
+    leave();
+    return;
+  }
   __threadfence();
   for (int idx = tid; idx < 2 * nsl; idx += kSThreads) {
     const int wi = idx / nsl, sl0 = idx - wi * nsl;
@@ -546,6 +575,7 @@ decode_split(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
         g, off, M, L, acc);
     store_out<T, VE>(out + ((int64_t)h * G + g) * D + sl * VE, acc, L);
   }
+  leave();
 }
 
 bool decode_split_supported(const Shape& s, int64_t cap) {
