@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--decode-batches", default="",
                     help="comma-separated batch sizes: decode alone over that many replicas of "
                          "the evicted sequence's flat cache (e.g. 1,8,32)")
+    ap.add_argument("--no-decode-per-layer", action="store_true",
+                    help="skip the decode-only measurement with one call per layer")
     ap.add_argument("--no-graph", action="store_true",
                     help="time the step with eager launches only (no CUDA graph replay)")
     ap.add_argument("--no-decode-large", action="store_true",
@@ -620,7 +622,7 @@ def run_ours(args):
     # replayed (a launch loop in Python would time the host, not the GPU), with the step's
     # inputs copied into the captured buffers and L2 flushed before each replay.
     dec_pl = None
-    if B == 1 and L > 1:
+    if B == 1 and L > 1 and not args.no_decode_per_layer:
         shape1 = kv.KvShape.from_workload(wl.with_(layers=1))
         w_d1 = torch.zeros(max(kv.kv_workspace_size(kv.KV_OP_DECODE, shape1), 256),
                            dtype=torch.uint8, device=dev)
