@@ -571,7 +571,7 @@ def run_ours(args):
     # capture works.
     d0 = W.make_decode_batch(wl, 1, inp["tau"], device=dev, seqs=seqs)
     xq, xk, xv = d0["q"].clone(), d0["k_new"].clone(), d0["v_new"].clone()
-    dec = {"eager": ([], []), "graph": ([], [])}   # times, bytes
+    dec_t = {"eager": ([], []), "graph": ([], [])}   # times, bytes
     dec_graph, dec_note = None, "not run (--no-graph)" if args.no_graph else None
     gsd = torch.cuda.Stream(dev)
     if not args.no_graph and nd >= 2:
@@ -604,16 +604,16 @@ def run_ours(args):
             e1.record(st_)
         torch.cuda.synchronize(dev)
         rows = lens0 + (s_ + 1) * B * L * wl.hkv
-        dec[kind][0].append(e0.elapsed_time(e1))
-        dec[kind][1].append(algorithmic_bytes(wl, B, L, hb_rows, rows)["decode"])
+        dec_t[kind][0].append(e0.elapsed_time(e1))
+        dec_t[kind][1].append(algorithmic_bytes(wl, B, L, hb_rows, rows)["decode"])
     if kv.kv_check_device_status(w_d, stream):
         raise RuntimeError("device check in decode")
     del dec_graph
     peak, peak_kind = read_peaks()
-    dec_kind = "graph" if dec["graph"][0] else "eager"
-    dts, dbytes = dec[dec_kind]
-    dec_eager_gbs = (sum(dec["eager"][1]) / (sum(dec["eager"][0]) / 1e3) / 1e9
-                     if dec["eager"][0] else None)
+    dec_kind = "graph" if dec_t["graph"][0] else "eager"
+    dts, dbytes = dec_t[dec_kind]
+    dec_eager_gbs = (sum(dec_t["eager"][1]) / (sum(dec_t["eager"][0]) / 1e3) / 1e9
+                     if dec_t["eager"][0] else None)
     dec_gbs = sum(dbytes) / (sum(dts) / 1e3) / 1e9
 
     # -------------------- decode alone, one launch per layer --------------------
@@ -831,8 +831,8 @@ def run_ours(args):
                             if dec_kind == "graph" else
                             "eager launches (graph: %s)" % (dec_note or "not run"),
                             "eager_value": dec_eager_gbs,
-                            "eager_ms_per_step": statistics.mean(dec["eager"][0])
-                            if dec["eager"][0] else None,
+                            "eager_ms_per_step": statistics.mean(dec_t["eager"][0])
+                            if dec_t["eager"][0] else None,
                             "l2": "flushed before each step"},
             "decode_attn_per_layer": dec_pl,
             "decode_attn_batches": dec_batches,
