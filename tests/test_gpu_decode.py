@@ -145,6 +145,11 @@ CASES = [
     ("bf16", 8, 2, 3),      # 1 slice per row
     ("f32", 128, 2, 2),     # 32 slices per row
     ("bf16", 96, 4, 2),     # 12 slices: lanes 12..15 of each row idle
+    # 256-byte rows with small groups: tiles of 16 rows (G padded to 2) and a padded G = 3
+    ("bf16", 128, 1, 8),
+    ("bf16", 128, 2, 4),
+    ("f32", 64, 2, 2),
+    ("bf16", 128, 3, 2),
 ]
 
 
