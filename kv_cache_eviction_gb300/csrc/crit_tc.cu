@@ -210,7 +210,8 @@ crit_tc_kernel(const __grid_constant__ CUtensorMap vmap, const __grid_constant__
       float acc0 = 0.f, acc1 = 0.f;
       for (int nt = 0; nt < p.NT; ++nt, ++gt) {
         const int tb = gt & 1;
-        if (!mbar_wait(&tl->tfull[tb], (gt >> 1) & 1) || *abort_flag) { ok = false; break; }
+        const bool landed = mbar_wait(&tl->tfull[tb], (gt >> 1) & 1) && !*abort_flag;
+        if (__any_sync(0xffffffffu, !landed)) { ok = false; break; }   // the whole warp
         tc_fence_after();
         const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + tb * 256 + h * 128;
 #pragma unroll

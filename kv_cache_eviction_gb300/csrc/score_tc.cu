@@ -491,8 +491,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
           const int nv = t + 1 < te ? 1 : t1 - t;
           for (int j = 0; j < nv; ++j, ++g) {
             const int sv = g % kStages;
-            if (!mbar_wait(&tl->fullv[sv], vuse[sv]++ & 1) || *abort_flag) { ok = false; break; }
-            vmax = fmaxf(vmax, vrow_l1_row(smem + kOffK + sv * kTileBytes, vt_));
+            const bool landed = mbar_wait(&tl->fullv[sv], vuse[sv]++ & 1) && !*abort_flag;
+            if (landed) vmax = fmaxf(vmax, vrow_l1_row(smem + kOffK + sv * kTileBytes, vt_));
+            // the whole warp leaves when any lane's wait gave up; otherwise every lane's
+            // reads of the stage are ordered before lane 0 frees it
+            if (__any_sync(0xffffffffu, !landed)) { ok = false; break; }
             __syncwarp();
             if (lane == 0 && atomicAdd(&tl->vcnt[sv], 1u) == (uint32_t)(kVWarps - 1)) {
               tl->vcnt[sv] = 0;
@@ -507,7 +510,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             atomicMax(reinterpret_cast<unsigned int*>(p.vbar) + u, __float_as_uint(wm));
         }
         // pool the item's window sums once the epilogue has written all of them
-        if (!mbar_wait(&tl->afull, np2 & 1) || *abort_flag) { ok = false; break; }
+        const bool filled = mbar_wait(&tl->afull, np2 & 1) && !*abort_flag;
+        if (__any_sync(0xffffffffu, !filled)) { ok = false; break; }   // the whole warp
         ++np2;
         const int sK = t0 * 128, eK = min(te * 128, p.C);
         pool_range<LW>(A, RK, sK, eK, p.C, p.G, p.r, p.group_max, p.inv_w, p.scores + u * p.C,
@@ -536,8 +540,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     const float c2 = p.c2;
     uint32_t g = 0;     // TMEM accumulator counter (K tiles)
     uint32_t np2 = 0;   // P2 items finished (phases of afull / aempty)
+    // ok turns false on a wait that gave up or an abort by another role.  The thread then
+    // raises the CTA's abort flag, stops waiting and skips the rest of each item's tiles,
+    // but keeps to the same sequence of items and named barriers as the other epilogue
+    // threads (leaving the item loop early would strand them at a barrier).
     bool ok = true;
-    for (int64_t i = 0; i < n_items && ok; ++i) {
+    for (int64_t i = 0; i < n_items; ++i) {
       int kind;
       int64_t k;
       item_of(i, m, kind, k);
@@ -546,9 +554,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       if (t0 >= te) continue;
       if (kind == 2) {
         // the window sums of the previous P2 item have been pooled
-        if (!mbar_wait(&tl->aempty, (np2 & 1) ^ 1) || *abort_flag) { ok = false; break; }
+        if (*abort_flag || !mbar_wait(&tl->aempty, (np2 & 1) ^ 1)) {
+          ok = false;
+          *abort_flag = 1;
+        }
         if (tl->pf_unit != u) {     // not prefetched during the previous P1 item: wait now
-          if (et == 0) {
+          if (et == 0 && !*abort_flag) {
             const uint64_t tw = globaltimer();
             while (ld_acquire_u32(&p.ready[u]) < (uint32_t)p.ncomb) {
               if (*abort_flag || globaltimer() - tw > 2000000000ull) {
@@ -560,7 +571,6 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             }
           }
           named_bar(1, kEpiThreads);
-          if (*abort_flag) { ok = false; break; }
           if (et < 128) nlse[et] = -__ldcg(&p.lse[u * 128 + et]);
         }
         named_bar(1, kEpiThreads);
@@ -579,7 +589,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         const int tb = g % kTBuf;
         uint32_t pf_flag = 0;
         if (pf_u >= 0 && lane == 0) pf_flag = ld_relaxed_u32(&p.ready[pf_u]);   // used below
-        if (!mbar_wait(&tl->tfull[tb], (g / kTBuf) & 1) || *abort_flag) { ok = false; break; }
+        if (*abort_flag || !mbar_wait(&tl->tfull[tb], (g / kTBuf) & 1)) {
+          ok = false;
+          *abort_flag = 1;
+          break;   // the item's remaining tiles only: its named barriers still follow
+        }
         tc_fence_after();
         uint32_t ra[32];
         tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + tb * 128 + qc * 32, ra);
@@ -654,7 +668,6 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
           }
         }
       }
-      if (!ok) break;
       if (kind == 1) {
         part_s[qc * 128 + row] = make_float2(m_run, l_run);
         named_bar(1, kEpiThreads);
