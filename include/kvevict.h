@@ -190,6 +190,8 @@ KV_API kv_status kv_compact(const kv_shape* shape, const void* k, const void* v,
  *   (an append that would land there sets the device error word instead)
  * out          [B][L][Hq][d] dtype
  * `shape.n` bounds the head length (lens <= n + reserve); `w` and `pool` are unused.
+ * The workspace holds counters that each call uses and leaves at zero (the reason for
+ * zeroing a workspace once before its first use).
  */
 KV_API kv_status flat_decode_attn(const kv_shape* shape, const void* q,
                            const void* k_new, const void* v_new,
