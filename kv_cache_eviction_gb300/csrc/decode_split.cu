@@ -23,8 +23,10 @@
 //      merges them.
 // CTA boundaries inside short heads move to the nearer head end, so only heads longer than
 // kSplitSnapRows ever cross CTAs.  The lengths are bumped by the last CTA to count itself
-// past step 1 (every CTA has read them by then), as it leaves.  The tickets return to zero at the end of every launch, so the workspace only has
-// to start zeroed.  No CTA waits for another: the grid needs no co-residency.
+// past step 1 (every CTA has read them by then), as it leaves.  The counters and tickets
+// return to zero at the end of every launch, so the workspace only has to start zeroed.
+// No CTA waits for another: the grid needs no co-residency.  The launch is a programmatic
+// dependent of the call before it on the stream (nothing is touched before that one ends).
 #include "decode_rows16.cuh"
 
 namespace kv {
@@ -540,7 +542,8 @@ decode_split(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
       uint32_t npc = (uint32_t)(cb - ca + 1);   // the head's CTAs with rows
       if (Tu < Ne) {
         npc = 0;
-        for (int64_t cc = ca; cc <= cb; ++cc) npc += cta_first(cc, Tu, Ne) < cta_first(cc + 1, Tu, Ne);
+        for (int64_t cc = ca; cc <= cb; ++cc)
+          npc += cta_first(cc, Tu, Ne) < cta_first(cc + 1, Tu, Ne);
       }
       const uint32_t old = atomicAdd(&tick[1 + h], 1u);
       if (old + 1u == npc) {
