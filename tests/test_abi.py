@@ -112,6 +112,26 @@ def test_invalid_parameters_rejected_on_host(L):
                         p, 1 << 20, p, 1 << 30, None) == 1
 
 
+def test_short_workspace_rejected_on_host(L):
+    """A workspace one byte short of kv_workspace_size is refused before anything is
+    enqueued (the decode plan includes the split kernel's counters and tickets)."""
+    s = shape()
+    p = ctypes.c_void_p(0x1000)
+    n = [kv.kv_workspace_size(op, s) for op in range(4)]
+    assert L.kv_score(ctypes.byref(s), 0, 0, p, p, None, None, 0, p, None, p, n[0] - 1,
+                      None) == kv.KV_ERR_WORKSPACE
+    assert L.kv_allocate(ctypes.byref(s), p, p, 0, 1, 5, p, p, p, n[1] - 1,
+                         None) == kv.KV_ERR_WORKSPACE
+    # (the compaction size covers CriticalKV's stage-1 flags: pass a norm array)
+    assert L.kv_compact(ctypes.byref(s), p, p, p, p, 1, 2, 0.0, p, 0, p, p, p, p, p, 1 << 20,
+                        p, n[2] - 1, None) == kv.KV_ERR_WORKSPACE
+    assert L.flat_decode_attn(ctypes.byref(s), p, None, None, p, p, p, p, 1 << 20, 0.1, p, p,
+                              n[3] - 1, None) == kv.KV_ERR_WORKSPACE
+    # the decode plan grows with the heads: one ticket per KV head at least
+    big = shape(batch=4 * s.batch)
+    assert kv.kv_workspace_size(3, big) >= n[3] + 3 * s.batch * s.layers * s.hkv * 4
+
+
 def test_empty_batch_is_a_no_op(L):
     s = shape(batch=0)
     p = ctypes.c_void_p(0x1000)
