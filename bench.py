@@ -55,6 +55,13 @@ def parse_args():
     ap.add_argument("--decode-batches", default="",
                     help="comma-separated batch sizes: decode alone over that many replicas of "
                          "the evicted sequence's flat cache (e.g. 1,8,32)")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="decode alone on a synthetic flat cache shaped like the workload's "
+                         "(log-normal head lengths around its mean budget per head); no "
+                         "eviction inputs are built")
+    ap.add_argument("--decode-sigma", type=float, default=0.4,
+                    help="--decode-only: sigma of the log-normal head lengths (0.4 matches the "
+                         "spread of the 128K LAVa allocation: p90 1.5x, max 2.8x the mean)")
     ap.add_argument("--no-decode-per-layer", action="store_true",
                     help="skip the decode-only measurement with one call per layer")
     ap.add_argument("--no-graph", action="store_true",
@@ -386,6 +393,60 @@ def decode_large(kv, W, dev, stream, flush, args):
                      "(log-normal, sigma 0.7), 256 reserve rows; L2 flushed before each step"}
 
 
+def run_decode_only(args, kv, W, dev):
+    """flat_decode_attn alone, L2 flushed before each step, on a flat cache of the workload's
+    shape whose head lengths are log-normal (--decode-sigma) around the workload's mean rows
+    per head: the decode of the eviction pass's output without its inputs on the device."""
+    import torch
+    wl = W.WORKLOADS[args.workload]
+    if args.layers > 0:
+        wl = wl.with_(layers=args.layers)
+    if wl.budget_kind == "total":
+        mean = wl.total_per_head_layer
+    else:
+        mean = wl.layer_budget_value() // wl.hkv
+    reserve = max(wl.reserve, 8)
+    fc = W.make_flat_cache(wl, mean_len=mean, sigma=args.decode_sigma, reserve=reserve,
+                           seed=0xDEC1, device=dev)
+    shape = kv.KvShape.from_workload(wl)
+    wsd = torch.zeros(max(kv.kv_workspace_size(kv.KV_OP_DECODE, shape), 256), dtype=torch.uint8,
+                      device=dev)
+    out = torch.empty_like(fc["q"])
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    scale = 1.0 / math.sqrt(wl.d)
+    B, L = wl.batch, wl.layers
+    steps = max(1, min(args.decode_steps if args.decode_steps > 0 else 32, reserve - 1))
+    dts, byts = [], []
+    for i in range(max(args.warmup, 0) + steps):
+        rows = int(fc["lens"].sum().item()) + B * L * wl.hkv
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        kv.flat_decode_attn(shape, fc["q"], fc["k_new"], fc["v_new"], fc["k_flat"], fc["v_flat"],
+                            fc["cu"], fc["lens"], scale, out, wsd, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= max(args.warmup, 0):
+            dts.append(e0.elapsed_time(e1))
+            byts.append(algorithmic_bytes(wl, B, L, 0, rows)["decode"])
+    if kv.kv_check_device_status(wsd, stream):
+        raise RuntimeError("device check in the decode-only run")
+    peak, peak_kind = read_peaks()
+    gbs = sum(byts) / (sum(dts) / 1e3) / 1e9
+    print(json.dumps({
+        "metric": "flat varlen decode attn HBM GB/s", "value": gbs, "unit": "GB/s",
+        "frac": gbs / peak, "peak": peak, "peak_kind": peak_kind, "n_gpus": 1, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": statistics.mean(dts),
+        "bytes_per_step": statistics.mean(byts), "higher_is_better": True,
+        "data": "synthetic flat cache (log-normal head lengths, sigma %g, around %d rows, "
+                "longest %d)" % (args.decode_sigma, mean, int(fc["lens"].max().item())),
+        "config": {"workload": wl.name, "batch": B, "layers": L, "hkv": wl.hkv, "hq": wl.hq,
+                   "d": wl.d, "reserve": reserve, "l2": "flushed before each step"}}),
+          flush=True)
+    return 0
+
+
 def run_ours(args):
     import torch
     import kv_cache_eviction_gb300 as kv
@@ -398,6 +459,11 @@ def run_ours(args):
         return 1
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.decode_only:
+        if rank != 0:
+            return 0
+        __graft_entry__.build()
+        return run_decode_only(args, kv, W, dev)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
