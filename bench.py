@@ -288,7 +288,10 @@ class ClockSampler:
 
 
 def algorithmic_bytes(wl, B, L, head_budget_total_rows, decode_rows):
-    """Bytes each stage must move (see the roofline section of the design notes)."""
+    """Bytes each stage must move: K once (and V once for LAVa and CriticalKV, plus W_O for
+    CriticalKV), the window queries and the scores written (score); the scores read
+    (allocate); the scores read, the kept K/V rows read and written and their indices
+    (compact); every used K/V row, q, out, k_new and v_new (decode)."""
     e = wl.elem_bytes
     C = wl.n - wl.w
     kv_bytes = B * L * wl.hkv * wl.n * wl.d * e

@@ -24,6 +24,8 @@
  *   nothing and never synchronises implicitly: all work is enqueued on
  *   `stream` (a cudaStream_t passed as void*; NULL is the legacy default
  *   stream).  Inputs are read-only.
+ * - Calls run on the device current on the calling thread.  A process may drive
+ *   several devices: launch settings are kept per device.
  * - `ws` is a caller-provided device workspace of at least
  *   kv_workspace_size(op, shape) bytes for the op it is passed to.  Its first
  *   256 bytes hold a device error word.  Zero the whole workspace once before
@@ -219,10 +221,14 @@ KV_API kv_status flat_decode_attn(const kv_shape* shape, const void* q,
  *   KV_ERR_WORKSPACE before anything is enqueued.
  * - The first call on each device looks up that device's copy of the array (with the
  *   device current) and caches it; make that first call before any stream capture.
- * - Every call on a device shares the one array and leaves its last contents there.
+ * - Every call on a device shares the one array and leaves its last contents there.  Each
+ *   call first clears, on its own stream (cudaMemsetAsync, which allocates nothing), the
+ *   parts the decode kernels need at zero: the error word and the split decode's tickets.
+ *   The rest (partials, chunk map, work counter) is written before it is read.
  *   Calls whose kernels overlap on the GPU (different streams without ordering between
- *   them) race on it: order them on one stream, or use flat_decode_attn with separate
- *   workspaces.
+ *   them) race on the array and can return wrong outputs: order them on one stream, or use
+ *   flat_decode_attn with separate workspaces.  A later, correctly ordered call is not
+ *   affected by such a race, since it clears the tickets again.
  * - Device-side checks (an append with no reserve row left) behave as in flat_decode_attn
  *   (the append is skipped and lens is not advanced) but are not reported: there is no
  *   workspace for kv_check_device_status to read.

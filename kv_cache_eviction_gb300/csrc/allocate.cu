@@ -575,18 +575,18 @@ alloc_sweep2(const float* __restrict__ scores, int Hkv, int C, int nch, int64_t 
 
 // CTAs of alloc_sweep2 that can be resident at once (its cooperative launch needs them all).
 static int64_t sweep2_resident() {
-  static int64_t cached = 0;
-  if (cached == 0) {
-    int occ = 0;
+  static std::atomic<int> slot[kMaxDevices];
+  const int occ = per_device(slot, []() {
+    int n = 0;
     if (cudaFuncSetAttribute(alloc_sweep2, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kRingBytes) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, alloc_sweep2, kThreads,
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, alloc_sweep2, kThreads,
                                                       kRingBytes) != cudaSuccess ||
-        occ < 1)
-      occ = 1;
-    cached = (int64_t)occ * num_sms();
-  }
-  return cached;
+        n < 1)
+      n = 1;
+    return n;
+  });
+  return (int64_t)occ * num_sms();
 }
 
 AllocPlan alloc_plan(const Shape& s) {
@@ -650,16 +650,18 @@ cudaError_t launch_allocate(const Shape& s, const float* scores, const int64_t* 
   // barriers, histograms and counts start at zero
   cudaError_t e = cudaMemsetAsync(ws + p.off_zero, 0, p.off_union - p.off_zero, st);
   if (e != cudaSuccess) return e;
-  static bool opted = false;   // the sweeps' rings are dynamic shared memory above 48 KB
-  if (!opted) {
+  // the sweeps' rings are dynamic shared memory above 48 KB: opted in once per device
+  static std::atomic<int> opted[kMaxDevices];
+  const int ok = per_device(opted, []() {
     const void* ks[3] = {(const void*)alloc_sweep1<true>, (const void*)alloc_sweep1<false>,
                          (const void*)alloc_sweep2};
-    for (const void* k : ks) {
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
-      if (e != cudaSuccess) return e;
-    }
-    opted = true;
-  }
+    for (const void* k : ks)
+      if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes) !=
+          cudaSuccess)
+        return 0;
+    return 1;
+  });
+  if (!ok) return cudaErrorInvalidConfiguration;
   const dim3 sweep((unsigned)nch, (unsigned)S);
   if (entropy_mode)
     alloc_sweep1<true><<<sweep, kThreads, kRingBytes, st>>>(scores, N, nch, part, ghist, hdr);

@@ -657,13 +657,12 @@ cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const f
     uint32_t* gkey = reinterpret_cast<uint32_t*>(
         ws + p.off_union + align_up((size_t)H * C * sizeof(int32_t), 256));
     auto kern = crit ? head_select<true> : head_select<false>;
-    static bool opted[2] = {false, false};
-    if (!opted[crit ? 1 : 0]) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)ring_bytes);
-      if (e != cudaSuccess) return e;
-      opted[crit ? 1 : 0] = true;
-    }
+    static std::atomic<int> opted[2][kMaxDevices];   // per kernel, per device
+    const int ok = per_device(opted[crit ? 1 : 0], [&]() {
+      return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)ring_bytes) == cudaSuccess ? 1 : 0;
+    });
+    if (!ok) return cudaErrorInvalidConfiguration;
     // a cluster of one CTA: the whole-head fallback's cluster barriers are the block's own
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)H);

@@ -620,16 +620,17 @@ static cudaError_t launch_attn(const Shape& s, const T* q, const void* kf, const
                                cudaStream_t st) {
   const size_t smem = sizeof(DecSmem);
   auto kern = decode_attn<T, GM, LPRT>;
-  // the shared-memory opt-in and the resident CTAs per SM, once per instantiation (host work
-  // on every call would delay the launches behind it)
-  static const int per_sm = [&]() {
+  // the shared-memory opt-in and the resident CTAs per SM, once per instantiation and device
+  // (host work on every call would delay the launches behind it)
+  static std::atomic<int> slot[kMaxDevices];
+  const int per_sm = per_device(slot, [&]() {
     int n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem) != cudaSuccess)
       return 0;
     return n;
-  }();
+  });
   if (per_sm <= 0) return cudaErrorInvalidConfiguration;
   int64_t grid = (int64_t)per_sm * num_sms();
   const int64_t need = cdiv(nchunks, kWarps);

@@ -209,17 +209,21 @@ bool decode_head_supported(const Shape& s, int64_t cap) {
   return s.d * s.esize() == kHRowBytes && s.G() <= 8 && H > 0 && cap / H <= kDecodeHeadRowsMax;
 }
 
-// One instantiation: its shared-memory opt-in once (each kernel needs its own), then the
-// launch, one CTA per KV head.
+// One instantiation: its shared-memory opt-in once per device (each kernel needs its own),
+// then the launch, one CTA per KV head.
 template <typename T, int GM>
 static cudaError_t launch_head_t(const Shape& s, const void* q, const void* kn, const void* vn,
                                  void* kf, void* vf, const int64_t* cu, int32_t* lens,
                                  int64_t cap, float c2, void* out, WsHeader* hdr,
                                  cudaStream_t st) {
   const size_t smem = sizeof(HeadSmem);
-  static const cudaError_t opted = cudaFuncSetAttribute(
-      decode_head<T, GM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (opted != cudaSuccess) return opted;
+  static std::atomic<int> opted[kMaxDevices];
+  if (!per_device(opted, [&]() {
+        return cudaFuncSetAttribute(decode_head<T, GM>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem) == cudaSuccess ? 1 : 0;
+      }))
+    return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)s.units());
   cfg.blockDim = dim3(kHThreads);

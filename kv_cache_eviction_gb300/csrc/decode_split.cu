@@ -587,8 +587,8 @@ bool decode_split_supported(const Shape& s, int64_t cap) {
          cap <= (int64_t)INT32_MAX;
 }
 
-// One instantiation: its shared-memory opt-in and resident CTAs per SM once (each kernel
-// needs its own), then the launch of one wave.
+// One instantiation: its shared-memory opt-in and resident CTAs per SM once per device
+// (each kernel needs its own), then the launch of one wave.
 template <typename T, int GM>
 static cudaError_t launch_split_t(const Shape& s, const void* q, const void* kn, const void* vn,
                                   void* kf, void* vf, const int64_t* cu, int32_t* lens,
@@ -596,7 +596,8 @@ static cudaError_t launch_split_t(const Shape& s, const void* q, const void* kn,
                                   int64_t part_slots, uint32_t* tick, WsHeader* hdr,
                                   cudaStream_t st) {
   const size_t smem = sizeof(SplitSmem);
-  static const int per_sm = [&]() {
+  static std::atomic<int> slot[kMaxDevices];
+  const int per_sm = per_device(slot, [&]() {
     int n = 0;
     if (cudaFuncSetAttribute(decode_split<T, GM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess ||
@@ -604,7 +605,7 @@ static cudaError_t launch_split_t(const Shape& s, const void* q, const void* kn,
                                                       smem) != cudaSuccess)
       return 0;
     return n;
-  }();
+  });
   if (per_sm <= 0) return cudaErrorInvalidConfiguration;
   int64_t grid = (int64_t)per_sm * num_sms();
   if (2 * grid > part_slots) grid = part_slots / 2;   // two partial slots per CTA

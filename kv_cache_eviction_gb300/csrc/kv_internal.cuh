@@ -1,9 +1,32 @@
 // Internal launch interface between the C ABI (kvevict_api.cu) and the kernels.
 #pragma once
 
+#include <atomic>
+
 #include "kv_common.cuh"
 
 namespace kv {
+
+// ------------------------- per-device launch state ---------------------------
+// Launch settings (shared-memory opt-ins, resident CTAs per SM, SM counts) belong to a
+// device, so they are cached per device: a process may drive several GPUs.
+constexpr int kMaxDevices = 64;
+// The device current on the calling thread, or -1 if it cannot be read.
+int current_device();
+// `make()` evaluated once per device (with that device current) and cached; a device id
+// outside [0, kMaxDevices) is not cached.  Two threads may both evaluate `make()` the
+// first time, which is harmless for the idempotent settings kept here.
+template <typename F>
+inline int per_device(std::atomic<int> (&slot)[kMaxDevices], F make) {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return make();
+  int v = slot[dev].load(std::memory_order_acquire);
+  if (v == 0) {
+    v = make();   // 0 means "not known yet": a failed query is retried on the next call
+    slot[dev].store(v, std::memory_order_release);
+  }
+  return v;
+}
 
 struct Shape {
   int B, L, Hq, Hkv, d, n, w, pool, dtype;

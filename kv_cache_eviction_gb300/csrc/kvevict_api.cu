@@ -9,31 +9,34 @@
 
 namespace kv {
 
+int current_device() {
+  int dev = -1;
+  return cudaGetDevice(&dev) == cudaSuccess ? dev : -1;
+}
+
 int num_sms() {
-  static int cached = 0;
-  if (cached == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      cached = v;
-    else
-      cached = 148;
-  }
-  return cached;
+  static std::atomic<int> slot[kMaxDevices];
+  return per_device(slot, []() {
+    int v = 0;
+    const int dev = current_device();
+    if (dev >= 0 && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        v > 0)
+      return v;
+    return 148;
+  });
 }
 
 size_t max_smem_optin() {
-  static size_t cached = 0;
-  if (cached == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
+  static std::atomic<int> slot[kMaxDevices];
+  return (size_t)per_device(slot, []() {
+    int v = 0;
+    const int dev = current_device();
+    if (dev >= 0 &&
         cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
         v > 0)
-      cached = (size_t)v;
-    else
-      cached = 48 * 1024;
-  }
-  return cached;
+      return v;
+    return 48 * 1024;
+  });
 }
 
 static std::atomic<unsigned long long> g_launches{0};
@@ -198,26 +201,42 @@ kv_status kv_compact(const kv_shape* shape, const void* k, const void* v, const 
                                     p, static_cast<cudaStream_t>(stream)));
 }
 
-kv_status flat_decode_attn(const kv_shape* shape, const void* q, const void* k_new,
-                           const void* v_new, void* k_flat, void* v_flat, const int64_t* cu_off,
-                           int32_t* lens, int64_t flat_capacity_rows, float softmax_scale,
-                           void* out, void* ws, size_t ws_bytes, void* stream) {
-  Shape s;
-  if (!shape_ok(shape, &s)) return KV_ERR_INVALID_ARG;
-  if (ws == nullptr || !aligned16(ws)) return KV_ERR_INVALID_ARG;
+// Argument checks of a decode step; on KV_OK, `s` and `p` hold its shape and workspace plan.
+static kv_status decode_check(const kv_shape* shape, const void* q, const void* k_new,
+                              const void* v_new, const void* k_flat, const void* v_flat,
+                              const int64_t* cu_off, const int32_t* lens,
+                              int64_t flat_capacity_rows, float softmax_scale, const void* out,
+                              Shape* s, DecodePlan* p) {
+  if (!shape_ok(shape, s)) return KV_ERR_INVALID_ARG;
   if ((k_new == nullptr) != (v_new == nullptr)) return KV_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return KV_ERR_INVALID_ARG;
   if (flat_capacity_rows < 0) return KV_ERR_INVALID_ARG;
-  if (s.units() == 0) return KV_OK;
+  if (s->units() == 0) {
+    *p = DecodePlan{};
+    return KV_OK;
+  }
   if (q == nullptr || k_flat == nullptr || v_flat == nullptr || cu_off == nullptr ||
       lens == nullptr || out == nullptr)
     return KV_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k_flat, v_flat, cu_off, lens, out};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return KV_ERR_INVALID_ARG;
+  for (const void* x : ptrs)
+    if (!aligned16(x)) return KV_ERR_INVALID_ARG;
   if (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))) return KV_ERR_INVALID_ARG;
-  if (!shape_supported(s) || s.G() * s.d > 1024) return KV_ERR_UNSUPPORTED;
-  const DecodePlan p = decode_plan(s);
+  if (!shape_supported(*s) || s->G() * s->d > 1024) return KV_ERR_UNSUPPORTED;
+  *p = decode_plan(*s);
+  return KV_OK;
+}
+
+kv_status flat_decode_attn(const kv_shape* shape, const void* q, const void* k_new,
+                           const void* v_new, void* k_flat, void* v_flat, const int64_t* cu_off,
+                           int32_t* lens, int64_t flat_capacity_rows, float softmax_scale,
+                           void* out, void* ws, size_t ws_bytes, void* stream) {
+  if (ws == nullptr || !aligned16(ws)) return KV_ERR_INVALID_ARG;
+  Shape s;
+  DecodePlan p;
+  const kv_status st = decode_check(shape, q, k_new, v_new, k_flat, v_flat, cu_off, lens,
+                                    flat_capacity_rows, softmax_scale, out, &s, &p);
+  if (st != KV_OK || s.units() == 0) return st;
   if (ws_bytes < p.off_end) return KV_ERR_WORKSPACE;
   return cuda_status(launch_decode(s, q, k_new, v_new, k_flat, v_flat, cu_off, lens,
                                    flat_capacity_rows, softmax_scale, out,
@@ -245,14 +264,30 @@ kv_status flat_decode_attn_noalloc(const kv_shape* shape, const void* q, const v
                                    const int64_t* cu_off, int32_t* lens,
                                    int64_t flat_capacity_rows, float softmax_scale, void* out,
                                    void* stream) {
+  Shape s;
+  DecodePlan p;
+  const kv_status st = decode_check(shape, q, k_new, v_new, k_flat, v_flat, cu_off, lens,
+                                    flat_capacity_rows, softmax_scale, out, &s, &p);
+  if (st != KV_OK || s.units() == 0) return st;
+  // A decode whose plan needs more than the fixed array is refused before anything is
+  // enqueued.
+  if (p.off_end > (size_t)KV_DECODE_NOALLOC_SCRATCH_BYTES) return KV_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (noalloc_scratch(&scratch) != cudaSuccess) return KV_ERR_CUDA;
-  // The split-K partials are fully written before they are read, so nothing in the shared
-  // scratch has to start at zero.  A decode that needs more than the fixed array gets
-  // KV_ERR_WORKSPACE from the size check below, before anything is enqueued.
-  return flat_decode_attn(shape, q, k_new, v_new, k_flat, v_flat, cu_off, lens,
-                          flat_capacity_rows, softmax_scale, out, scratch,
-                          (size_t)KV_DECODE_NOALLOC_SCRATCH_BYTES, stream);
+  char* ws = static_cast<char*>(scratch);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // The array starts at zero when the library is loaded, but it is shared by every call and
+  // no caller reads its error word back.  So each call clears, on its own stream, what the
+  // decode kernels need at zero: the error word (a check that fired in an earlier call must
+  // not linger) and the one-launch split's tickets.  Those return to zero at the end of every
+  // complete launch; clearing them here also undoes a launch that was cut short or raced
+  // with an overlapping call.  The partials, the chunk map and the work counter are written
+  // before they are read in every launch.  A memset allocates nothing.
+  if (cudaMemsetAsync(ws, 0, kWsHeader, cs) != cudaSuccess ||
+      cudaMemsetAsync(ws + p.off_tick, 0, p.off_end - p.off_tick, cs) != cudaSuccess)
+    return KV_ERR_CUDA;
+  return cuda_status(launch_decode(s, q, k_new, v_new, k_flat, v_flat, cu_off, lens,
+                                   flat_capacity_rows, softmax_scale, out, ws, p, cs));
 }
 
 uint64_t kv_kernel_launches(void) { return (uint64_t)g_launches.load(); }

@@ -23,11 +23,10 @@ Pages (cited by title and section):
 * The LaProx page ("Reformulating KV cache eviction for long-context LLM
   inference"), Eq. 2, for the 1/sqrt(d_h) logit scale.
 
-Readings taken where the pages are silent or disagree (each one is listed in
-DESIGN.md as well):
+Readings taken where the pages are silent or disagree:
 
 * Logits carry 1/sqrt(d_h) (LaProx Eq. 2, LAVa's residual-stream view); the
-  Ada-KV arXiv page drops it only "for simplification".
+  Ada-KV arXiv page leaves the scale out only to keep its notation short.
 * The window softmax normalises over all n keys with the causal mask: window
   row t is the query of position n-w+t and sees keys j <= n-w+t.  The literal
   prefix-only normalisation of Algorithm 2 is kept as ``normalise="prefix"``.
@@ -36,8 +35,9 @@ DESIGN.md as well):
   reduction (mean for Ada-KV, max for LAVa).  Pooling each window row before the
   mean (the literal Algorithm 2 order) is kept as ``order="pool_rows"``.
 * GQA maps query head q to KV head floor(q / G).
-* The layer budget B counts the w*Hkv window rows (Algorithm 2, "B = B -
-  winsize*h"); B' = B - w*Hkv is what the selection distributes.
+* The layer budget B counts the w*Hkv window rows (Ada-KV Algorithm 2 takes the
+  window's rows off the budget before allocating); B' = B - w*Hkv is what the
+  selection distributes.
 * Safeguard: B_g = alpha*B'/Hkv + (1-alpha)*f_g, alpha the weight on the
   uniform share (alpha = 1 gives uniform SnapKV, budgets never fall below
   floor(alpha*B'/Hkv)); alpha = a/b is rational and rounding is exact.

@@ -109,3 +109,64 @@ def oracle_kept_check(sg_oracle: np.ndarray, kept_gpu: np.ndarray, k: int, tie_r
     # scores below the 1e-12 absolute floor of the score tolerance count as ties too
     assert np.all(gap <= tie_rel * tau + abs_floor), (diff, sg_oracle[diff], tau)
     return diff.size
+
+
+def oracle_crit_kept_check(s_ref: np.ndarray, c_ref: np.ndarray, s_gpu: np.ndarray,
+                           kept_gpu: np.ndarray, k: int, a: int, b: int, eps: float,
+                           tie_rel=1e-5, abs_floor=1e-12):
+    """End-to-end check of one head's CriticalKV two-stage selection.
+
+    The GPU's stage-1 set is recovered from its kept rows: the floor(a/b * k) of them that
+    rank highest by the GPU's own float32 scores (stage 1 is the top of every candidate by
+    that order, so it is the top of the kept rows too).  Then
+      - stage 1 may differ from the oracle's top by s only at s near-ties (oracle_kept_check);
+      - the rest of the kept rows must be the top k - k1 of the candidates outside the GPU's
+        stage 1, ranked by the oracle's kappa = (s + eps) * c, up to kappa near-ties.
+    Returns the number of positions that differ from the oracle's own two-stage result."""
+    assert len(kept_gpu) == k
+    assert np.all(np.diff(kept_gpu) > 0)
+    k1 = (a * k) // b
+    order = np.lexsort((kept_gpu, -s_gpu[kept_gpu].astype(np.float64)))
+    st1 = np.sort(kept_gpu[order[:k1]])
+    oracle_kept_check(s_ref, st1, k1, tie_rel, abs_floor)
+    st2 = np.setdiff1d(kept_gpu, st1)
+    rest = np.setdiff1d(np.arange(len(s_ref)), st1)
+    kappa = (s_ref + eps) * c_ref
+    k2 = k - k1
+    ref2 = rest[np.lexsort((rest, -kappa[rest]))[:k2]]
+    diff = np.setxor1d(ref2, st2)
+    if diff.size:
+        tau = np.sort(kappa[rest])[::-1][k2 - 1]
+        gap = np.abs(kappa[diff] - tau)
+        assert np.all(gap <= tie_rel * tau + abs_floor), (diff, kappa[diff], tau)
+    full = O.critical_positions(s_ref, c_ref, k, a, b, eps)
+    return int(np.setxor1d(full, kept_gpu).size)
+
+
+def assert_decode_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "decode",
+                        atol: float = None) -> float:
+    """The decode bar against the fp64 oracle; returns the plain max-abs error.
+
+    bf16: 1e-2 max-abs, applied to the float32-accumulated result.  The ABI stores the output
+    in bf16, whose rounding adds up to half an ulp (at most 2^-8 |ref|).  Below |ref| = 4 that
+    half ulp is at most 2^-7 < 1e-2, so there the plain bar |got - ref| <= 1e-2 is asserted as
+    it stands; at |ref| >= 4 (where no bf16 value could meet a plain 1e-2) the half ulp is
+    added to it.  float32 (stored as computed): 1e-4 max-abs.
+    """
+    err = np.abs(got - ref)
+    if dtype == "bf16":
+        a = 1e-2 if atol is None else atol
+        small = np.abs(ref) < 4.0
+        ok = np.where(small, err <= a, err <= a + 2.0 ** -8 * np.abs(ref))
+    else:
+        a = 1e-4 if atol is None else atol
+        ok = err <= a
+    plain = float(err.max()) if err.size else 0.0
+    small_err = float(err[np.abs(ref) < 4.0].max()) if (np.abs(ref) < 4.0).any() else 0.0
+    print("%s: plain max-abs err %.3e (%.3e where |ref| < 4), max |ref| %.3g" %
+          (what, plain, small_err, float(np.abs(ref).max()) if ref.size else 0.0))
+    if not ok.all():
+        i = np.unravel_index(np.argmax(np.where(ok, 0.0, err)), err.shape)
+        raise AssertionError("%s: %d outside the decode bar; worst at %s got %r ref %r" %
+                             (what, int((~ok).sum()), i, got[i], ref[i]))
+    return plain

@@ -20,7 +20,7 @@ import torch
 import kv_cache_eviction_gb300 as kv
 import oracle as O
 
-from .kvpath import np64, workspace
+from .kvpath import assert_decode_close, np64, workspace
 
 pytestmark = pytest.mark.gpu
 
@@ -115,12 +115,7 @@ def check(c, B, L, hkv, G, d, dtype, append, expect_code=0):
     assert code == expect_code
     got = np64(out)
     assert np.isfinite(got).all()
-    if dtype == "bf16":
-        tol = 1e-2 + 2.0 ** -8 * np.abs(ref)      # fp32 accumulation, bf16 output rounding
-    else:
-        tol = 1e-4 + 1e-4 * np.abs(ref)
-    err = np.abs(got - ref)
-    assert (err <= tol).all(), "max err %g at %s" % (err.max(), np.unravel_index(err.argmax(), err.shape))
+    assert_decode_close(got, ref, dtype)
     np.testing.assert_array_equal(lens.cpu().numpy().reshape(B, L, hkv), ref_lens)
     if append:
         # the appended rows are exact copies of k_new / v_new
@@ -222,5 +217,5 @@ def test_decode_repeated_steps_match_single_oracle_run():
         ref, Kf, Vf, ln = O.flat_decode(np64(q[0, 0]), Kf, Vf, cu_h, ln, scale, np64(kn[0, 0]),
                                         np64(vn[0, 0]))
         got = np64(out[0, 0])
-        assert (np.abs(got - ref) <= 1e-2 + 2.0 ** -8 * np.abs(ref)).all(), step
+        assert_decode_close(got, ref, "bf16", what="decode step %d" % step)
     np.testing.assert_array_equal(lens_d.cpu().numpy(), ln)
