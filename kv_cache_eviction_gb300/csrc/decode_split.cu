@@ -17,6 +17,8 @@
 //      through its own ring of bulk copies, in tiles of 2U rows, and reads the new row from
 //      k_new / v_new (appending it to the flat buffer);
 //   (a call with few rows uses only as many CTAs as give each kSplitMinRows rows);
+//   the q rows and the new row of a warp's heads are loaded one head ahead, so neither is a
+//   dependent load behind a head's stream;
 //   3. a head held by one warp is written out by it; the pieces of a head split between
 //      warps are merged in shared memory; a head that crosses CTA boundaries leaves one
 //      partial per CTA in global memory, and the last CTA to finish it (a per-head ticket)
@@ -38,14 +40,16 @@ constexpr int kSThreads = kSWarps * 32;
 constexpr int kSPer = (int)(kDecodeSplitHeadsMax / kSThreads);   // heads per thread, step 1
 static_assert(kSPer * kSThreads == kDecodeSplitHeadsMax, "scan covers every head");
 constexpr int kSCand = kSWarps + 1;   // heads a CTA may have to merge
-// Used rows per CTA at least (8 warps x 48 rows in flight): a small call, such as one
-// layer's heads, runs on as few CTAs as that allows instead of merging every head from
-// partials of a dozen CTAs.
-constexpr int64_t kSplitMinRows = 384;
+// Used rows per CTA at least: a small call, such as one layer's heads, runs on as few CTAs
+// as that allows.  Measured on GB300 (L2 flushed): 64 rather than 384 spreads a 128K
+// context's 34K used rows over every SM (27 vs 32 us) and one layer's 1K rows over 17 CTAs
+// instead of 3 (15 vs 20 us), and changes nothing on caches of 1M rows.
+constexpr int64_t kSplitMinRows = 64;
 // A CTA boundary that falls inside a head of at most this many used rows moves to the
 // nearer end of that head: short heads are never split between CTAs (no partials in global
 // memory, no ticket), and a CTA's range grows or shrinks by at most half such a head.
-constexpr int64_t kSplitSnapRows = 512;
+// (256 measured slightly ahead of 512 on the 128K cache, equal elsewhere.)
+constexpr int64_t kSplitSnapRows = 256;
 
 struct SplitSmem {
   WarpRing ring[kSWarps];   // after the stream: the warps' partials, slots 2k and 2k + 1
@@ -58,6 +62,7 @@ struct SplitSmem {
   uint32_t cslots[kSCand];                   // each) and counts, and whether they cross
   int32_t cn[kSCand], ccross[kSCand];        // the CTA's ends
   int32_t ncand, win[2];
+  int64_t bnd[2];                            // the CTA's first and end used rows
 };
 static_assert(sizeof(SplitSmem) <= 227 * 1024, "one CTA per SM");
 
@@ -170,7 +175,7 @@ decode_split(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
              T* __restrict__ kf, T* __restrict__ vf, const int64_t* __restrict__ cu,
              int32_t* __restrict__ lens, int64_t cap, T* __restrict__ out, int H, int Hkv,
              int G, float c2, float* __restrict__ part, uint32_t* __restrict__ tick,
-             WsHeader* hdr) {
+             int64_t min_rows, int64_t snap_rows, WsHeader* hdr) {
   using Att = RowTileAttn<T, GM>;
   constexpr int VE = Att::VE, V2 = Att::V2, D = Att::D, U = Att::U;
   constexpr int NSL = D / VE;   // 16-byte slices per row
@@ -277,7 +282,7 @@ decode_split(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
 
   // ---- 2. this CTA's rows, an eighth per warp
   const int64_t Tu = S.P[H];   // used rows of all heads
-  const int64_t ne = (Tu + kSplitMinRows - 1) / kSplitMinRows;
+  const int64_t ne = (Tu + min_rows - 1) / min_rows;
   const int Ne = (int)(ne < 1 ? 1 : ne > N ? N : ne);   // CTAs that take rows
   if (c >= Ne) {
     leave();
@@ -291,10 +296,14 @@ decode_split(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
     if (x <= 0 || x >= Tu) return x;
     const int h = head_of(S.P, H, x);
     const int64_t lo = S.P[h], hi = S.P[h + 1];
-    if (hi - lo > kSplitSnapRows) return x;
+    if (hi - lo > snap_rows) return x;
     return x - lo <= hi - x ? lo : hi;
   };
-  const int64_t b0 = bound(c), b1 = bound(c + 1);
+  // the CTA's two ends, each found by one thread, shared through shared memory
+  if (tid == 0) S.bnd[0] = bound(c);
+  if (tid == 32) S.bnd[1] = bound(c + 1);
+  __syncthreads();
+  const int64_t b0 = S.bnd[0], b1 = S.bnd[1];
   const int64_t span = b1 - b0;
   const int64_t xs = b0 + span * warp / kSWarps, xe = b0 + span * (warp + 1) / kSWarps;
 
@@ -339,8 +348,18 @@ decode_split(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
     __syncwarp();   // the barriers are initialised
     for (int i = 0; i < kStages; ++i) issue_next();
 
+    // q and the new row (k_new / v_new, half 0 of the warp) of a head are loaded when its
+    // turn is one head away, so neither is a dependent load behind the head's stream
     uint4 qr[GM];
+    uint4 nkr = make_uint4(0u, 0u, 0u, 0u), nvr = nkr;
+    auto load_new = [&](int hh) {
+      if (half == 0 && S.app[hh]) {
+        nkr = *reinterpret_cast<const uint4*>(kn + (int64_t)hh * D + ci * VE);
+        nvr = *reinterpret_cast<const uint4*>(vn + (int64_t)hh * D + ci * VE);
+      }
+    };
     load_q<T, GM>(q, hf, G, ci, qr);
+    load_new(hf);
     int qh = hf, hlast = hf;
     for (int h = hf; h < H; ++h) {
       const int64_t Ph = S.P[h], Ph1 = S.P[h + 1];
@@ -351,11 +370,16 @@ decode_split(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
       const bool app = S.app[h] != 0;
       const int64_t fend = Ph1 - (app ? 1 : 0);
       const int64_t fe = fend < hi ? fend : hi;
-      if (qh != h) load_q<T, GM>(q, h, G, ci, qr);
+      if (qh != h) {
+        load_q<T, GM>(q, h, G, ci, qr);
+        load_new(h);
+      }
       att.begin(qr, c2);
-      // the next head's q, while this one streams
+      const uint4 ckr = nkr, cvr = nvr;   // this head's new row
+      // the next head's q and new row, while this one streams
       if (h + 1 < H && Ph1 < xe) {
         load_q<T, GM>(q, h + 1, G, ci, qr);
+        load_new(h + 1);
         qh = h + 1;
       }
       for (int64_t x = lo; x < fe;) {
@@ -387,8 +411,8 @@ decode_split(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
           vr[u] = kr[u];
         }
         if (half == 0) {
-          kr[0] = *reinterpret_cast<const uint4*>(kn + (int64_t)h * D + ci * VE);
-          vr[0] = *reinterpret_cast<const uint4*>(vn + (int64_t)h * D + ci * VE);
+          kr[0] = ckr;
+          vr[0] = cvr;
           const int64_t row = (int64_t)S.base[h] + (fend - Ph);
           reinterpret_cast<uint4*>(kf + row * D)[ci] = kr[0];
           reinterpret_cast<uint4*>(vf + row * D)[ci] = vr[0];
@@ -620,7 +644,8 @@ static cudaError_t launch_split_t(const Shape& s, const void* q, const void* kn,
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split<T, GM>, (const T*)q, (const T*)kn,
                                            (const T*)vn, (T*)kf, (T*)vf, cu, lens, cap, (T*)out,
-                                           (int)s.units(), s.Hkv, s.G(), c2, part, tick, hdr);
+                                           (int)s.units(), s.Hkv, s.G(), c2, part, tick,
+                                           kSplitMinRows, kSplitSnapRows, hdr);
   if (e == cudaSuccess) count_launches(1);
   return e;
 }
