@@ -1,14 +1,16 @@
 #!/usr/bin/env python3
 """Throughput of the KV-cache eviction pass and the flat decode attention on GB300.
 
-One step = one eviction pass over every (sequence, layer) of the workload
-(kv_score -> kv_allocate -> kv_compact) followed by one decode step of
-flat_decode_attn over every layer (with the append).  The headline value is
-eviction-pass prefix tokens per second per layer: batch * n * L prefix tokens
-pass through one layer's eviction in (step time / L), i.e.
-value = batch * n * L / step_time, summed over ranks.  The second number, the
-flat varlen decode attention's HBM GB/s, is measured on its own with L2 flushed
-before every decode step.
+One step = one pass of the whole hot path over one batch: an eviction pass over every
+(sequence, layer) of the workload (kv_score -> kv_allocate -> kv_compact) followed by one
+decode step of flat_decode_attn over every layer (with the append).  The headline value is
+eviction-pass prefix tokens per second per layer, (batch * n * L) / step_time / L, i.e.
+batch * n / step_time summed over ranks: the prompt tokens whose whole-model cache the path
+evicts (and then decodes over) per second.  `eviction_only` gives the same rate over the
+eviction stages alone (score + allocate + compact).  The second number, the flat varlen
+decode attention's HBM GB/s, is measured on its own with L2 flushed before every decode
+step.  The other workloads of the pages' configurations are timed after the headline one
+(`workloads`), and the CPU oracle on the host cores (`cpu_baseline`: one core and all).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -66,6 +68,8 @@ def parse_args():
                     help="skip the decode-only measurement with one call per layer")
     ap.add_argument("--no-graph", action="store_true",
                     help="time the step with eager launches only (no CUDA graph replay)")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the step timings of the pages' other configurations")
     ap.add_argument("--no-decode-large", action="store_true",
                     help="skip the decode-only measurement on the large flat cache")
     return ap.parse_args()
@@ -89,9 +93,9 @@ def max_over_ranks(t: float, device=None) -> float:
 
 
 def aggregate_value(world: int, batch: int, n: int, layers: int, ms: float) -> float:
-    """Whole-job eviction-pass prefix tokens/s per layer: every rank's batch * n * L prefix
-    tokens through one layer's eviction in (slowest rank's step time / L)."""
-    return world * batch * n * layers / (ms / 1e3)
+    """Whole-job eviction-pass prefix tokens/s per layer: every rank's batch * n * L
+    (token, layer) pairs in the slowest rank's step time, per layer (divided by L)."""
+    return world * batch * n * layers / (ms / 1e3) / layers
 
 
 def dist_env():
@@ -157,20 +161,31 @@ def read_peaks():
 # CPU oracle sample (the cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(wl, use_cuda_inputs: bool):
-    """One KV head of (sequence 0, layer 0): its inputs as fp64 numpy arrays."""
+def oracle_heads(wl, count: int, use_cuda_inputs: bool):
+    """Inputs of `count` KV heads as fp64 numpy arrays: (sequence 0, layer l, head g) in
+    (l, g) order, each with its G window queries, its K and V rows (and its W_O block) and
+    one decode step's q, k_new and v_new."""
     import torch
     from kv_cache_eviction_gb300 import workloads as W
     dev = "cuda" if use_cuda_inputs else "cpu"
-    u = W.make_unit(wl, 0, 0, device=dev)
     G = wl.hq // wl.hkv
     to = lambda t: t.to("cpu", torch.float64).numpy()
-    out = {"q": to(u["q_win"][:G]), "k": to(u["k"][:1]), "v": to(u["v"][:1])}
-    if "w_o" in u:
-        out["w_o"] = to(u["w_o"][:1])
-    dec = W.make_decode_step(wl, 0, u["tau"], 0, 0, device=dev)
-    out["dq"], out["kn"], out["vn"] = to(dec["q"][:G]), to(dec["k_new"][:1]), to(dec["v_new"][:1])
-    del u
+    out = []
+    layer = 0
+    while len(out) < count:
+        u = W.make_unit(wl, 0, layer, device=dev)
+        dec = W.make_decode_step(wl, 0, u["tau"], 0, layer, device=dev)
+        for g in range(wl.hkv):
+            if len(out) == count:
+                break
+            x = {"q": to(u["q_win"][g * G:(g + 1) * G]), "k": to(u["k"][g:g + 1]),
+                 "v": to(u["v"][g:g + 1]), "dq": to(dec["q"][g * G:(g + 1) * G]),
+                 "kn": to(dec["k_new"][g:g + 1]), "vn": to(dec["v_new"][g:g + 1])}
+            if "w_o" in u:
+                x["w_o"] = to(u["w_o"][g:g + 1])
+            out.append(x)
+        del u, dec
+        layer += 1
     return out
 
 
@@ -179,7 +194,6 @@ def oracle_step(wl, x):
     selection, gather) plus one decode step of its G query heads."""
     import numpy as np
     import oracle as O
-    C = wl.n - wl.w
     s, c = O.score_layer(x["q"], x["k"], x["v"], w=wl.w, pool=wl.pool, mode=wl.mode,
                          group=wl.group, w_o=x.get("w_o"))
     if wl.budget_kind == "layer":
@@ -195,10 +209,61 @@ def oracle_step(wl, x):
     return float(np.abs(o).sum())
 
 
-def sample_desc(wl):
-    return ("one KV head of one (sequence, layer) of %s (n=%d, %d query heads): window scoring, "
-            "its uniform share of the layer budget, selection, gather and one decode step; "
-            "tokens/s per layer = n / (Hkv * time)" % (wl.name, wl.n, wl.hq // wl.hkv))
+def oracle_rate(wl, heads: int, seconds: float) -> float:
+    """tokens/s per layer of the oracle: `heads` KV heads of n prefix tokens are each
+    1 / (L * Hkv) of a sequence's whole-model eviction."""
+    return heads * wl.n / (wl.layers * wl.hkv * seconds)
+
+
+def sample_desc(wl, heads=1):
+    return ("%d KV head(s) of (sequence 0, layers 0..%d) of %s (n=%d, %d query heads each): "
+            "window scoring, the head's uniform share of the layer budget, selection, gather "
+            "and one decode step; tokens/s per layer = heads * n / (L * Hkv * time)" %
+            (heads, (heads - 1) // wl.hkv, wl.name, wl.n, wl.hq // wl.hkv))
+
+
+_POOL_WL = None
+_POOL_X = None
+
+
+def _oracle_worker(i):
+    t0 = time.perf_counter()
+    oracle_step(_POOL_WL, _POOL_X[i])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl):
+    """The oracle on the host: one KV head on one core, then one head per core on every core
+    at once (a process pool forked before the process touches the GPU).  Call it before any
+    CUDA work."""
+    import multiprocessing
+    global _POOL_WL, _POOL_X
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    nproc = os.cpu_count() or cores
+    _POOL_WL = wl
+    _POOL_X = oracle_heads(wl, cores, False)
+    # one core: heads one after another, until about 10 s of work or every generated head
+    t1, done = 0.0, 0
+    while done < cores and (done == 0 or t1 < 10.0):
+        t1 += _oracle_worker(done)
+        done += 1
+    res = {"value": oracle_rate(wl, done, t1), "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": sample_desc(wl, done), "seconds": t1, "nproc": nproc}
+    if cores > 1:
+        with multiprocessing.get_context("fork").Pool(cores) as pool:
+            pool.map(_oracle_worker, range(cores), chunksize=1)    # touch every worker once
+            t0 = time.perf_counter()
+            per = pool.map(_oracle_worker, range(cores), chunksize=1)
+            t_all = time.perf_counter() - t0
+        res["all_cores"] = {"value": oracle_rate(wl, cores, t_all), "unit": UNIT,
+                            "cores": cores, "seconds": t_all,
+                            "sample": sample_desc(wl, cores),
+                            "per_head_seconds_mean": statistics.mean(per)}
+    _POOL_X = None
+    return res
 
 
 def run_reference(args):
@@ -213,7 +278,7 @@ def run_reference(args):
     use_cuda = torch.cuda.is_available()
     if use_cuda:
         torch.cuda.set_device(local)
-    x = oracle_sample(wl, use_cuda)
+    x = oracle_heads(wl, 1, use_cuda)[0]
     for _ in range(args.warmup):
         oracle_step(wl, x)
     times = []
@@ -222,7 +287,7 @@ def run_reference(args):
         oracle_step(wl, x)
         times.append(time.perf_counter() - t0)
     t = statistics.mean(times)
-    value = wl.n / (wl.hkv * t)
+    value = oracle_rate(wl, 1, t)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -230,7 +295,7 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator)",
         "config": {"workload": wl.name, "sample": "1 KV head of 1 (sequence, layer)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample_desc(wl)},
+                         "sample": sample_desc(wl, 1), "nproc": os.cpu_count()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -396,6 +461,139 @@ def decode_large(kv, W, dev, stream, flush, args):
                      "(log-normal, sigma 0.7), 256 reserve rows; L2 flushed before each step"}
 
 
+def time_crit_norm(kv, wl, shape, inp, crit, ws, dev, stream, reps=5):
+    """crit_tc_kernel alone: kv_crit_norm (the CriticalKV norm by itself, one launch) between
+    CUDA events on the launching stream, median of `reps` after one warm-up."""
+    import torch
+    B, L = shape.batch, shape.layers
+    C = wl.n - wl.w
+    ts = []
+    for _ in range(reps + 1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        kv.kv_crit_norm(shape, inp["v"], inp["w_o"], wl.model_dim, crit, ws, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ts.append(e0.elapsed_time(e1))
+    if kv.kv_check_device_status(ws, stream):
+        raise RuntimeError("device check in kv_crit_norm")
+    ms = statistics.median(ts[1:])
+    flops = 2.0 * B * L * wl.hkv * C * wl.d * wl.model_dim
+    tf = flops / (ms / 1e3) / 1e12
+    tpeak, tkind = read_tensor_peak()
+    return {"kernel": "crit_tc_kernel (||(V W_O)_j||_1 on tcgen05)", "ms": ms, "flops": flops,
+            "achieved": tf, "unit": "TFLOP/s", "peak": tpeak, "frac": tf / tpeak,
+            "peak_kind": tkind,
+            "how": "kv_crit_norm alone between CUDA events, median of %d" % reps}
+
+
+def measure_workload(kv, W, wl, dev, stream, steps, warmup):
+    """One more workload of the pages' configurations: the same step as the headline (eviction
+    pass over every (sequence, layer), then one decode step over every layer), eager launches
+    with CUDA events between the stages, inputs resident in HBM (larger than L2 except for
+    the one-layer workload, which flushes L2 between steps).  Its tensors are freed on
+    return."""
+    import torch
+    B, L = wl.batch, wl.layers
+    C = wl.n - wl.w
+    shape = kv.KvShape.from_workload(wl)
+    mode = {"ada": kv.KV_SCORE_ADA, "lava": kv.KV_SCORE_LAVA, "critical": kv.KV_SCORE_CRITICAL}[
+        wl.mode]
+    group = kv.KV_GROUP_MAX if wl.group == "max" else kv.KV_GROUP_MEAN
+    entropy = 1 if wl.budget_kind == "total" else 0
+    inp = W.make_batch(wl, device=dev)
+    budgets = wl.budgets().to(dev)
+    dec = W.make_decode_batch(wl, 0, inp["tau"], device=dev)
+    cap = wl.flat_capacity_rows()
+
+    def ws(op):
+        return torch.zeros(max(kv.kv_workspace_size(op, shape), 256), dtype=torch.uint8,
+                           device=dev)
+
+    w_s, w_a, w_c, w_d = (ws(kv.KV_OP_SCORE), ws(kv.KV_OP_ALLOCATE), ws(kv.KV_OP_COMPACT),
+                          ws(kv.KV_OP_DECODE))
+    scores = torch.empty(B, L, wl.hkv, C, dtype=torch.float32, device=dev)
+    crit = torch.empty_like(scores) if wl.mode == "critical" else None
+    lb = torch.empty(B, L, dtype=torch.int32, device=dev)
+    hb = torch.empty(B, L, wl.hkv, dtype=torch.int32, device=dev)
+    kept = torch.empty(cap, dtype=torch.int32, device=dev)
+    cu = torch.empty(B, L, wl.hkv + 1, dtype=torch.int64, device=dev)
+    lens = torch.empty(B, L, wl.hkv, dtype=torch.int32, device=dev)
+    kf = torch.empty(cap, wl.d, dtype=wl.torch_dtype, device=dev)
+    vf = torch.empty_like(kf)
+    out = torch.empty_like(dec["q"])
+    scale = 1.0 / math.sqrt(wl.d)
+    input_bytes = 2 * inp["k"].numel() * inp["k"].element_size()
+    flush = (torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+             if input_bytes <= 2 * L2_BYTES else None)
+
+    def step(ev):
+        ev[0].record(stream)
+        kv.kv_score(shape, mode, group, inp["q_win"], inp["k"],
+                    inp["v"] if wl.mode != "ada" else None, inp["w_o"], wl.model_dim, scores,
+                    crit, w_s, stream)
+        ev[1].record(stream)
+        kv.kv_allocate(shape, scores, budgets, entropy, wl.alpha[0], wl.alpha[1], lb, hb, w_a,
+                       stream)
+        ev[2].record(stream)
+        kv.kv_compact(shape, inp["k"], inp["v"], scores, crit, wl.crit_alpha[0],
+                      wl.crit_alpha[1], wl.crit_eps, hb, wl.reserve, kept, cu, lens, kf, vf, cap,
+                      w_c, stream)
+        ev[3].record(stream)
+        kv.flat_decode_attn(shape, dec["q"], dec["k_new"], dec["v_new"], kf, vf, cu, lens, scale,
+                            out, w_d, stream)
+        ev[4].record(stream)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
+           for _ in range(warmup + steps)]
+    for i in range(warmup + steps):
+        if flush is not None:
+            flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    for w_ in (w_s, w_a, w_c, w_d):
+        if kv.kv_check_device_status(w_, stream):
+            raise RuntimeError("device check in the %s step" % wl.name)
+    timed = evs[warmup:]
+    names = ["score", "allocate", "compact", "decode"]
+    stages = {nm: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in timed)
+              for j, nm in enumerate(names)}
+    ms = statistics.mean(e[0].elapsed_time(e[4]) for e in timed)
+    t_evict = stages["score"] + stages["allocate"] + stages["compact"]
+    hb_rows = int(hb.sum().item())
+    rows = int(lens.sum().item())
+    ab = algorithmic_bytes(wl, B, L, hb_rows, rows)
+    peak = read_peaks()[0]
+    res = {"workload": wl.name, "batch": B, "layers": L, "n": wl.n, "score": wl.mode,
+           "budget": ("total %d per sequence" % wl.total_budget_value()
+                      if wl.budget_kind == "total" else
+                      "%d per layer" % wl.layer_budget_value()),
+           "ms_per_step": ms, "value": aggregate_value(1, B, wl.n, L, ms), "unit": UNIT,
+           "eviction_only": aggregate_value(1, B, wl.n, L, t_evict), "stages_ms": stages,
+           "score_gbs": ab["score"] / (stages["score"] / 1e3) / 1e9,
+           "eviction_frac_of_hbm": (ab["score"] + ab["allocate"] + ab["compact"]) /
+           (t_evict / 1e3) / 1e9 / peak,
+           "decode_gbs_in_step": ab["decode"] / (stages["decode"] / 1e3) / 1e9,
+           "steps": steps, "timing": "eager launches, CUDA events between the stages",
+           "l2": "flushed before each step" if flush is not None else
+           "inputs larger than L2 (K+V %.1f GiB)" % (input_bytes / 2**30)}
+    if wl.mode == "critical":
+        res["crit_norm"] = time_crit_norm(kv, wl, shape, inp, crit, w_s, dev, stream)
+    del inp, scores, crit, kf, vf, kept, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+# Workloads timed after the headline one on the default run: the pages' other
+# configurations (the one-layer 16K sweep at three budgets, the 4 x 32-layer 32K set and the
+# 32-layer 64K CriticalKV set).
+OTHER_WORKLOADS = (("llama8b_16k_layer", {"head_budget_frac": 0.2}),
+                   ("llama8b_16k_layer", {"head_budget_frac": 0.4}),
+                   ("llama8b_16k_layer", {"head_budget_frac": 0.8}),
+                   ("llama8b_32k_b4", {}),
+                   ("llama8b_64k_criticalkv", {}))
+
+
 def run_decode_only(args, kv, W, dev):
     """flat_decode_attn alone, L2 flushed before each step, on a flat cache of the workload's
     shape whose head lengths are log-normal (--decode-sigma) around the workload's mean rows
@@ -457,6 +655,13 @@ def run_ours(args):
     import __graft_entry__
 
     rank, world, local = dist_env()
+    wl = W.WORKLOADS[args.workload]
+    if args.layers > 0:
+        wl = wl.with_(layers=args.layers)
+    # the CPU oracle first: its process pool is forked before this process touches the GPU
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.decode_only:
+        cpu = cpu_baseline(wl)
     if not torch.cuda.is_available():
         print(json.dumps({"error": "no CUDA device"}))
         return 1
@@ -472,9 +677,6 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
     __graft_entry__.build()
 
-    wl = W.WORKLOADS[args.workload]
-    if args.layers > 0:
-        wl = wl.with_(layers=args.layers)
     B, L = wl.batch, wl.layers
     seqs = rank_sequences(rank, B)
     shape = kv.KvShape.from_workload(wl)
@@ -779,33 +981,12 @@ def run_ours(args):
                 "algorithmic_bytes_per_launch": ab[dom]}
     crit_norm = None
     if wl.mode == "critical":
-        # The CriticalKV norm (tensor-bound) is the dominant kernel of kv_score here: its
-        # time is kv_score in CriticalKV mode minus kv_score in Ada mode on the same inputs.
-        def t_score(m, reps=3):
-            ts = []
-            for _ in range(reps + 1):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                kv.kv_score(shape, m, group, inp["q_win"], inp["k"], inp["v"],
-                            inp["w_o"] if m == kv.KV_SCORE_CRITICAL else None, wl.model_dim,
-                            scores, crit if m == kv.KV_SCORE_CRITICAL else None, w_s, stream)
-                e1.record(stream)
-                torch.cuda.synchronize(dev)
-                ts.append(e0.elapsed_time(e1))
-            return statistics.median(ts[1:])
-        t_crit, t_ada = t_score(kv.KV_SCORE_CRITICAL), t_score(kv.KV_SCORE_ADA)
-        flops = 2.0 * B * L * wl.hkv * C * wl.d * wl.model_dim
-        crit_ms = max(t_crit - t_ada, 1e-6)
-        tf = flops / (crit_ms / 1e3) / 1e12
-        tpeak, tkind = read_tensor_peak()
-        crit_norm = {"kernel": "crit_tc_kernel (||(V W_O)_j||_1 on tcgen05)", "ms": crit_ms,
-                     "flops": flops, "achieved": tf, "unit": "TFLOP/s", "peak": tpeak,
-                     "frac": tf / tpeak, "peak_kind": tkind,
-                     "how": "kv_score(CRITICAL) - kv_score(ADA) on the same inputs"}
-        roofline = {"kernel": crit_norm["kernel"], "bound": "tensor", "achieved": tf,
-                    "peak": tpeak, "unit": "TFLOP/s", "frac": tf / tpeak, "peak_kind": tkind,
-                    "traffic": None, "flops_per_launch": flops,
-                    "how": crit_norm["how"]}
+        crit_norm = time_crit_norm(kv, wl, shape, inp, crit, w_s, dev, stream)
+        roofline = {"kernel": crit_norm["kernel"], "bound": "tensor",
+                    "achieved": crit_norm["achieved"], "peak": crit_norm["peak"],
+                    "unit": "TFLOP/s", "frac": crit_norm["frac"],
+                    "peak_kind": crit_norm["peak_kind"], "traffic": None,
+                    "flops_per_launch": crit_norm["flops"], "how": crit_norm["how"]}
 
     # -------------------- end to end through host buffers --------------------
     e2e = None
@@ -857,15 +1038,18 @@ def run_ours(args):
                "steps": args.e2e_steps}
         del host
 
-    # -------------------- CPU oracle baseline --------------------
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        x = oracle_sample(wl, True)
-        t0 = time.perf_counter()
-        oracle_step(wl, x)
-        t_cpu = time.perf_counter() - t0
-        cpu = {"value": wl.n / (wl.hkv * t_cpu), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": sample_desc(wl), "seconds": t_cpu}
+    # -------------------- the pages' other configurations --------------------
+    others = None
+    if rank == 0 and world == 1 and not args.no_other_workloads and args.layers <= 0:
+        del step, inp, dec, scores, crit, kept, kf, vf, out, flush
+        torch.cuda.empty_cache()
+        others = []
+        for name, kw in OTHER_WORKLOADS:
+            if name == wl.name and not kw:
+                continue
+            others.append(measure_workload(kv, W, W.WORKLOADS[name].with_(**kw), dev, stream,
+                                           steps=min(args.steps, 10), warmup=3))
+    t_evict = stage_ms["score"] + stage_ms["allocate"] + stage_ms["compact"]
 
     if rank == 0:
         line = {
@@ -893,6 +1077,9 @@ def run_ours(args):
             },
             "eager_ms_per_step": eager_ms,
             "stages_ms": stage_ms,
+            "eviction_only": {"value": aggregate_value(world, B, wl.n, L, t_evict),
+                              "unit": UNIT, "ms": t_evict,
+                              "how": "score + allocate + compact stage times (eager)"},
             "decode_attn": {"value": dec_gbs, "unit": "GB/s", "frac": dec_gbs / peak,
                             "peak": peak, "steps": len(dts), "ms_per_step": statistics.mean(dts),
                             "bytes_per_step": statistics.mean(dbytes),
@@ -910,6 +1097,7 @@ def run_ours(args):
             "roofline": roofline,
             "crit_norm": crit_norm,
             "cpu_baseline": cpu,
+            "workloads": others,
             "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clk,

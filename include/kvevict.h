@@ -106,6 +106,24 @@ KV_API kv_status kv_score(const kv_shape* shape, int mode, int group,
                    void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * kv_crit_norm -- CriticalKV's projected-value norm on its own
+ * ("CriticalKV: Optimizing KV Cache Eviction from an Output Perturbation Perspective",
+ * key designs: the perturbation bound weighs each entry by the L1 norm of its value row
+ * projected through the output matrix).  The same values kv_score writes to crit_norm in
+ * KV_SCORE_CRITICAL mode, for callers that score with another mode first or time the two
+ * apart:  crit_norm[b][l][g][j] = || v[b][l][g][j] W_O[l][g] ||_1  for j < C.
+ *
+ * v         [B][L][Hkv][n][d]   dtype
+ * w_o       [L][Hkv][d][D]      dtype, model_dim = D (multiple of 8)
+ * crit_norm [B][L][Hkv][C]      float32 out
+ * ws        a workspace of at least kv_workspace_size(KV_OP_SCORE, shape) bytes (only its
+ *           error word is used; 256 bytes suffice)
+ */
+KV_API kv_status kv_crit_norm(const kv_shape* shape, const void* v, const void* w_o,
+                              int32_t model_dim, float* crit_norm, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/*
  * kv_allocate -- per-head budgets (Ada-KV Algorithm 1 + safeguard; LAVa layer budgets).
  *
  * layer_entropy_mode = 0: budget [B][L] int64 is the layer budget B including

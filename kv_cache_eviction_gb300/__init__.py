@@ -18,8 +18,8 @@ __all__ = [
     "KV_ERR_CUDA", "KV_ERR_DEVICE_CHECK", "KV_BF16", "KV_F32", "KV_SCORE_ADA", "KV_SCORE_LAVA",
     "KV_SCORE_CRITICAL", "KV_GROUP_MEAN", "KV_GROUP_MAX", "KV_OP_SCORE", "KV_OP_ALLOCATE",
     "KV_OP_COMPACT", "KV_OP_DECODE", "KvShape", "KvError", "lib", "library_path",
-    "kv_workspace_size", "kv_score", "kv_allocate", "kv_compact", "flat_decode_attn",
-    "kv_check_device_status", "kv_status_string", "kv_kernel_launches",
+    "kv_workspace_size", "kv_score", "kv_crit_norm", "kv_allocate", "kv_compact",
+    "flat_decode_attn", "kv_check_device_status", "kv_status_string", "kv_kernel_launches",
     "flat_decode_attn_noalloc",
 ]
 
@@ -66,6 +66,7 @@ _SIGS = {
     "kv_workspace_size": (_sz, [ctypes.c_int, ctypes.POINTER(KvShape)]),
     "kv_score": (ctypes.c_int, [ctypes.POINTER(KvShape), ctypes.c_int, ctypes.c_int, _vp, _vp, _vp,
                                 _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "kv_crit_norm": (ctypes.c_int, [ctypes.POINTER(KvShape), _vp, _vp, _i32, _vp, _vp, _sz, _vp]),
     "kv_allocate": (ctypes.c_int, [ctypes.POINTER(KvShape), _vp, _vp, ctypes.c_int, _u32, _u32,
                                    _vp, _vp, _vp, _sz, _vp]),
     "kv_compact": (ctypes.c_int, [ctypes.POINTER(KvShape), _vp, _vp, _vp, _vp, _u32, _u32, _f32,
@@ -142,6 +143,12 @@ def kv_score(shape: KvShape, mode: int, group: int, q_win, k, v, w_o, model_dim:
                         model_dim, _ptr(scores), _ptr(crit_norm), _ptr(ws), _nbytes(ws),
                         _stream(stream))
     _check("kv_score", st)
+
+
+def kv_crit_norm(shape: KvShape, v, w_o, model_dim: int, crit_norm, ws, stream=None) -> None:
+    st = lib().kv_crit_norm(ctypes.byref(shape), _ptr(v), _ptr(w_o), model_dim, _ptr(crit_norm),
+                            _ptr(ws), _nbytes(ws), _stream(stream))
+    _check("kv_crit_norm", st)
 
 
 def kv_allocate(shape: KvShape, scores, budget, layer_entropy_mode: int, alpha_num: int,

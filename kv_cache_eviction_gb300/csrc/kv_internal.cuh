@@ -50,6 +50,11 @@ cudaError_t launch_score(const Shape& s, int mode, int group, const void* q_win,
                          const void* v, const void* w_o, int D, float* scores, float* crit,
                          char* ws, const ScorePlan& p, cudaStream_t st);
 
+// CriticalKV's ||(V W_O)_j||_1 alone (tcgen05 kernel where the shape allows); `ws` is a
+// scoring workspace (only its error word is used).
+cudaError_t launch_crit_norm(const Shape& s, const void* v, const void* w_o, int D, float* crit,
+                             char* ws, cudaStream_t st);
+
 // After the tcgen05 scoring kernel: LAVa's V-bar factor (vbar != nullptr) and the keys whose
 // pooling window crosses a range boundary (from the halo copies of both ranges).
 cudaError_t launch_score_fixup(const float* halo, const float* vbar, int64_t units, int Pg,

@@ -143,6 +143,21 @@ kv_status kv_score(const kv_shape* shape, int mode, int group, const void* q_win
                                   static_cast<cudaStream_t>(stream)));
 }
 
+kv_status kv_crit_norm(const kv_shape* shape, const void* v, const void* w_o, int32_t model_dim,
+                       float* crit_norm, void* ws, size_t ws_bytes, void* stream) {
+  Shape s;
+  if (!shape_ok(shape, &s)) return KV_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned16(ws)) return KV_ERR_INVALID_ARG;
+  if (s.units() == 0 || s.C() <= 0) return KV_OK;
+  if (v == nullptr || w_o == nullptr || crit_norm == nullptr) return KV_ERR_INVALID_ARG;
+  if (!aligned16(v) || !aligned16(w_o) || !aligned16(crit_norm)) return KV_ERR_INVALID_ARG;
+  if (model_dim <= 0 || model_dim % 8 != 0) return KV_ERR_INVALID_ARG;
+  if (!shape_supported(s)) return KV_ERR_UNSUPPORTED;
+  if (ws_bytes < kWsHeader) return KV_ERR_WORKSPACE;
+  return cuda_status(launch_crit_norm(s, v, w_o, model_dim, crit_norm, static_cast<char*>(ws),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
 kv_status kv_allocate(const kv_shape* shape, const float* scores, const int64_t* budget,
                       int layer_entropy_mode, uint32_t alpha_num, uint32_t alpha_den,
                       int32_t* layer_budget, int32_t* head_budget, void* ws, size_t ws_bytes,

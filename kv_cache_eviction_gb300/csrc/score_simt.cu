@@ -349,6 +349,11 @@ cudaError_t launch_score(const Shape& s, int mode, int group, const void* q_win,
                                    (const float*)v, scores, ws, p, st);
   }
   if (e != cudaSuccess || mode != KV_SCORE_CRITICAL) return e;
+  return launch_crit_norm(s, v, w_o, D, crit, ws, st);
+}
+
+cudaError_t launch_crit_norm(const Shape& s, const void* v, const void* w_o, int D, float* crit,
+                             char* ws, cudaStream_t st) {
   if (crit_tc_supported(s, D) && !simt_forced())
     return launch_crit_tc(s, v, w_o, D, crit, ws, st);
   if (s.dtype == KV_BF16)

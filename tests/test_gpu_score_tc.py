@@ -114,3 +114,24 @@ def test_crit_norm_tc_matches_oracle(case):
             for path, c in crits.items():
                 assert_scores_close(c[b, l].astype(np.float64), ref,
                                     what="crit %s b%d l%d" % (path, b, l))
+
+
+def test_crit_norm_entry_equals_score_output():
+    """kv_crit_norm alone writes exactly what kv_score writes to crit_norm in CriticalKV
+    mode (the same kernel), and matches the oracle."""
+    import oracle as O
+    wl = W.Workload(name="critnorm", batch=1, layers=2, hq=8, hkv=2, d=128, n=1000, w=32, pool=7,
+                    dtype="bf16", temp=(0.5, 16.0), mode="critical", head_budget_frac=0.4,
+                    model_dim=520, seed=21)
+    shape = kv.KvShape.from_workload(wl)
+    inp = W.make_batch(wl, device="cuda")
+    _, c_score = run_score(wl, shape, inp)
+    c_alone = torch.full_like(c_score, float("nan"))
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    kv.kv_crit_norm(shape, inp["v"], inp["w_o"], wl.model_dim, c_alone, ws)
+    assert kv.kv_check_device_status(ws) == 0
+    assert torch.equal(c_alone, c_score)
+    C = wl.n - wl.w
+    for l in range(wl.layers):
+        ref = O.critical_row_norm(np64(inp["v"][0, l]), np64(inp["w_o"][l]), C)
+        assert_scores_close(c_alone[0, l].double().cpu().numpy(), ref, what="crit l%d" % l)

@@ -66,7 +66,7 @@ def test_two_ranks_max_time_disjoint_sequences_and_value():
     assert s0 == [0, 1, 2] and s1 == [3, 4, 5]
     # ... with different inputs (per-sequence seeds)
     assert g0 == g1 and g0[0] != g0[1]
-    # whole-job value: both ranks' tokens over the slowest time
+    # whole-job value: both ranks' tokens over the slowest time (per layer: L = 1 here)
     assert v0 == v1 == pytest.approx(2 * 3 * 512 * 1 / (2.75 / 1e3))
 
 
