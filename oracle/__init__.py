@@ -4,3 +4,4 @@ TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
 baseline legs of ``bench.py`` import it; the library never does.
 """
 from .kvevict_oracle import *  # noqa: F401,F403
+from .kvevict_next import capped_split, lava_cascade, layer_top_from_held  # noqa: F401
