@@ -155,6 +155,37 @@ KV_API kv_status kv_allocate(const kv_shape* shape, const float* scores, const i
                       void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * kv_allocate_capped -- LAVa layer budgets with a ceiling per layer, for the online
+ * layer-wise prefill ("LAVa: Layer-wise KV Cache Eviction with Dynamic Budget Allocation",
+ * online prefill and layer budget adjustment: after layer l is prefilled, the layers below
+ * it are compressed again with the same scores and budgets that shrink as more layers
+ * share the memory).
+ *
+ * The entropy split of kv_allocate's layer_entropy_mode = 1 over the L layers of `shape`,
+ * except that layer l keeps at most layer_cap[b][l] rows (window included): a layer whose
+ * proportional share exceeds its cap is fixed at the cap and the rest re-split, floors plus
+ * largest remainders as before.  When the layers cannot hold the selectable total together,
+ * every layer keeps its cap (no device check).  Then the per-head counts and the blend with
+ * alpha as in kv_allocate (LAVa: alpha = 0).
+ *
+ * Stage t of the cascade (layers 0..t-1 prefilled, B = 1): shape.layers = t, scores of
+ * layers 0..t-1 (contiguous), budget [1] the sequence's total, layer_cap [t] the previous
+ * stage's layer_budget for layers 0..t-2 and at least Hkv*n for layer t-1.  layer_cap and
+ * layer_budget must not be the same array (the caps are read while budgets are written).
+ *
+ * scores       [B][L][Hkv][C] float32
+ * budget       [B] int64 total per sequence (all windows included)
+ * layer_cap    [B][L] int32
+ * layer_budget [B][L] int32 out, head_budget [B][L][Hkv] int32 out (B_g + w)
+ * ws           a kv_workspace_size(KV_OP_ALLOCATE, shape) workspace
+ */
+KV_API kv_status kv_allocate_capped(const kv_shape* shape, const float* scores,
+                                    const int64_t* budget, const int32_t* layer_cap,
+                                    uint32_t alpha_num, uint32_t alpha_den,
+                                    int32_t* layer_budget, int32_t* head_budget,
+                                    void* ws, size_t ws_bytes, void* stream);
+
+/*
  * kv_compact -- per-head Top-B_g selection and the flat cache gather
  * (Ada-KV Algorithm 2, selection and concatenation of the window; the flat
  * layout that concatenates every head of a layer into one tensor;
@@ -190,6 +221,53 @@ KV_API kv_status kv_compact(const kv_shape* shape, const void* k, const void* v,
                      int32_t* kept_idx, int64_t* cu_off, int32_t* lens,
                      void* k_flat, void* v_flat, int64_t flat_capacity_rows,
                      void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * kv_recompact -- a smaller per-head Top-B_g chosen among the rows a flat cache still holds,
+ * gathered into another flat buffer (LAVa, online prefill and layer budget adjustment: the
+ * layers already compressed are compressed again with the same scores; Ada-KV Algorithm 2's
+ * per-head selection and window).
+ *
+ * Source: a flat cache as kv_compact / kv_recompact write it (src_kept, src_cu, src_lens,
+ * src_k, src_v; head h holds src_lens[h] rows from src_cu), or, with src_kept, src_cu and
+ * src_lens all NULL, the uncompacted K/V [B][L][Hkv][n][d] (head h holds all n positions).
+ * For every head: a row whose position p (its src_kept entry) is a candidate, 0 <= p < C,
+ * competes by (scores[b][l][g][p] desc, p asc); every other row -- the window positions
+ * C..n-1, and rows with no position (-1, e.g. decode appends) -- is always kept.  The head
+ * keeps head_budget[h] rows in all (at most the rows it holds, at least its forced rows),
+ * in source order (ascending positions), and they are gathered with their positions.
+ *
+ * Since Top-B sets of one total order are nested, re-selecting a smaller budget among the
+ * rows kept by an earlier selection on the same scores gives the same rows as selecting
+ * among all candidates.
+ *
+ * Output layout as in kv_compact, starting at row *row_base (row_base a device pointer to
+ * one int64, 16-byte alignment not required, 8 bytes required; NULL = row 0): head h owns
+ * rows [cu_off[h], cu_off[h] + lens[h] + reserve).  Pointing row_base at the last cu_off
+ * entry of an earlier call appends after that call's rows without a host round trip.
+ *
+ * scores     [B][L][Hkv][C] float32
+ * head_budget[B][L][Hkv] int32 (kv_allocate / kv_allocate_capped's head_budget)
+ * src_capacity_rows: rows of src_k / src_v (ignored for the uncompacted source)
+ * kept_idx, cu_off [B][L][Hkv+1], lens, k_flat, v_flat: outputs; k_flat / v_flat must not be
+ *   the source buffers (the source is read while the output is written)
+ * ws         at least kv_recompact_workspace_size(src rows) bytes (src rows = B*L*Hkv*n for
+ *            the uncompacted source), zeroed once before its first use
+ * head_budget out of range sets DEV check 4 (clamped); rows past flat_capacity_rows set
+ * check 2 and are not written.  Modes without a second stage only (no CriticalKV norm).
+ * Alignment: src_k, src_v, k_flat, v_flat 16 bytes; the tables only their element's
+ * (scores, head_budget, src_kept, src_lens, kept_idx, lens 4 bytes; src_cu, cu_off,
+ * row_base 8 bytes), so that one layer's slice of a [B][L] table can be passed.
+ */
+KV_API size_t kv_recompact_workspace_size(int64_t src_capacity_rows);
+KV_API kv_status kv_recompact(const kv_shape* shape, const float* scores,
+                              const int32_t* head_budget, const int32_t* src_kept,
+                              const int64_t* src_cu, const int32_t* src_lens,
+                              const void* src_k, const void* src_v, int64_t src_capacity_rows,
+                              int32_t reserve, const int64_t* row_base, int32_t* kept_idx,
+                              int64_t* cu_off, int32_t* lens, void* k_flat, void* v_flat,
+                              int64_t flat_capacity_rows, void* ws, size_t ws_bytes,
+                              void* stream);
 
 /*
  * flat_decode_attn -- one decode step of attention over the flat cache

@@ -18,7 +18,8 @@ __all__ = [
     "KV_ERR_CUDA", "KV_ERR_DEVICE_CHECK", "KV_BF16", "KV_F32", "KV_SCORE_ADA", "KV_SCORE_LAVA",
     "KV_SCORE_CRITICAL", "KV_GROUP_MEAN", "KV_GROUP_MAX", "KV_OP_SCORE", "KV_OP_ALLOCATE",
     "KV_OP_COMPACT", "KV_OP_DECODE", "KvShape", "KvError", "lib", "library_path",
-    "kv_workspace_size", "kv_score", "kv_crit_norm", "kv_allocate", "kv_compact",
+    "kv_workspace_size", "kv_score", "kv_crit_norm", "kv_allocate", "kv_allocate_capped",
+    "kv_compact", "kv_recompact", "kv_recompact_workspace_size",
     "flat_decode_attn", "kv_check_device_status", "kv_status_string", "kv_kernel_launches",
     "flat_decode_attn_noalloc",
 ]
@@ -67,6 +68,12 @@ _SIGS = {
     "kv_score": (ctypes.c_int, [ctypes.POINTER(KvShape), ctypes.c_int, ctypes.c_int, _vp, _vp, _vp,
                                 _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
     "kv_crit_norm": (ctypes.c_int, [ctypes.POINTER(KvShape), _vp, _vp, _i32, _vp, _vp, _sz, _vp]),
+    "kv_allocate_capped": (ctypes.c_int, [ctypes.POINTER(KvShape), _vp, _vp, _vp, _u32, _u32,
+                                          _vp, _vp, _vp, _sz, _vp]),
+    "kv_recompact_workspace_size": (_sz, [_i64]),
+    "kv_recompact": (ctypes.c_int, [ctypes.POINTER(KvShape), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                    _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _sz,
+                                    _vp]),
     "kv_allocate": (ctypes.c_int, [ctypes.POINTER(KvShape), _vp, _vp, ctypes.c_int, _u32, _u32,
                                    _vp, _vp, _vp, _sz, _vp]),
     "kv_compact": (ctypes.c_int, [ctypes.POINTER(KvShape), _vp, _vp, _vp, _vp, _u32, _u32, _f32,
@@ -157,6 +164,34 @@ def kv_allocate(shape: KvShape, scores, budget, layer_entropy_mode: int, alpha_n
                            alpha_num, alpha_den, _ptr(layer_budget), _ptr(head_budget), _ptr(ws),
                            _nbytes(ws), _stream(stream))
     _check("kv_allocate", st)
+
+
+def kv_allocate_capped(shape: KvShape, scores, budget, layer_cap, alpha_num: int, alpha_den: int,
+                       layer_budget, head_budget, ws, stream=None) -> None:
+    st = lib().kv_allocate_capped(ctypes.byref(shape), _ptr(scores), _ptr(budget),
+                                  _ptr(layer_cap), alpha_num, alpha_den, _ptr(layer_budget),
+                                  _ptr(head_budget), _ptr(ws), _nbytes(ws), _stream(stream))
+    _check("kv_allocate_capped", st)
+
+
+def kv_recompact_workspace_size(src_capacity_rows: int) -> int:
+    return int(lib().kv_recompact_workspace_size(src_capacity_rows))
+
+
+def kv_recompact(shape: KvShape, scores, head_budget, src_kept, src_cu, src_lens, src_k, src_v,
+                 reserve: int, row_base, kept_idx, cu_off, lens, k_flat, v_flat, ws,
+                 stream=None, src_capacity_rows=None, flat_capacity_rows=None) -> None:
+    """src_kept / src_cu / src_lens None: the source is the uncompacted K/V."""
+    src_cap = src_k.shape[0] if src_capacity_rows is None else src_capacity_rows
+    if src_kept is None:
+        src_cap = 0
+    cap = k_flat.shape[0] if flat_capacity_rows is None else flat_capacity_rows
+    st = lib().kv_recompact(ctypes.byref(shape), _ptr(scores), _ptr(head_budget), _ptr(src_kept),
+                            _ptr(src_cu), _ptr(src_lens), _ptr(src_k), _ptr(src_v), src_cap,
+                            reserve, _ptr(row_base), _ptr(kept_idx), _ptr(cu_off), _ptr(lens),
+                            _ptr(k_flat), _ptr(v_flat), cap, _ptr(ws), _nbytes(ws),
+                            _stream(stream))
+    _check("kv_recompact", st)
 
 
 def kv_compact(shape: KvShape, k, v, scores, crit_norm, crit_alpha_num: int, crit_alpha_den: int,

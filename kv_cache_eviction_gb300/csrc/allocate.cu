@@ -201,13 +201,17 @@ constexpr int kMaxLayers = 1024;
 struct SplitSmem {
   double e[kMaxLayers], frac[kMaxLayers];
   int64_t sel[kMaxLayers];   // -1: active; >= 0: capped at that value
+  int64_t cap[kMaxLayers];   // most selectable rows the layer can keep
   double red_d[kWarps];
   long long red_i[kWarps];
   int64_t mine;
 };
+// layer_cap (nullable) [B][L]: the most rows (window included) layer l may keep; the
+// layer's selectable share is capped at it as well as at Hkv * C.  With caps, a total that
+// the layers cannot hold together leaves every layer at its cap.
 __device__ int64_t lava_layer_share(SplitSmem& sm, const double2* part, int nch, int L, int Hkv,
                                     int n, int w, int C, int64_t total, int b, int lme,
-                                    WsHeader* hdr) {
+                                    const int32_t* layer_cap, WsHeader* hdr) {
   for (int l = threadIdx.x; l < L; l += blockDim.x) {
     double S = 0.0, T = 0.0;
     const double2* p = part + ((int64_t)b * L + l) * nch;
@@ -220,12 +224,24 @@ __device__ int64_t lava_layer_share(SplitSmem& sm, const double2* part, int nch,
     if (S > 0.0) el = (log(S) - T / S) / ((double)Hkv * (double)n);
     sm.e[l] = el > 0.0 ? el : 0.0;
     sm.sel[l] = -1;
+    int64_t cl = (int64_t)Hkv * C;
+    if (layer_cap != nullptr) {
+      const int64_t given = (int64_t)layer_cap[(int64_t)b * L + l] - (int64_t)w * Hkv;
+      cl = given < 0 ? 0 : given < cl ? given : cl;
+    }
+    sm.cap[l] = cl;
   }
-  const int64_t cap = (int64_t)Hkv * C;
+  long long capsum = 0;
+  for (int l = threadIdx.x; l < L; l += blockDim.x) capsum += sm.cap[l];
+  capsum = block_sum_ll(capsum, sm.red_i);   // also a barrier: every cap is in place
   int64_t R = total - (int64_t)L * w * Hkv;
-  if (R < 0 || R > (int64_t)L * cap) {
+  if (R < 0 || (layer_cap == nullptr && R > (int64_t)capsum)) {
     if (threadIdx.x == 0 && lme == 0) raise_dev(hdr, DEV_BUDGET_RANGE, (unsigned)b);
-    R = R < 0 ? 0 : (int64_t)L * cap;
+    R = R < 0 ? 0 : (int64_t)capsum;
+  }
+  if (R >= (int64_t)capsum) {   // the layers keep all they can
+    __syncthreads();
+    return sm.cap[lme];
   }
   // a thread reads and writes only its own layers' e/sel/frac until the ranks below
   int64_t rem = R;
@@ -239,18 +255,22 @@ __device__ int64_t lava_layer_share(SplitSmem& sm, const double2* part, int nch,
       }
     const double esum = block_sum_dbl(es, sm.red_d);
     const long long active = block_sum_ll(na, sm.red_i);
-    long long nover = 0;
+    long long nover = 0, capped = 0;
     for (int l = threadIdx.x; l < L; l += blockDim.x) {
       if (sm.sel[l] >= 0) continue;
       const double q = esum > 0.0 ? (double)rem * sm.e[l] / esum : (double)rem / (double)active;
       sm.frac[l] = q;
-      if (q > (double)cap) ++nover;
+      if (q > (double)sm.cap[l]) {
+        ++nover;
+        capped += sm.cap[l];
+      }
     }
     nover = block_sum_ll(nover, sm.red_i);
+    capped = block_sum_ll(capped, sm.red_i);
     if (nover == 0 || active == 0) break;
     for (int l = threadIdx.x; l < L; l += blockDim.x)
-      if (sm.sel[l] < 0 && sm.frac[l] > (double)cap) sm.sel[l] = cap;
-    rem -= (int64_t)nover * cap;
+      if (sm.sel[l] < 0 && sm.frac[l] > (double)sm.cap[l]) sm.sel[l] = sm.cap[l];
+    rem -= (int64_t)capped;
   }
   long long used = 0;
   for (int l = threadIdx.x; l < L; l += blockDim.x) {
@@ -283,7 +303,8 @@ __device__ int64_t lava_layer_share(SplitSmem& sm, const double2* part, int nch,
 // group maximum (2048 when B' == 0: no candidates).
 __global__ void __launch_bounds__(kThreads)
 alloc_bound(const double2* __restrict__ part, int nch, int L, int Hkv, int n, int w, int C,
-            const int64_t* __restrict__ budget, int entropy, int32_t* __restrict__ layer_budget,
+            const int64_t* __restrict__ budget, int entropy, const int32_t* __restrict__ layer_cap,
+            int32_t* __restrict__ layer_budget,
             int64_t* __restrict__ bprime, const uint32_t* __restrict__ ghist,
             uint32_t* __restrict__ gbin, WsHeader* hdr) {
   __shared__ SplitSmem sm;
@@ -293,7 +314,7 @@ alloc_bound(const double2* __restrict__ part, int nch, int L, int Hkv, int n, in
   int64_t Bp;
   if (entropy) {
     const int b = (int)(seg / L), lme = (int)(seg - (int64_t)b * L);
-    Bp = lava_layer_share(sm, part, nch, L, Hkv, n, w, C, budget[b], b, lme, hdr);
+    Bp = lava_layer_share(sm, part, nch, L, Hkv, n, w, C, budget[b], b, lme, layer_cap, hdr);
   } else {
     Bp = budget[seg] - (int64_t)w * Hkv;
     if (Bp < 0 || Bp > N) {
@@ -623,9 +644,9 @@ AllocPlan alloc_plan(const Shape& s) {
 }
 
 cudaError_t launch_allocate(const Shape& s, const float* scores, const int64_t* budget,
-                            int entropy_mode, uint32_t an, uint32_t ad, int32_t* layer_budget,
-                            int32_t* head_budget, char* ws, const AllocPlan& p,
-                            cudaStream_t st) {
+                            int entropy_mode, const int32_t* layer_cap, uint32_t an, uint32_t ad,
+                            int32_t* layer_budget, int32_t* head_budget, char* ws,
+                            const AllocPlan& p, cudaStream_t st) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   const int64_t S = s.segments();
   if (S <= 0) return cudaSuccess;
@@ -668,8 +689,8 @@ cudaError_t launch_allocate(const Shape& s, const float* scores, const int64_t* 
   else
     alloc_sweep1<false><<<sweep, kThreads, kRingBytes, st>>>(scores, N, nch, part, ghist, hdr);
   alloc_bound<<<(unsigned)S, kThreads, 0, st>>>(part, nch, s.L, s.Hkv, s.n, s.w, C, budget,
-                                                entropy_mode, layer_budget, bprime, ghist, gbin,
-                                                hdr);
+                                                entropy_mode, layer_cap, layer_budget, bprime,
+                                                ghist, gbin, hdr);
   count_launches(2);
   // sweep 2 is a cooperative launch (the CTAs of a layer wait for one another), over as many
   // layers at a time as can be resident

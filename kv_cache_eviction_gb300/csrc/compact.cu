@@ -35,33 +35,6 @@ constexpr int kGatherThreads = 256;
 constexpr uint32_t kNoBin = 0xFFFFFFFFu;
 }
 
-// 64-bit inclusive block scan (one value per thread).
-__device__ __forceinline__ int64_t block_incl_scan64(int64_t v, int64_t* scratch, int64_t* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int64_t x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) scratch[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int64_t s = lane < nw ? scratch[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int64_t y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    if (lane < nw) scratch[lane] = s;
-  }
-  __syncthreads();
-  const int64_t base = warp > 0 ? scratch[warp - 1] : 0;
-  *total = scratch[nw - 1];
-  __syncthreads();
-  return base + x;
-}
-
 // Offsets of every head in the flat buffer and the initial lengths.
 __global__ void __launch_bounds__(kScanThreads)
 compact_offsets(const int32_t* __restrict__ head_budget, int64_t H, int Hkv, int w, int n,

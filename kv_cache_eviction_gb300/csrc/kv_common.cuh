@@ -106,6 +106,34 @@ __device__ __forceinline__ unsigned int block_incl_scan(unsigned int v, unsigned
   return base + x;
 }
 
+// 64-bit inclusive block scan (one value per thread, blockDim.x a multiple of 32, at most
+// 1024); *total receives the block's sum.  Ends with a barrier.
+__device__ __forceinline__ int64_t block_incl_scan64(int64_t v, int64_t* scratch, int64_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t s = lane < nw ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < nw) scratch[lane] = s;
+  }
+  __syncthreads();
+  const int64_t base = warp > 0 ? scratch[warp - 1] : 0;
+  *total = scratch[nw - 1];
+  __syncthreads();
+  return base + x;
+}
+
 // Histogram update of one bin per lane (0xFFFFFFFF = none) with runs of equal bins in
 // adjacent lanes merged into one add (max-pooled scores come in plateaus, so equal keys
 // sit next to each other; other repeats fall back to the atomic unit).  Warps with no

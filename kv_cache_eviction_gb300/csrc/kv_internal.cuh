@@ -68,9 +68,11 @@ struct AllocPlan {
   size_t off_bprime, off_epart, off_gbin, off_zero, off_union, off_end;
 };
 AllocPlan alloc_plan(const Shape& s);
+// layer_cap (nullable, entropy mode only): [B][L] the most rows each layer may keep.
 cudaError_t launch_allocate(const Shape& s, const float* scores, const int64_t* budget,
-                            int entropy_mode, uint32_t an, uint32_t ad, int32_t* layer_budget,
-                            int32_t* head_budget, char* ws, const AllocPlan& p, cudaStream_t st);
+                            int entropy_mode, const int32_t* layer_cap, uint32_t an, uint32_t ad,
+                            int32_t* layer_budget, int32_t* head_budget, char* ws,
+                            const AllocPlan& p, cudaStream_t st);
 
 // ----------------------------- compaction ----------------------------------
 struct CompactPlan {
@@ -83,6 +85,19 @@ cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const f
                            const int32_t* head_budget, int reserve, int32_t* kept,
                            int64_t* cu, int32_t* lens, void* kf, void* vf, int64_t cap,
                            char* ws, const CompactPlan& p, cudaStream_t st);
+
+// ----------------------------- re-compaction --------------------------------
+// Workspace of kv_recompact: the header, then one int32 per source row (the rows each head
+// keeps, listed at the head's own source offsets).
+size_t recompact_ws_bytes(int64_t src_rows);
+// src_kept == nullptr: the source is the uncompacted [B][L][Hkv][n][d] K/V (head h's rows
+// [h*n, (h+1)*n) hold positions 0..n-1); src_rows = its row count either way.
+cudaError_t launch_recompact(const Shape& s, const float* scores, const int32_t* head_budget,
+                             const int32_t* src_kept, const int64_t* src_cu,
+                             const int32_t* src_lens, const void* src_k, const void* src_v,
+                             int64_t src_rows, int reserve, const int64_t* row_base,
+                             int32_t* kept, int64_t* cu, int32_t* lens, void* kf, void* vf,
+                             int64_t cap, char* ws, cudaStream_t st);
 
 // ----------------------------- decode --------------------------------------
 struct DecodePlan {

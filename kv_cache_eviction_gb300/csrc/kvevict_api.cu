@@ -176,7 +176,31 @@ kv_status kv_allocate(const kv_shape* shape, const float* scores, const int64_t*
   if (!shape_supported(s) || (layer_entropy_mode && s.L > 1024)) return KV_ERR_UNSUPPORTED;
   const AllocPlan p = alloc_plan(s);
   if (ws_bytes < p.off_end) return KV_ERR_WORKSPACE;
-  return cuda_status(launch_allocate(s, scores, budget, layer_entropy_mode, alpha_num, alpha_den,
+  return cuda_status(launch_allocate(s, scores, budget, layer_entropy_mode, nullptr, alpha_num,
+                                     alpha_den, layer_budget, head_budget,
+                                     static_cast<char*>(ws), p,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+kv_status kv_allocate_capped(const kv_shape* shape, const float* scores, const int64_t* budget,
+                             const int32_t* layer_cap, uint32_t alpha_num, uint32_t alpha_den,
+                             int32_t* layer_budget, int32_t* head_budget, void* ws,
+                             size_t ws_bytes, void* stream) {
+  Shape s;
+  if (!shape_ok(shape, &s)) return KV_ERR_INVALID_ARG;
+  if (alpha_den == 0 || alpha_num > alpha_den || alpha_den > 65536u) return KV_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned16(ws)) return KV_ERR_INVALID_ARG;
+  if (s.units() == 0) return KV_OK;
+  if (scores == nullptr || budget == nullptr || layer_cap == nullptr || layer_budget == nullptr ||
+      head_budget == nullptr)
+    return KV_ERR_INVALID_ARG;
+  if (!aligned16(scores) || !aligned16(budget) || !aligned16(layer_cap) ||
+      !aligned16(layer_budget) || !aligned16(head_budget))
+    return KV_ERR_INVALID_ARG;
+  if (!shape_supported(s) || s.L > 1024) return KV_ERR_UNSUPPORTED;
+  const AllocPlan p = alloc_plan(s);
+  if (ws_bytes < p.off_end) return KV_ERR_WORKSPACE;
+  return cuda_status(launch_allocate(s, scores, budget, 1, layer_cap, alpha_num, alpha_den,
                                      layer_budget, head_budget, static_cast<char*>(ws), p,
                                      static_cast<cudaStream_t>(stream)));
 }
@@ -240,6 +264,52 @@ static kv_status decode_check(const kv_shape* shape, const void* q, const void* 
   if (!shape_supported(*s) || s->G() * s->d > 1024) return KV_ERR_UNSUPPORTED;
   *p = decode_plan(*s);
   return KV_OK;
+}
+
+size_t kv_recompact_workspace_size(int64_t src_capacity_rows) {
+  if (src_capacity_rows < 0) return 0;
+  return recompact_ws_bytes(src_capacity_rows);
+}
+
+kv_status kv_recompact(const kv_shape* shape, const float* scores, const int32_t* head_budget,
+                       const int32_t* src_kept, const int64_t* src_cu, const int32_t* src_lens,
+                       const void* src_k, const void* src_v, int64_t src_capacity_rows,
+                       int32_t reserve, const int64_t* row_base, int32_t* kept_idx,
+                       int64_t* cu_off, int32_t* lens, void* k_flat, void* v_flat,
+                       int64_t flat_capacity_rows, void* ws, size_t ws_bytes, void* stream) {
+  Shape s;
+  if (!shape_ok(shape, &s)) return KV_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned16(ws)) return KV_ERR_INVALID_ARG;
+  if (reserve < 0 || flat_capacity_rows < 0 || src_capacity_rows < 0) return KV_ERR_INVALID_ARG;
+  if (s.units() == 0) return KV_OK;
+  const bool full = src_kept == nullptr;   // the source is the uncompacted K/V
+  if (full != (src_cu == nullptr) || full != (src_lens == nullptr)) return KV_ERR_INVALID_ARG;
+  if (scores == nullptr || head_budget == nullptr || src_k == nullptr || src_v == nullptr ||
+      kept_idx == nullptr || cu_off == nullptr || lens == nullptr || k_flat == nullptr ||
+      v_flat == nullptr)
+    return KV_ERR_INVALID_ARG;
+  // the rows move as 16-byte vectors; every table is read and written element by element,
+  // so slices of per-layer tables need only their element's alignment
+  const void* rows[] = {src_k, src_v, k_flat, v_flat};
+  for (const void* x : rows)
+    if (!aligned16(x)) return KV_ERR_INVALID_ARG;
+  auto al = [](const void* x, uintptr_t a) {
+    return x == nullptr || (reinterpret_cast<uintptr_t>(x) & (a - 1)) == 0;
+  };
+  if (!al(scores, 4) || !al(head_budget, 4) || !al(src_kept, 4) || !al(src_cu, 8) ||
+      !al(src_lens, 4) || !al(row_base, 8) || !al(kept_idx, 4) || !al(cu_off, 8) ||
+      !al(lens, 4))
+    return KV_ERR_INVALID_ARG;
+  if (src_k == k_flat || src_v == v_flat) return KV_ERR_INVALID_ARG;
+  if (!shape_supported(s)) return KV_ERR_UNSUPPORTED;
+  const int64_t src_rows = full ? s.units() * (int64_t)s.n : src_capacity_rows;
+  if (src_rows >= ((int64_t)1 << 31)) return KV_ERR_UNSUPPORTED;
+  if (ws_bytes < recompact_ws_bytes(src_rows)) return KV_ERR_WORKSPACE;
+  return cuda_status(launch_recompact(s, scores, head_budget, src_kept, src_cu, src_lens, src_k,
+                                      src_v, src_rows, reserve, row_base, kept_idx, cu_off, lens,
+                                      k_flat, v_flat, flat_capacity_rows,
+                                      static_cast<char*>(ws),
+                                      static_cast<cudaStream_t>(stream)));
 }
 
 kv_status flat_decode_attn(const kv_shape* shape, const void* q, const void* k_new,
