@@ -13,6 +13,15 @@ Pages (cited by title and section):
   compressed again with the same LAVa scores and budgets that shrink as more layers share
   the memory), uncertainty-based layer budgets, head-flattened layer eviction.
 
+* "CriticalKV: Optimizing KV Cache Eviction from an Output Perturbation Perspective" -- key
+  designs: the bound weighs entry i by ||(V W^O)_{i,:}||_1 per head, and the two-stage
+  greedy selection (top alpha*b by A, then the rest by (A_i + eps) * ||(V W^O)_i||_1);
+  "Ada-KV" notes, efficiency section, GQA: the mean over a group as the criterion.
+* "Reformulating KV cache eviction for long-context LLM inference" (LaProx) -- Eqs. 2-4
+  (the output is the sum of the heads' contributions A^(h) V^(h) W_O^(h)) and Algorithm 1:
+  p[i] = ||A[:, i]||_2 * ||H[i, :]||_2 with A the window's attention rows and H = V W_O,
+  the last w entries always kept, then one TopK over the budget B_total.
+
 Readings taken where the pages are silent:
 
 * Stage t (t = 1..L) starts when layer t-1 has been prefilled and scored.  The total
@@ -25,6 +34,19 @@ Readings taken where the pages are silent:
   stage L reproduces the one-shot split.
 * Each layer then keeps its head-flattened top B'_l (alpha = 0, the order (score desc, head
   asc, position asc)) chosen among the rows it still holds; the window rows stay.
+* GQA-exact CriticalKV: W^O is split per query head (the [d, D] block of head q's rows of
+  the model's output projection), so KV head g's rows meet G different blocks.  The
+  composite score of query head q is (A_q[i] + eps) * ||(V_g W^O_q)_i||_1 with A_q that
+  head's pooled window mean; the KV head's score is their mean over the group (Ada-KV's
+  GQA criterion).  Stage 1 stays the Ada-KV score (group mean of A_q).  With one W^O block
+  shared by the group this is exactly the per-KV-head form (s + eps) * ||(V W^O)_i||_1.
+* LaProx under GQA: the output is a sum over query heads, so KV head g's entry i carries
+  sum_{q in g} ||A_q[:, i]||_2 * ||(V_g W^O_q)_i||_2 (the bound of the Frobenius norm of
+  the entry's contribution to the window's outputs; one term for MHA, as on the page).
+  ||A_q[:, i]||_2 is over the w window rows with no pooling (Algorithm 1 prints none).
+  B_total is the whole model's budget with every window included; TopK runs over every
+  candidate of every layer and KV head at once (the page's model-wide selection), ties by
+  (layer, head, position) ascending.
 """
 from __future__ import annotations
 
@@ -34,7 +56,7 @@ from typing import List, Sequence
 
 import numpy as np
 
-from .kvevict_oracle import layer_entropy
+from .kvevict_oracle import global_topk_counts, layer_entropy, max_pool, window_attention
 
 
 def capped_split(e: Sequence[float], R: int, caps: Sequence[int]) -> np.ndarray:
@@ -137,3 +159,104 @@ def lava_cascade(S: Sequence[np.ndarray], total: int, w: int, n: int) -> List[di
             "caps_bound": bool(np.any(sel != uncapped)),
         })
     return stages
+
+
+# ----------------------------------------------------------------------------
+# Per-query-head terms: CriticalKV with one W^O block per query head, and LaProx.
+# ----------------------------------------------------------------------------
+
+def window_head_terms(q_win: np.ndarray, k: np.ndarray, w: int, pool: int, kind: str,
+                      scale=None) -> np.ndarray:
+    """The window term of every query head for every candidate j < C, before any group
+    reduction.  q_win [Hq, w, d], k [Hkv, n, d] -> [Hq, C].
+
+    ``mean_pool``: max_pool(window mean of P_q) -- Ada-KV's per-head score (Algorithm 2);
+    ``l2``:        sqrt(sum_t P_q[t, j]^2) -- LaProx's ||A[:, j]||_2, no pooling.
+    P is the causal window attention over all n keys (as for the Ada-KV scores).
+    """
+    n, d = k.shape[1], k.shape[2]
+    C = n - w
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    P = window_attention(q_win, k, scale)
+    if kind == "mean_pool":
+        return max_pool(P[:, :, :C].mean(axis=1), pool) if C > 0 else np.zeros((len(P), 0))
+    if kind == "l2":
+        return np.sqrt((P[:, :, :C] ** 2).sum(axis=1))
+    raise ValueError(kind)
+
+
+def head_proj_norm(v: np.ndarray, w_o_q: np.ndarray, C: int, p: int) -> np.ndarray:
+    """||(V_g W^O_q)_j||_p for every query head q (KV head g = q // G) and j < C.
+
+    v [Hkv, n, d], w_o_q [Hq, d, D] -> [Hq, C]."""
+    hkv = v.shape[0]
+    hq = w_o_q.shape[0]
+    G = hq // hkv
+    out = np.empty((hq, C))
+    for q in range(hq):
+        proj = v[q // G, :C].astype(np.float64) @ w_o_q[q].astype(np.float64)
+        if p == 1:
+            out[q] = np.abs(proj).sum(axis=1)
+        elif p == 2:
+            out[q] = np.sqrt((proj ** 2).sum(axis=1))
+        else:
+            raise ValueError(p)
+    return out
+
+
+def gqa_critical_kappa(terms: np.ndarray, v: np.ndarray, w_o_q: np.ndarray, eps: float
+                       ) -> np.ndarray:
+    """CriticalKV's stage-2 key with one W^O block per query head, group mean:
+    kappa[g, j] = (1/G) sum_{q in g} (A_q[j] + eps) * ||(V_g W^O_q)_j||_1.
+    terms [Hq, C] (window_head_terms 'mean_pool') -> [Hkv, C]."""
+    hq, C = terms.shape
+    hkv = v.shape[0]
+    G = hq // hkv
+    c = head_proj_norm(v, w_o_q, C, 1)
+    kap = np.zeros((hkv, C))
+    for q in range(hq):
+        kap[q // G] += (terms[q] + eps) * c[q]
+    return kap / G
+
+
+def laprox_score(terms: np.ndarray, v: np.ndarray, w_o_q: np.ndarray) -> np.ndarray:
+    """LaProx's entry score, per KV head: p[g, j] = sum_{q in g} ||A_q[:, j]||_2 *
+    ||(V_g W^O_q)_j||_2.  terms [Hq, C] (window_head_terms 'l2') -> [Hkv, C]."""
+    hq, C = terms.shape
+    hkv = v.shape[0]
+    G = hq // hkv
+    h = head_proj_norm(v, w_o_q, C, 2)
+    p = np.zeros((hkv, C))
+    for q in range(hq):
+        p[q // G] += terms[q] * h[q]
+    return p
+
+
+def laprox_head_budgets(P: Sequence[np.ndarray], total: int, w: int) -> np.ndarray:
+    """LaProx's model-wide TopK: the top (total - L*w*Hkv) candidates over every layer's
+    every KV head at once (order: score desc, then layer, head, position ascending), counted
+    per (layer, head).  P[l] [Hkv, C].  Returns the kept rows per (layer, head) [L, Hkv],
+    window included."""
+    L = len(P)
+    hkv, C = P[0].shape
+    Bp = total - L * w * hkv
+    if Bp < 0 or Bp > L * hkv * C:
+        raise ValueError("total budget out of range")
+    f = global_topk_counts(np.concatenate([np.asarray(x, dtype=np.float64) for x in P]), Bp)
+    return f.reshape(L, hkv) + w
+
+
+def critical_positions_kappa(sg: np.ndarray, kg: np.ndarray, k: int, a: int, b: int
+                             ) -> np.ndarray:
+    """CriticalKV's two-stage selection with the stage-2 key given: floor(a/b * k) by the
+    score s, then the rest of the candidates by kappa (desc, position asc); ascending."""
+    C = len(sg)
+    k1 = (a * k) // b
+    order1 = np.lexsort((np.arange(C), -sg))
+    first = order1[:k1]
+    mask = np.ones(C, dtype=bool)
+    mask[first] = False
+    rest = np.nonzero(mask)[0]
+    order2 = np.lexsort((rest, -np.asarray(kg, dtype=np.float64)[rest]))
+    return np.sort(np.concatenate([first, rest[order2[:k - k1]]]))
