@@ -70,6 +70,8 @@ typedef enum { KV_BF16 = 0, KV_F32 = 1 } kv_dtype;
 typedef enum { KV_SCORE_ADA = 0, KV_SCORE_LAVA = 1, KV_SCORE_CRITICAL = 2 } kv_score_mode;
 typedef enum { KV_GROUP_MEAN = 0, KV_GROUP_MAX = 1 } kv_group_reduce;
 typedef enum { KV_OP_SCORE = 0, KV_OP_ALLOCATE = 1, KV_OP_COMPACT = 2, KV_OP_DECODE = 3 } kv_op;
+typedef enum { KV_TERMS_MEAN_POOLED = 0, KV_TERMS_L2 = 1 } kv_terms_kind;
+typedef enum { KV_PROJ_CRIT_GQA = 0, KV_PROJ_LAPROX = 1 } kv_proj_kind;
 
 /* Shape of one eviction problem: B sequences x L layers of one model. */
 typedef struct {
@@ -124,10 +126,52 @@ KV_API kv_status kv_crit_norm(const kv_shape* shape, const void* v, const void* 
                               void* stream);
 
 /*
+ * kv_window_terms -- every query head's observation-window term, before any reduction over
+ * its group: the per-query-head inputs of the scores below that need one W_O block per
+ * query head.  For every (b, l, query head q) and candidate j < C, with P the causal window
+ * attention of kv_score:
+ *   KV_TERMS_MEAN_POOLED: max-pool (width pool) of (1/w) sum_t P[q,t,j]  -- the per-head
+ *       score of Ada-KV Algorithm 2 (kv_score's KV_GROUP_MEAN is its group mean);
+ *   KV_TERMS_L2: sqrt(sum_t P[q,t,j]^2), no pooling -- ||A[:, j]||_2 of LaProx Algorithm 1.
+ * q_win [B][L][Hq][w][d], k [B][L][Hkv][n][d]; terms [B][L][Hq][C] float32 out.
+ * ws: a kv_workspace_size(KV_OP_SCORE, shape) workspace.  CUDA-core kernels.
+ */
+KV_API kv_status kv_window_terms(const kv_shape* shape, int kind, const void* q_win,
+                                 const void* k, float* terms, void* ws, size_t ws_bytes,
+                                 void* stream);
+
+/*
+ * kv_proj_score -- a score per KV head and candidate from the value rows projected through
+ * one W_O block per query head ([L][Hq][d][D]: query head q's rows of the output
+ * projection), each query head weighted by its window term (kv_window_terms):
+ *   KV_PROJ_CRIT_GQA: out[g][j] = (1/G) sum_{q in g} (terms[q][j] + eps) * ||v[g][j] W_O[q]||_1
+ *       -- CriticalKV's stage-2 key (A_j + eps) * ||(V W^O)_j||_1 ("CriticalKV", two-stage
+ *       greedy selection) with W^O split per query head and Ada-KV's group mean over GQA;
+ *       terms of kind KV_TERMS_MEAN_POOLED.  Feed it to kv_compact_kappa.
+ *   KV_PROJ_LAPROX: out[g][j] = sum_{q in g} terms[q][j] * ||v[g][j] W_O[q]||_2 (eps unused)
+ *       -- LaProx's p[i] = ||A[:, i]||_2 * ||H[i, :]||_2, H = V W_O (Algorithm 1), summed over
+ *       the group's query heads; terms of kind KV_TERMS_L2.  Select with kv_allocate
+ *       (layer_entropy_mode 2, alpha 0) and kv_compact.
+ * v [B][L][Hkv][n][d], w_o [L][Hq][d][D] (model_dim = D, a multiple of 8), terms
+ * [B][L][Hq][C], out [B][L][Hkv][C] float32.  tcgen05 kernel: bf16, d = 128 only (others
+ * KV_ERR_UNSUPPORTED).  ws: 256 bytes (the error word).
+ */
+KV_API kv_status kv_proj_score(const kv_shape* shape, int kind, const void* v, const void* w_o,
+                               int32_t model_dim, const float* terms, float eps, float* out,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/*
  * kv_allocate -- per-head budgets (Ada-KV Algorithm 1 + safeguard; LAVa layer budgets).
  *
  * layer_entropy_mode = 0: budget [B][L] int64 is the layer budget B including
  *   the w*Hkv window rows.  B' = B - w*Hkv must lie in [0, Hkv*C].
+ * layer_entropy_mode = 2: budget [B] int64 is one total over the L layers of a
+ *   sequence (all windows included), selected model-wide ("Reformulating KV cache
+ *   eviction for long-context LLM inference" (LaProx), Algorithm 1: one TopK over every
+ *   head of every layer): the top total - L*w*Hkv candidates of all L*Hkv heads at once
+ *   by (score desc, layer asc, head asc, position asc), counted per head, then the blend
+ *   with alpha over all L*Hkv heads (LaProx: alpha = 0).  layer_budget[b][l] is the sum
+ *   of layer l's head budgets.  Needs L*Hkv <= 256 and L*Hkv*n < 2^31.
  * layer_entropy_mode = 1: budget [B] int64 is one total over the L layers of a
  *   sequence (including all windows).  Each layer's selectable share of
  *   R = total - L*w*Hkv is proportional to its score entropy
@@ -221,6 +265,21 @@ KV_API kv_status kv_compact(const kv_shape* shape, const void* k, const void* v,
                      int32_t* kept_idx, int64_t* cu_off, int32_t* lens,
                      void* k_flat, void* v_flat, int64_t flat_capacity_rows,
                      void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * kv_compact_kappa -- kv_compact's CriticalKV two-stage selection with the stage-2 key
+ * given: stage 1 keeps the top floor(crit_alpha * B_g) by score, stage 2 the rest by
+ * kappa[b][l][g][j] itself (desc, position asc), for keys computed elsewhere such as
+ * kv_proj_score's KV_PROJ_CRIT_GQA.  Arguments, layout and checks as kv_compact, with kappa
+ * in crit_norm's place and no eps.
+ */
+KV_API kv_status kv_compact_kappa(const kv_shape* shape, const void* k, const void* v,
+                                  const float* scores, const float* kappa,
+                                  uint32_t crit_alpha_num, uint32_t crit_alpha_den,
+                                  const int32_t* head_budget, int32_t reserve,
+                                  int32_t* kept_idx, int64_t* cu_off, int32_t* lens,
+                                  void* k_flat, void* v_flat, int64_t flat_capacity_rows,
+                                  void* ws, size_t ws_bytes, void* stream);
 
 /*
  * kv_recompact -- a smaller per-head Top-B_g chosen among the rows a flat cache still holds,

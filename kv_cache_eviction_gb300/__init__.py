@@ -19,7 +19,9 @@ __all__ = [
     "KV_SCORE_CRITICAL", "KV_GROUP_MEAN", "KV_GROUP_MAX", "KV_OP_SCORE", "KV_OP_ALLOCATE",
     "KV_OP_COMPACT", "KV_OP_DECODE", "KvShape", "KvError", "lib", "library_path",
     "kv_workspace_size", "kv_score", "kv_crit_norm", "kv_allocate", "kv_allocate_capped",
-    "kv_compact", "kv_recompact", "kv_recompact_workspace_size",
+    "kv_compact", "kv_recompact", "kv_recompact_workspace_size", "kv_window_terms",
+    "kv_proj_score", "kv_compact_kappa", "KV_TERMS_MEAN_POOLED", "KV_TERMS_L2",
+    "KV_PROJ_CRIT_GQA", "KV_PROJ_LAPROX",
     "flat_decode_attn", "kv_check_device_status", "kv_status_string", "kv_kernel_launches",
     "flat_decode_attn_noalloc",
 ]
@@ -30,6 +32,8 @@ KV_BF16, KV_F32 = 0, 1
 KV_SCORE_ADA, KV_SCORE_LAVA, KV_SCORE_CRITICAL = 0, 1, 2
 KV_GROUP_MEAN, KV_GROUP_MAX = 0, 1
 KV_OP_SCORE, KV_OP_ALLOCATE, KV_OP_COMPACT, KV_OP_DECODE = 0, 1, 2, 3
+KV_TERMS_MEAN_POOLED, KV_TERMS_L2 = 0, 1
+KV_PROJ_CRIT_GQA, KV_PROJ_LAPROX = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -68,6 +72,13 @@ _SIGS = {
     "kv_score": (ctypes.c_int, [ctypes.POINTER(KvShape), ctypes.c_int, ctypes.c_int, _vp, _vp, _vp,
                                 _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
     "kv_crit_norm": (ctypes.c_int, [ctypes.POINTER(KvShape), _vp, _vp, _i32, _vp, _vp, _sz, _vp]),
+    "kv_window_terms": (ctypes.c_int, [ctypes.POINTER(KvShape), ctypes.c_int, _vp, _vp, _vp, _vp,
+                                       _sz, _vp]),
+    "kv_proj_score": (ctypes.c_int, [ctypes.POINTER(KvShape), ctypes.c_int, _vp, _vp, _i32, _vp,
+                                     _f32, _vp, _vp, _sz, _vp]),
+    "kv_compact_kappa": (ctypes.c_int, [ctypes.POINTER(KvShape), _vp, _vp, _vp, _vp, _u32, _u32,
+                                        _vp, _i32, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _sz,
+                                        _vp]),
     "kv_allocate_capped": (ctypes.c_int, [ctypes.POINTER(KvShape), _vp, _vp, _vp, _u32, _u32,
                                           _vp, _vp, _vp, _sz, _vp]),
     "kv_recompact_workspace_size": (_sz, [_i64]),
@@ -164,6 +175,30 @@ def kv_allocate(shape: KvShape, scores, budget, layer_entropy_mode: int, alpha_n
                            alpha_num, alpha_den, _ptr(layer_budget), _ptr(head_budget), _ptr(ws),
                            _nbytes(ws), _stream(stream))
     _check("kv_allocate", st)
+
+
+def kv_window_terms(shape: KvShape, kind: int, q_win, k, terms, ws, stream=None) -> None:
+    st = lib().kv_window_terms(ctypes.byref(shape), kind, _ptr(q_win), _ptr(k), _ptr(terms),
+                               _ptr(ws), _nbytes(ws), _stream(stream))
+    _check("kv_window_terms", st)
+
+
+def kv_proj_score(shape: KvShape, kind: int, v, w_o, model_dim: int, terms, eps: float, out, ws,
+                  stream=None) -> None:
+    st = lib().kv_proj_score(ctypes.byref(shape), kind, _ptr(v), _ptr(w_o), model_dim,
+                             _ptr(terms), eps, _ptr(out), _ptr(ws), _nbytes(ws), _stream(stream))
+    _check("kv_proj_score", st)
+
+
+def kv_compact_kappa(shape: KvShape, k, v, scores, kappa, crit_alpha_num: int,
+                     crit_alpha_den: int, head_budget, reserve: int, kept_idx, cu_off, lens,
+                     k_flat, v_flat, flat_capacity_rows: int, ws, stream=None) -> None:
+    st = lib().kv_compact_kappa(ctypes.byref(shape), _ptr(k), _ptr(v), _ptr(scores), _ptr(kappa),
+                                crit_alpha_num, crit_alpha_den, _ptr(head_budget), reserve,
+                                _ptr(kept_idx), _ptr(cu_off), _ptr(lens), _ptr(k_flat),
+                                _ptr(v_flat), flat_capacity_rows, _ptr(ws), _nbytes(ws),
+                                _stream(stream))
+    _check("kv_compact_kappa", st)
 
 
 def kv_allocate_capped(shape: KvShape, scores, budget, layer_cap, alpha_num: int, alpha_den: int,

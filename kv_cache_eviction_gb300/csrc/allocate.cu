@@ -716,4 +716,23 @@ cudaError_t launch_allocate(const Shape& s, const float* scores, const int64_t* 
   return cudaGetLastError();
 }
 
+// Per-layer sums of the head budgets of a model-wide selection (one thread per segment).
+__global__ void layer_sums(const int32_t* __restrict__ head_budget, int64_t segments, int Hkv,
+                           int32_t* __restrict__ layer_budget) {
+  const int64_t seg = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (seg >= segments) return;
+  int64_t t = 0;
+  for (int g = 0; g < Hkv; ++g) t += head_budget[seg * Hkv + g];
+  layer_budget[seg] = (int32_t)t;
+}
+
+cudaError_t launch_layer_sums(const int32_t* head_budget, int64_t segments, int Hkv,
+                              int32_t* layer_budget, cudaStream_t st) {
+  if (segments <= 0) return cudaSuccess;
+  layer_sums<<<(unsigned)cdiv(segments, (int64_t)256), 256, 0, st>>>(head_budget, segments, Hkv,
+                                                                     layer_budget);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 }  // namespace kv

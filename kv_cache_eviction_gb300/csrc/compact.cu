@@ -106,6 +106,7 @@ struct KappaSrc {            // CriticalKV stage 2: stage-1 positions are forced
   bool bits_mode;
   uint32_t tau1;             // otherwise stage 1 kept key > tau1, and key == tau1 at
   int pcut1;                 // positions <= pcut1
+  bool given;                // Cn already holds the stage-2 key (kappa itself)
   // stage-1 membership of position p with score s
   __device__ bool in1(int p, float s) const {
     if (p < 0 || p >= C) return false;
@@ -114,7 +115,7 @@ struct KappaSrc {            // CriticalKV stage 2: stage-1 positions are forced
     return k > tau1 || (k == tau1 && p <= pcut1);
   }
   __device__ uint32_t kappa_key(float s, float c) const {
-    return score_key(__fmul_rn(__fadd_rn(s, eps), c)) + 1u;
+    return score_key(given ? c : __fmul_rn(__fadd_rn(s, eps), c)) + 1u;
   }
   __device__ void keys(const float4& x, const float4& y, int pos0, uint32_t (&k)[4],
                        bool (&f)[4]) const {
@@ -500,7 +501,7 @@ __device__ uint32_t select_head(SelRing& R, HeadSelSmem& sm, unsigned char* ring
 template <bool CRIT>
 __global__ void __launch_bounds__(kSelThreads, 2)
 head_select(const float* __restrict__ scores, const float* __restrict__ crit, uint32_t can,
-            uint32_t cad, float ceps, const int32_t* __restrict__ lens,
+            uint32_t cad, float ceps, int kappa_given, const int32_t* __restrict__ lens,
             const int64_t* __restrict__ cu, int Hkv, int C, int w, int reserve,
             int32_t* __restrict__ kept, int64_t cap, uint32_t* __restrict__ flags, int64_t words,
             int32_t* __restrict__ gpos, uint32_t* __restrict__ gkey, int streaming,
@@ -527,7 +528,7 @@ head_select(const float* __restrict__ scores, const float* __restrict__ crit, ui
     const int64_t K1 = ((int64_t)can * Bg) / cad;
     const int64_t K2 = Bg - K1;
     const ScoreSrc src1{scores + flat0};
-    KappaSrc src2{scores + flat0, crit + flat0, F, ceps, C, false, 0u, -1};
+    KappaSrc src2{scores + flat0, crit + flat0, F, ceps, C, false, 0u, -1, kappa_given != 0};
     if (streaming) {
       // stage 1 yields its threshold and tie cut; stage 2 tests membership from the score
       __shared__ uint32_t tau1;
@@ -612,9 +613,9 @@ CompactPlan compact_plan(const Shape& s, bool critical) {
 
 cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const float* scores,
                            const float* crit, uint32_t can, uint32_t cad, float ceps,
-                           const int32_t* head_budget, int reserve, int32_t* kept,
-                           int64_t* cu, int32_t* lens, void* kf, void* vf, int64_t cap,
-                           char* ws, const CompactPlan& p, cudaStream_t st) {
+                           bool kappa_given, const int32_t* head_budget, int reserve,
+                           int32_t* kept, int64_t* cu, int32_t* lens, void* kf, void* vf,
+                           int64_t cap, char* ws, const CompactPlan& p, cudaStream_t st) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   const int64_t H = s.units();
   compact_offsets<<<1, kScanThreads, 0, st>>>(head_budget, H, s.Hkv, s.w, s.n, reserve, cap, cu,
@@ -650,7 +651,8 @@ cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const f
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(
-        &cfg, kern, scores, crit, can, cad, ceps, (const int32_t*)lens, (const int64_t*)cu, s.Hkv,
+        &cfg, kern, scores, crit, can, cad, ceps, kappa_given ? 1 : 0, (const int32_t*)lens,
+        (const int64_t*)cu, s.Hkv,
         C, s.w, reserve, kept, cap, reinterpret_cast<uint32_t*>(ws + p.off_flags), p.flag_words,
         gpos, gkey, streaming ? 1 : 0, hdr);
     if (e != cudaSuccess) return e;

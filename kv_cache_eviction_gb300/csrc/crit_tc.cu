@@ -69,10 +69,16 @@ __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo,
 
 struct CritParams {
   int C, D, NT;          // candidates per unit, model dim, D / 128 tiles
-  int LHkv;              // W_O blocks (layers x KV heads)
+  int LHkv;              // layers x KV heads
   int64_t units, pairs;  // units and 256-key items per unit
   float* crit;           // [units][C]
   WsHeader* hdr;
+  // Per query head (mode != 0): W_O holds one [d][D] block per query head, Gq of them per
+  // unit; the epilogue weighs query head q's norm by terms[unit][q][key] (+ eps) and sums,
+  // times `scale`.  mode 1: L1 norms (GQA-exact CriticalKV), mode 2: L2 norms (LaProx).
+  int mode, Gq;
+  const float* terms;    // [units][Gq][C]
+  float eps, scale;
 };
 
 __global__ void __launch_bounds__(kCThreads, 1)
@@ -131,7 +137,7 @@ crit_tc_kernel(const __grid_constant__ CUtensorMap vmap, const __grid_constant__
           tma_load_3d(A + h * kTile, &vmap, &tl->afull[ab], 0, key0 + 128 * h, (int)u);
           tma_load_3d(A + h * kTile + kBox, &vmap, &tl->afull[ab], 64, key0 + 128 * h, (int)u);
         }
-        for (int nt = 0; nt < p.NT; ++nt, ++gb) {
+        for (int nt = 0; nt < p.NT * p.Gq; ++nt, ++gb) {
           const int s = gb % kBStages;
           if (!mbar_wait(&tl->bempty[s], ((gb / kBStages) & 1) ^ 1) || *abort_flag) {
             ok = false;
@@ -140,8 +146,10 @@ crit_tc_kernel(const __grid_constant__ CUtensorMap vmap, const __grid_constant__
           ++bfill[s];
           mbar_arrive_expect_tx(&tl->bfull[s], kTile);
           unsigned char* B = smem + kOffB + s * kTile;
-          tma_load_3d(B, &wmap, &tl->bfull[s], nt * 128, 0, lg);
-          tma_load_3d(B + kBox, &wmap, &tl->bfull[s], nt * 128 + 64, 0, lg);
+          // tile nt: query head nt / NT of the unit's group, output columns (nt % NT) * 128
+          const int blk = lg * p.Gq + nt / p.NT, col = (nt % p.NT) * 128;
+          tma_load_3d(B, &wmap, &tl->bfull[s], col, 0, blk);
+          tma_load_3d(B + kBox, &wmap, &tl->bfull[s], col + 64, 0, blk);
         }
       }
       if (!ok) {
@@ -165,7 +173,7 @@ crit_tc_kernel(const __grid_constant__ CUtensorMap vmap, const __grid_constant__
         const int ab = li & 1;
         if (!mbar_wait(&tl->afull[ab], (li >> 1) & 1) || *abort_flag) { ok = false; break; }
         const uint32_t aaddr = smem_u32(smem + kOffA + ab * 2 * kTile);
-        for (int nt = 0; nt < p.NT; ++nt, ++gb, ++gt) {
+        for (int nt = 0; nt < p.NT * p.Gq; ++nt, ++gb, ++gt) {
           const int s = gb % kBStages, tb = gt & 1;
           if (!mbar_wait(&tl->bfull[s], (gb / kBStages) & 1) ||
               !mbar_wait(&tl->tempty[tb], ((gt >> 1) & 1) ^ 1) || *abort_flag) {
@@ -207,8 +215,8 @@ crit_tc_kernel(const __grid_constant__ CUtensorMap vmap, const __grid_constant__
     for (int64_t it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
       const int64_t u = it / p.pairs;
       const int key = (int)(it - u * p.pairs) * 256 + 128 * h + 32 * q + lane;
-      float acc0 = 0.f, acc1 = 0.f;
-      for (int nt = 0; nt < p.NT; ++nt, ++gt) {
+      float acc0 = 0.f, acc1 = 0.f, comb = 0.f;
+      for (int nt = 0; nt < p.NT * p.Gq; ++nt, ++gt) {
         const int tb = gt & 1;
         const bool landed = mbar_wait(&tl->tfull[tb], (gt >> 1) & 1) && !*abort_flag;
         if (__any_sync(0xffffffffu, !landed)) { ok = false; break; }   // the whole warp
@@ -219,18 +227,35 @@ crit_tc_kernel(const __grid_constant__ CUtensorMap vmap, const __grid_constant__
           uint32_t r[32];
           tmem_ld32(base + cq * 32, r);
           tmem_ld_wait(r);
+          if (p.mode == 2) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            acc0 += fabsf(__uint_as_float(r[c]));
-            acc1 += fabsf(__uint_as_float(r[c + 1]));
+            for (int c = 0; c < 32; c += 2) {
+              const float x0 = __uint_as_float(r[c]), x1 = __uint_as_float(r[c + 1]);
+              acc0 = fmaf(x0, x0, acc0);
+              acc1 = fmaf(x1, x1, acc1);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              acc0 += fabsf(__uint_as_float(r[c]));
+              acc1 += fabsf(__uint_as_float(r[c + 1]));
+            }
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tl->tempty[tb]);
+        if (p.mode != 0 && nt % p.NT == p.NT - 1) {
+          // query head nt / NT is complete: its weighted norm joins the key's sum
+          const int qh = nt / p.NT;
+          const float nrm = p.mode == 2 ? sqrtf(acc0 + acc1) : acc0 + acc1;
+          const float wt = key < p.C ? p.terms[(u * p.Gq + qh) * p.C + key] + p.eps : 0.f;
+          comb = fmaf(wt, nrm, comb);
+          acc0 = acc1 = 0.f;
+        }
       }
       if (!ok) break;
-      if (key < p.C) p.crit[u * p.C + key] = acc0 + acc1;
+      if (key < p.C) p.crit[u * p.C + key] = p.mode == 0 ? acc0 + acc1 : comb * p.scale;
     }
     if (!ok) {
       raise_dev(p.hdr, DEV_WAIT_TIMEOUT, 0x200u + 3);
@@ -280,12 +305,25 @@ bool crit_tc_supported(const Shape& s, int D) {
 
 cudaError_t launch_crit_tc(const Shape& s, const void* v, const void* w_o, int D, float* crit,
                            char* ws, cudaStream_t st) {
+  return launch_proj_tc(s, 0, v, w_o, D, nullptr, 0.f, crit, ws, st);
+}
+
+cudaError_t launch_proj_tc(const Shape& s, int mode, const void* v, const void* w_o, int D,
+                           const float* terms, float eps, float* crit, char* ws,
+                           cudaStream_t st) {
   const int64_t units = s.units();
+  const int Gq = mode == 0 ? 1 : s.G();
   CUtensorMap vm, wm;
   if (!make_map_3d(&vm, v, 128, (uint64_t)s.n, (uint64_t)units) ||
-      !make_map_3d(&wm, w_o, (uint64_t)D, 128, (uint64_t)s.L * s.Hkv))
+      !make_map_3d(&wm, w_o, (uint64_t)D, 128, (uint64_t)s.L * s.Hkv * Gq))
     return cudaErrorInvalidValue;
   CritParams prm{};
+  prm.mode = mode;
+  prm.Gq = Gq;
+  prm.terms = terms;
+  prm.eps = eps;
+  // GQA-exact CriticalKV: the group mean; LaProx: the sum over the group
+  prm.scale = mode == 1 ? 1.0f / (float)Gq : 1.0f;
   prm.C = s.C();
   prm.D = D;
   prm.NT = (int)cdiv(D, 128);

@@ -55,6 +55,18 @@ cudaError_t launch_score(const Shape& s, int mode, int group, const void* q_win,
 cudaError_t launch_crit_norm(const Shape& s, const void* v, const void* w_o, int D, float* crit,
                              char* ws, cudaStream_t st);
 
+// Every query head's window term (kind KV_TERMS_MEAN_POOLED or KV_TERMS_L2) into
+// terms [units][G][C]; `p` is the scoring plan of the shape (its LSE scratch is used).
+cudaError_t launch_window_terms(const Shape& s, int kind, const void* q_win, const void* k,
+                                float* terms, char* ws, const ScorePlan& p, cudaStream_t st);
+// The norm kernel with one W_O block per query head ([L][Hq][d][D]), each query head's norm
+// weighted by its window term (+ eps): mode 1 L1 norms, group mean (KV_PROJ_CRIT_GQA);
+// mode 2 L2 norms, group sum (KV_PROJ_LAPROX).  bf16, d = 128 (crit_tc_supported).
+bool crit_tc_supported(const Shape& s, int D);
+cudaError_t launch_proj_tc(const Shape& s, int mode, const void* v, const void* w_o, int D,
+                           const float* terms, float eps, float* out, char* ws,
+                           cudaStream_t st);
+
 // After the tcgen05 scoring kernel: LAVa's V-bar factor (vbar != nullptr) and the keys whose
 // pooling window crosses a range boundary (from the halo copies of both ranges).
 cudaError_t launch_score_fixup(const float* halo, const float* vbar, int64_t units, int Pg,
@@ -74,17 +86,22 @@ cudaError_t launch_allocate(const Shape& s, const float* scores, const int64_t* 
                             int32_t* layer_budget, int32_t* head_budget, char* ws,
                             const AllocPlan& p, cudaStream_t st);
 
+// layer_budget[seg] = sum over the segment's Hkv heads of head_budget.
+cudaError_t launch_layer_sums(const int32_t* head_budget, int64_t segments, int Hkv,
+                              int32_t* layer_budget, cudaStream_t st);
+
 // ----------------------------- compaction ----------------------------------
 struct CompactPlan {
   size_t off_flags, off_union, off_end;
   int64_t flag_words;   // per head, when CriticalKV stage-1 flags are needed
 };
 CompactPlan compact_plan(const Shape& s, bool critical);
+// kappa_given: crit holds the stage-2 key itself instead of ||(V W_O)_j||_1.
 cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const float* scores,
                            const float* crit, uint32_t can, uint32_t cad, float ceps,
-                           const int32_t* head_budget, int reserve, int32_t* kept,
-                           int64_t* cu, int32_t* lens, void* kf, void* vf, int64_t cap,
-                           char* ws, const CompactPlan& p, cudaStream_t st);
+                           bool kappa_given, const int32_t* head_budget, int reserve,
+                           int32_t* kept, int64_t* cu, int32_t* lens, void* kf, void* vf,
+                           int64_t cap, char* ws, const CompactPlan& p, cudaStream_t st);
 
 // ----------------------------- re-compaction --------------------------------
 // Workspace of kv_recompact: the header, then one int32 per source row (the rows each head

@@ -70,6 +70,17 @@ static bool shape_supported(const Shape& s) {
 
 static kv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KV_OK : KV_ERR_CUDA; }
 
+// The shape of a model-wide selection (kv_allocate layer_entropy_mode 2): the L layers of a
+// sequence as one layer of L * Hkv heads.  Scores [B][L][Hkv][C] and head budgets
+// [B][L][Hkv] already have that layout.  False when it exceeds the kernels' limits.
+static bool model_wide_shape(const Shape& s, Shape* m) {
+  *m = s;
+  m->L = 1;
+  m->Hq = s.Hq * s.L;
+  m->Hkv = s.Hkv * s.L;
+  return s.L > 0 && shape_supported(*m);
+}
+
 // Scratch of flat_decode_attn_noalloc: one fixed array per device, never allocated at run
 // time.  Host code must not pass the symbol itself to a kernel (on the host it names a
 // host-side stand-in); the device address comes from cudaGetSymbolAddress, looked up once
@@ -110,7 +121,15 @@ size_t kv_workspace_size(int op, const kv_shape* shape) {
       const ScorePlan b = score_plan(s, KV_SCORE_CRITICAL);
       return a.off_end > b.off_end ? a.off_end : b.off_end;
     }
-    case KV_OP_ALLOCATE: return alloc_plan(s).off_end;
+    case KV_OP_ALLOCATE: {
+      size_t need = alloc_plan(s).off_end;
+      Shape m;
+      if (model_wide_shape(s, &m)) {   // room for layer_entropy_mode 2 as well
+        const size_t w2 = alloc_plan(m).off_end + align_up((size_t)s.B * sizeof(int32_t), 256);
+        if (w2 > need) need = w2;
+      }
+      return need;
+    }
     case KV_OP_COMPACT: return compact_plan(s, true).off_end;
     case KV_OP_DECODE: return decode_plan(s).off_end;
     default: return 0;
@@ -164,7 +183,7 @@ kv_status kv_allocate(const kv_shape* shape, const float* scores, const int64_t*
                       void* stream) {
   Shape s;
   if (!shape_ok(shape, &s)) return KV_ERR_INVALID_ARG;
-  if (layer_entropy_mode != 0 && layer_entropy_mode != 1) return KV_ERR_INVALID_ARG;
+  if (layer_entropy_mode < 0 || layer_entropy_mode > 2) return KV_ERR_INVALID_ARG;
   if (alpha_den == 0 || alpha_num > alpha_den || alpha_den > 65536u) return KV_ERR_INVALID_ARG;
   if (ws == nullptr || !aligned16(ws)) return KV_ERR_INVALID_ARG;
   if (s.units() == 0) return KV_OK;
@@ -173,6 +192,21 @@ kv_status kv_allocate(const kv_shape* shape, const float* scores, const int64_t*
   if (!aligned16(scores) || !aligned16(budget) || !aligned16(layer_budget) ||
       !aligned16(head_budget))
     return KV_ERR_INVALID_ARG;
+  if (layer_entropy_mode == 2) {
+    // one selection over every layer of a sequence, then each layer's sum of head budgets
+    Shape m;
+    if (!shape_supported(s) || !model_wide_shape(s, &m)) return KV_ERR_UNSUPPORTED;
+    const AllocPlan pm = alloc_plan(m);
+    if (ws_bytes < pm.off_end + align_up((size_t)s.B * sizeof(int32_t), 256))
+      return KV_ERR_WORKSPACE;
+    char* w = static_cast<char*>(ws);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_allocate(m, scores, budget, 0, nullptr, alpha_num, alpha_den,
+                                    reinterpret_cast<int32_t*>(w + pm.off_end), head_budget, w,
+                                    pm, st);
+    if (e == cudaSuccess) e = launch_layer_sums(head_budget, s.segments(), s.Hkv, layer_budget, st);
+    return cuda_status(e);
+  }
   if (!shape_supported(s) || (layer_entropy_mode && s.L > 1024)) return KV_ERR_UNSUPPORTED;
   const AllocPlan p = alloc_plan(s);
   if (ws_bytes < p.off_end) return KV_ERR_WORKSPACE;
@@ -205,17 +239,16 @@ kv_status kv_allocate_capped(const kv_shape* shape, const float* scores, const i
                                      static_cast<cudaStream_t>(stream)));
 }
 
-kv_status kv_compact(const kv_shape* shape, const void* k, const void* v, const float* scores,
-                     const float* crit_norm, uint32_t crit_alpha_num, uint32_t crit_alpha_den,
-                     float crit_eps, const int32_t* head_budget, int32_t reserve,
-                     int32_t* kept_idx, int64_t* cu_off, int32_t* lens, void* k_flat,
-                     void* v_flat, int64_t flat_capacity_rows, void* ws, size_t ws_bytes,
-                     void* stream) {
-  Shape s;
-  if (!shape_ok(shape, &s)) return KV_ERR_INVALID_ARG;
+// Argument checks of a compaction (kv_compact, kv_compact_kappa): KV_OK or the error.
+static kv_status kv_compact_check(const Shape& s, const void* k, const void* v,
+                                  const float* scores, const float* crit_norm,
+                                  uint32_t crit_alpha_num, uint32_t crit_alpha_den,
+                                  float crit_eps, const int32_t* head_budget, int32_t reserve,
+                                  int32_t* kept_idx, int64_t* cu_off, int32_t* lens,
+                                  void* k_flat, void* v_flat, int64_t flat_capacity_rows,
+                                  void* ws) {
   if (ws == nullptr || !aligned16(ws)) return KV_ERR_INVALID_ARG;
   if (reserve < 0 || flat_capacity_rows < 0) return KV_ERR_INVALID_ARG;
-  if (s.units() == 0) return KV_OK;
   if (k == nullptr || v == nullptr || scores == nullptr || head_budget == nullptr ||
       kept_idx == nullptr || cu_off == nullptr || lens == nullptr || k_flat == nullptr ||
       v_flat == nullptr)
@@ -232,12 +265,92 @@ kv_status kv_compact(const kv_shape* shape, const void* k, const void* v, const 
   // The smallest flat buffer any valid budgets can need: every head keeps its window.
   if (flat_capacity_rows < s.units() * (int64_t)(s.w + reserve)) return KV_ERR_CAPACITY;
   if (!shape_supported(s)) return KV_ERR_UNSUPPORTED;
+  return KV_OK;
+}
+
+kv_status kv_compact(const kv_shape* shape, const void* k, const void* v, const float* scores,
+                     const float* crit_norm, uint32_t crit_alpha_num, uint32_t crit_alpha_den,
+                     float crit_eps, const int32_t* head_budget, int32_t reserve,
+                     int32_t* kept_idx, int64_t* cu_off, int32_t* lens, void* k_flat,
+                     void* v_flat, int64_t flat_capacity_rows, void* ws, size_t ws_bytes,
+                     void* stream) {
+  Shape s;
+  if (!shape_ok(shape, &s)) return KV_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned16(ws)) return KV_ERR_INVALID_ARG;
+  if (reserve < 0 || flat_capacity_rows < 0) return KV_ERR_INVALID_ARG;
+  if (s.units() == 0) return KV_OK;
+  const kv_status st = kv_compact_check(s, k, v, scores, crit_norm, crit_alpha_num,
+                                        crit_alpha_den, crit_eps, head_budget, reserve, kept_idx,
+                                        cu_off, lens, k_flat, v_flat, flat_capacity_rows, ws);
+  if (st != KV_OK) return st;
   const CompactPlan p = compact_plan(s, crit_norm != nullptr);
   if (ws_bytes < p.off_end) return KV_ERR_WORKSPACE;
   return cuda_status(launch_compact(s, k, v, scores, crit_norm, crit_alpha_num, crit_alpha_den,
-                                    crit_eps, head_budget, reserve, kept_idx, cu_off, lens,
-                                    k_flat, v_flat, flat_capacity_rows, static_cast<char*>(ws),
-                                    p, static_cast<cudaStream_t>(stream)));
+                                    crit_eps, false, head_budget, reserve, kept_idx, cu_off,
+                                    lens, k_flat, v_flat, flat_capacity_rows,
+                                    static_cast<char*>(ws), p,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+kv_status kv_compact_kappa(const kv_shape* shape, const void* k, const void* v,
+                           const float* scores, const float* kappa, uint32_t crit_alpha_num,
+                           uint32_t crit_alpha_den, const int32_t* head_budget, int32_t reserve,
+                           int32_t* kept_idx, int64_t* cu_off, int32_t* lens, void* k_flat,
+                           void* v_flat, int64_t flat_capacity_rows, void* ws, size_t ws_bytes,
+                           void* stream) {
+  if (kappa == nullptr) return KV_ERR_INVALID_ARG;
+  Shape s;
+  if (!shape_ok(shape, &s)) return KV_ERR_INVALID_ARG;
+  if (s.units() == 0) return KV_OK;
+  // the argument checks of kv_compact, with kappa in the norm's place
+  const kv_status st = kv_compact_check(s, k, v, scores, kappa, crit_alpha_num, crit_alpha_den,
+                                        0.0f, head_budget, reserve, kept_idx, cu_off, lens,
+                                        k_flat, v_flat, flat_capacity_rows, ws);
+  if (st != KV_OK) return st;
+  const CompactPlan p = compact_plan(s, true);
+  if (ws_bytes < p.off_end) return KV_ERR_WORKSPACE;
+  return cuda_status(launch_compact(s, k, v, scores, kappa, crit_alpha_num, crit_alpha_den, 0.0f,
+                                    true, head_budget, reserve, kept_idx, cu_off, lens, k_flat,
+                                    v_flat, flat_capacity_rows, static_cast<char*>(ws), p,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+kv_status kv_window_terms(const kv_shape* shape, int kind, const void* q_win, const void* k,
+                          float* terms, void* ws, size_t ws_bytes, void* stream) {
+  Shape s;
+  if (!shape_ok(shape, &s)) return KV_ERR_INVALID_ARG;
+  if (kind != KV_TERMS_MEAN_POOLED && kind != KV_TERMS_L2) return KV_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned16(ws)) return KV_ERR_INVALID_ARG;
+  if (s.units() == 0) return KV_OK;
+  if (s.n == 0 || s.w == 0) return KV_ERR_INVALID_ARG;
+  if (q_win == nullptr || k == nullptr || terms == nullptr) return KV_ERR_INVALID_ARG;
+  if (!aligned16(q_win) || !aligned16(k) || !aligned16(terms)) return KV_ERR_INVALID_ARG;
+  if (!shape_supported(s)) return KV_ERR_UNSUPPORTED;
+  const ScorePlan p = score_plan(s, KV_SCORE_ADA);
+  if (ws_bytes < p.off_end) return KV_ERR_WORKSPACE;
+  return cuda_status(launch_window_terms(s, kind, q_win, k, terms, static_cast<char*>(ws), p,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+kv_status kv_proj_score(const kv_shape* shape, int kind, const void* v, const void* w_o,
+                        int32_t model_dim, const float* terms, float eps, float* out, void* ws,
+                        size_t ws_bytes, void* stream) {
+  Shape s;
+  if (!shape_ok(shape, &s)) return KV_ERR_INVALID_ARG;
+  if (kind != KV_PROJ_CRIT_GQA && kind != KV_PROJ_LAPROX) return KV_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f) || std::isinf(eps)) return KV_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned16(ws)) return KV_ERR_INVALID_ARG;
+  if (s.units() == 0 || s.C() <= 0) return KV_OK;
+  if (v == nullptr || w_o == nullptr || terms == nullptr || out == nullptr)
+    return KV_ERR_INVALID_ARG;
+  if (!aligned16(v) || !aligned16(w_o) || !aligned16(terms) || !aligned16(out))
+    return KV_ERR_INVALID_ARG;
+  if (model_dim <= 0 || model_dim % 8 != 0) return KV_ERR_INVALID_ARG;
+  if (!shape_supported(s) || !crit_tc_supported(s, model_dim)) return KV_ERR_UNSUPPORTED;
+  if (ws_bytes < kWsHeader) return KV_ERR_WORKSPACE;
+  return cuda_status(launch_proj_tc(s, kind == KV_PROJ_CRIT_GQA ? 1 : 2, v, w_o, model_dim,
+                                    terms, kind == KV_PROJ_CRIT_GQA ? eps : 0.0f, out,
+                                    static_cast<char*>(ws), static_cast<cudaStream_t>(stream)));
 }
 
 // Argument checks of a decode step; on KV_OK, `s` and `p` hold its shape and workspace plan.

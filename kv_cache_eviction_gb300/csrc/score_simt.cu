@@ -93,7 +93,10 @@ __global__ void score_lse_combine(const float2* __restrict__ part, int nchunk, i
   }
 }
 
-template <typename T>
+// TERMS = 0: the KV head's score (window mean, pool, group mean or max, V-bar factor) into
+// scores[unit][C].  TERMS = 1: every query head's pooled window mean, TERMS = 2: every query
+// head's sqrt(sum_t P[t, j]^2) (no pooling: pool = 1), into scores[unit][G][C].
+template <typename T, int TERMS = 0>
 __global__ void __launch_bounds__(kThreads)
 score_pass2_simt(const T* __restrict__ q_win, const T* __restrict__ k,
                  const float* __restrict__ lse2, const float* __restrict__ vbar, int n, int w,
@@ -135,7 +138,8 @@ score_pass2_simt(const T* __restrict__ q_win, const T* __restrict__ k,
         const float* kr = Ks + lane * dp;
         float acc = 0.f;
         for (int c = 0; c < d; ++c) acc = fmaf(qr[c], kr[c], acc);
-        const float p = exp2f(acc * c2 - Ls[row]);
+        float p = exp2f(acc * c2 - Ls[row]);
+        if (TERMS == 2) p *= p;
 #pragma unroll
         for (int q = 0; q < kMaxG; ++q) accq[q] += (q == ql) ? p : 0.f;
       }
@@ -147,11 +151,21 @@ score_pass2_simt(const T* __restrict__ q_win, const T* __restrict__ k,
       for (int q = 0; q < G; ++q) {
         float s = 0.f;
         for (int ww = 0; ww < 8; ++ww) s += red[(ww * G + q) * 32 + lane];
-        if (j < e1) As[q * ext + (j - e0)] = s * inv_w;
+        if (j < e1) As[q * ext + (j - e0)] = TERMS == 2 ? sqrtf(s) : s * inv_w;
       }
     }
   }
   __syncthreads();
+  if (TERMS != 0) {
+    for (int idx = threadIdx.x; idx < G * (c1 - c0); idx += blockDim.x) {
+      const int q = idx / (c1 - c0), j = c0 + (idx - q * (c1 - c0));
+      const int lo = max(0, j - r), hi = min(C - 1, j + r);
+      float pm = -INFINITY;
+      for (int jj = lo; jj <= hi; ++jj) pm = fmaxf(pm, As[q * ext + (jj - e0)]);
+      scores[(unit * G + q) * C + j] = pm;
+    }
+    return;
+  }
   const float vb = vbar ? vbar[unit] : 1.0f;
   for (int j = c0 + threadIdx.x; j < c1; j += blockDim.x) {
     const int lo = max(0, j - r), hi = min(C - 1, j + r);
@@ -317,6 +331,47 @@ static cudaError_t launch_score_simt_t(const Shape& s, int mode, int group, cons
     count_launches(1);
   }
   return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_terms_simt_t(const Shape& s, int kind, const T* q_win, const T* k,
+                                      float* terms, char* ws, const ScorePlan& p,
+                                      cudaStream_t st) {
+  const int R = s.R(), d = s.d, n = s.n, w = s.w, C = s.C();
+  const int64_t units = s.units();
+  const float c2 = (1.0f / sqrtf((float)d)) * 1.4426950408889634f;
+  float2* part = reinterpret_cast<float2*>(ws + p.off_part);
+  float* lse2 = reinterpret_cast<float*>(ws + p.off_lse);
+  const size_t sm1 = (size_t)(R * d + 32 * (d + 1)) * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(score_pass1_simt<T>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1);
+  if (e != cudaSuccess) return e;
+  score_pass1_simt<T><<<dim3(p.nchunk1, (unsigned)units), kThreads, sm1, st>>>(
+      q_win, k, n, w, d, R, p.chunk1, p.nchunk1, c2, part);
+  score_lse_combine<<<(unsigned)units, 128, 0, st>>>(part, p.nchunk1, R, lse2);
+  count_launches(2);
+  if (C > 0) {
+    const int G = s.G();
+    const int pool = kind == KV_TERMS_L2 ? 1 : s.pool, r = pool / 2;
+    const size_t sm2 = (size_t)(R * d + 32 * (d + 1) + R + 8 * G * 32 + G * (p.chunk2 + 2 * r)) *
+                       sizeof(float);
+    auto kern = kind == KV_TERMS_L2 ? score_pass2_simt<T, 2> : score_pass2_simt<T, 1>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(p.nchunk2, (unsigned)units), kThreads, sm2, st>>>(
+        q_win, k, lse2, nullptr, n, w, d, G, pool, 0, p.chunk2, c2, terms);
+    count_launches(1);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_window_terms(const Shape& s, int kind, const void* q_win, const void* k,
+                                float* terms, char* ws, const ScorePlan& p, cudaStream_t st) {
+  if (s.dtype == KV_BF16)
+    return launch_terms_simt_t<__nv_bfloat16>(s, kind, (const __nv_bfloat16*)q_win,
+                                              (const __nv_bfloat16*)k, terms, ws, p, st);
+  return launch_terms_simt_t<float>(s, kind, (const float*)q_win, (const float*)k, terms, ws, p,
+                                    st);
 }
 
 template <typename T>

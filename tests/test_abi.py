@@ -92,7 +92,7 @@ def test_invalid_parameters_rejected_on_host(L):
     # alpha must be a fraction in [0, 1] with a denominator <= 65536
     for a, b in [(1, 0), (3, 2), (1, 1 << 20)]:
         assert L.kv_allocate(ctypes.byref(s), p, p, 0, a, b, p, p, p, 1 << 30, None) == 1
-    assert L.kv_allocate(ctypes.byref(s), p, p, 2, 1, 5, p, p, p, 1 << 30, None) == 1
+    assert L.kv_allocate(ctypes.byref(s), p, p, 3, 1, 5, p, p, p, 1 << 30, None) == 1
     # k_new without v_new
     assert L.flat_decode_attn(ctypes.byref(s), p, p, None, p, p, p, p, 1 << 20, 0.1, p, p,
                               1 << 30, None) == 1
