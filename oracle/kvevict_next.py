@@ -17,6 +17,10 @@ Pages (cited by title and section):
   designs: the bound weighs entry i by ||(V W^O)_{i,:}||_1 per head, and the two-stage
   greedy selection (top alpha*b by A, then the rest by (A_i + eps) * ||(V W^O)_i||_1);
   "Ada-KV" notes, efficiency section, GQA: the mean over a group as the criterion.
+* "Ada-KV" arXiv page, Parameters: the sliding-window baseline (StreamingLLM) keeps 4 sink
+  tokens and the most recent window's cache.
+* "CriticalKV" notes, limitations: how to re-select when new entries join the cache during
+  decoding (streaming, chunked prefill) is left open.
 * "Reformulating KV cache eviction for long-context LLM inference" (LaProx) -- Eqs. 2-4
   (the output is the sum of the heads' contributions A^(h) V^(h) W_O^(h)) and Algorithm 1:
   p[i] = ||A[:, i]||_2 * ||H[i, :]||_2 with A the window's attention rows and H = V W_O,
@@ -34,6 +38,14 @@ Readings taken where the pages are silent:
   stage L reproduces the one-shot split.
 * Each layer then keeps its head-flattened top B'_l (alpha = 0, the order (score desc, head
   asc, position asc)) chosen among the rows it still holds; the window rows stay.
+* StreamingLLM as a budget preset: head g keeps its first min(sinks, B_g) positions and the
+  B_g - that many most recent candidates before the window (the window itself always
+  stays): the recent window grows into the candidates to fill the same budget an adaptive
+  head would get.
+* Re-eviction during decoding: the rows appended by decode steps carry no prefill score;
+  they are the cache's newest tokens and stay, like the window.  To return to a smaller
+  budget, each head keeps its top prefill rows by the prefill scores among those it still
+  holds.
 * GQA-exact CriticalKV: W^O is split per query head (the [d, D] block of head q's rows of
   the model's output projection), so KV head g's rows meet G different blocks.  The
   composite score of query head q is (A_q[i] + eps) * ||(V_g W^O_q)_i||_1 with A_q that
@@ -260,3 +272,34 @@ def critical_positions_kappa(sg: np.ndarray, kg: np.ndarray, k: int, a: int, b: 
     rest = np.nonzero(mask)[0]
     order2 = np.lexsort((rest, -np.asarray(kg, dtype=np.float64)[rest]))
     return np.sort(np.concatenate([first, rest[order2[:k - k1]]]))
+
+
+# ----------------------------------------------------------------------------
+# Budget presets and re-eviction of a decoded cache.
+# ----------------------------------------------------------------------------
+
+def streaming_positions(C: int, k: int, sinks: int) -> np.ndarray:
+    """StreamingLLM's kept candidates of one head with budget k (window not included): the
+    first min(sinks, k) positions and the most recent k - min(sinks, k) before the window,
+    ascending."""
+    if k < 0 or k > C:
+        raise ValueError("budget out of range")
+    s = min(sinks, k)
+    return np.concatenate([np.arange(s), np.arange(C - (k - s), C)]).astype(np.int64)
+
+
+def reevict_rows(held: Sequence[int], s: np.ndarray, keep: int) -> np.ndarray:
+    """Re-eviction of one head of a flat cache: `held` lists the positions of its rows in row
+    order (-1 for a row appended by decoding, no prefill score; positions >= C are the
+    window).  Rows without a candidate position always stay; the rest compete by the
+    prefill score s (desc, position asc).  Returns the kept row indices, ascending; `keep`
+    rows in all."""
+    held = np.asarray(held, dtype=np.int64)
+    C = len(s)
+    cand = np.nonzero((held >= 0) & (held < C))[0]
+    forced = np.nonzero(~((held >= 0) & (held < C)))[0]
+    k = keep - len(forced)
+    if k < 0 or k > len(cand):
+        raise ValueError("budget out of range")
+    order = np.lexsort((held[cand], -np.asarray(s, dtype=np.float64)[held[cand]]))
+    return np.sort(np.concatenate([cand[order[:k]], forced]))
