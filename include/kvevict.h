@@ -267,6 +267,21 @@ KV_API kv_status kv_compact(const kv_shape* shape, const void* k, const void* v,
                      void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * kv_compact_streaming -- the sliding-window baseline as a budget preset (Ada-KV arXiv page,
+ * Parameters: StreamingLLM keeps 4 sink tokens and the most recent window's cache): head g
+ * keeps its first min(sinks, B_g) positions and the most recent B_g - min(sinks, B_g)
+ * candidates before the window, then the window C..n-1, in ascending order; no scores are
+ * read.  B_g = head_budget - w, as from kv_allocate (alpha = 1 gives the uniform per-head
+ * budgets of a fixed-window policy whatever the scores).  Layout, outputs and checks as
+ * kv_compact (sinks >= 0; the default of the page is 4).  ws: 256 bytes (error word).
+ */
+KV_API kv_status kv_compact_streaming(const kv_shape* shape, const void* k, const void* v,
+                                      int32_t sinks, const int32_t* head_budget, int32_t reserve,
+                                      int32_t* kept_idx, int64_t* cu_off, int32_t* lens,
+                                      void* k_flat, void* v_flat, int64_t flat_capacity_rows,
+                                      void* ws, size_t ws_bytes, void* stream);
+
+/*
  * kv_compact_kappa -- kv_compact's CriticalKV two-stage selection with the stage-2 key
  * given: stage 1 keeps the top floor(crit_alpha * B_g) by score, stage 2 the rest by
  * kappa[b][l][g][j] itself (desc, position asc), for keys computed elsewhere such as
@@ -298,7 +313,10 @@ KV_API kv_status kv_compact_kappa(const kv_shape* shape, const void* k, const vo
  *
  * Since Top-B sets of one total order are nested, re-selecting a smaller budget among the
  * rows kept by an earlier selection on the same scores gives the same rows as selecting
- * among all candidates.
+ * among all candidates.  On a cache that decode steps have appended to (their rows carry
+ * position -1), the same call is a re-eviction: the appended rows and the window stay, and
+ * the prefill rows make room by their prefill scores (CriticalKV notes, limitations: how to
+ * re-select as entries join the cache during decoding is left open there).
  *
  * Output layout as in kv_compact, starting at row *row_base (row_base a device pointer to
  * one int64, 16-byte alignment not required, 8 bytes required; NULL = row 0): head h owns

@@ -20,7 +20,8 @@ __all__ = [
     "KV_OP_COMPACT", "KV_OP_DECODE", "KvShape", "KvError", "lib", "library_path",
     "kv_workspace_size", "kv_score", "kv_crit_norm", "kv_allocate", "kv_allocate_capped",
     "kv_compact", "kv_recompact", "kv_recompact_workspace_size", "kv_window_terms",
-    "kv_proj_score", "kv_compact_kappa", "KV_TERMS_MEAN_POOLED", "KV_TERMS_L2",
+    "kv_proj_score", "kv_compact_kappa", "kv_compact_streaming", "KV_TERMS_MEAN_POOLED",
+    "KV_TERMS_L2",
     "KV_PROJ_CRIT_GQA", "KV_PROJ_LAPROX",
     "flat_decode_attn", "kv_check_device_status", "kv_status_string", "kv_kernel_launches",
     "flat_decode_attn_noalloc",
@@ -76,6 +77,8 @@ _SIGS = {
                                        _sz, _vp]),
     "kv_proj_score": (ctypes.c_int, [ctypes.POINTER(KvShape), ctypes.c_int, _vp, _vp, _i32, _vp,
                                      _f32, _vp, _vp, _sz, _vp]),
+    "kv_compact_streaming": (ctypes.c_int, [ctypes.POINTER(KvShape), _vp, _vp, _i32, _vp, _i32,
+                                            _vp, _vp, _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
     "kv_compact_kappa": (ctypes.c_int, [ctypes.POINTER(KvShape), _vp, _vp, _vp, _vp, _u32, _u32,
                                         _vp, _i32, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _sz,
                                         _vp]),
@@ -188,6 +191,16 @@ def kv_proj_score(shape: KvShape, kind: int, v, w_o, model_dim: int, terms, eps:
     st = lib().kv_proj_score(ctypes.byref(shape), kind, _ptr(v), _ptr(w_o), model_dim,
                              _ptr(terms), eps, _ptr(out), _ptr(ws), _nbytes(ws), _stream(stream))
     _check("kv_proj_score", st)
+
+
+def kv_compact_streaming(shape: KvShape, k, v, sinks: int, head_budget, reserve: int, kept_idx,
+                         cu_off, lens, k_flat, v_flat, flat_capacity_rows: int, ws,
+                         stream=None) -> None:
+    st = lib().kv_compact_streaming(ctypes.byref(shape), _ptr(k), _ptr(v), sinks,
+                                    _ptr(head_budget), reserve, _ptr(kept_idx), _ptr(cu_off),
+                                    _ptr(lens), _ptr(k_flat), _ptr(v_flat), flat_capacity_rows,
+                                    _ptr(ws), _nbytes(ws), _stream(stream))
+    _check("kv_compact_streaming", st)
 
 
 def kv_compact_kappa(shape: KvShape, k, v, scores, kappa, crit_alpha_num: int,

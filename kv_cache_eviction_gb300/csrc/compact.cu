@@ -668,4 +668,50 @@ cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const f
   return cudaGetLastError();
 }
 
+// StreamingLLM preset: head h keeps its first min(sinks, B_g) positions and the most recent
+// B_g - that many before the window, then the window C..n-1; reserve rows get -1.
+__global__ void __launch_bounds__(kGatherThreads)
+streaming_kept(const int64_t* __restrict__ cu, const int32_t* __restrict__ lens, int Hkv, int C,
+               int w, int sinks, int reserve, int64_t cap, int32_t* __restrict__ kept) {
+  const int64_t h = blockIdx.y;
+  const int64_t seg = h / Hkv;
+  const int g = (int)(h - seg * Hkv);
+  const int64_t base = cu[seg * (Hkv + 1) + g];
+  const int64_t Bg = (int64_t)lens[h] - w;   // lens was clamped to [w, n]
+  const int64_t sk = Bg < sinks ? Bg : sinks;
+  const int64_t total = Bg + w + reserve;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = base + i;
+    if (row < 0 || row >= cap) continue;
+    int64_t pos;
+    if (i < sk) pos = i;
+    else if (i < Bg) pos = C - (Bg - sk) + (i - sk);
+    else if (i < Bg + w) pos = C + (i - Bg);
+    else pos = -1;
+    kept[row] = (int32_t)pos;
+  }
+}
+
+cudaError_t launch_compact_streaming(const Shape& s, const void* k, const void* v, int sinks,
+                                     const int32_t* head_budget, int reserve, int32_t* kept,
+                                     int64_t* cu, int32_t* lens, void* kf, void* vf, int64_t cap,
+                                     char* ws, cudaStream_t st) {
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  const int64_t H = s.units();
+  compact_offsets<<<1, kScanThreads, 0, st>>>(head_budget, H, s.Hkv, s.w, s.n, reserve, cap, cu,
+                                               lens, hdr);
+  int gx = (int)cdiv((int64_t)num_sms() * 16, H);
+  if (gx < 1) gx = 1;
+  if (gx > 64) gx = 64;
+  streaming_kept<<<dim3(gx, (unsigned)H), kGatherThreads, 0, st>>>(cu, lens, s.Hkv, s.C(), s.w,
+                                                                    sinks, reserve, cap, kept);
+  const int row_bytes = s.d * s.esize();
+  compact_gather<<<dim3(gx, (unsigned)H), kGatherThreads, 0, st>>>(
+      (const char*)k, (const char*)v, kept, cu, lens, s.Hkv, s.n, row_bytes, cap, (char*)kf,
+      (char*)vf);
+  count_launches(3);
+  return cudaGetLastError();
+}
+
 }  // namespace kv

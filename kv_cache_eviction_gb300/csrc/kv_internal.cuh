@@ -103,6 +103,12 @@ cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const f
                            int32_t* kept, int64_t* cu, int32_t* lens, void* kf, void* vf,
                            int64_t cap, char* ws, const CompactPlan& p, cudaStream_t st);
 
+// StreamingLLM preset: sinks and the most recent candidates fill each head's budget.
+cudaError_t launch_compact_streaming(const Shape& s, const void* k, const void* v, int sinks,
+                                     const int32_t* head_budget, int reserve, int32_t* kept,
+                                     int64_t* cu, int32_t* lens, void* kf, void* vf, int64_t cap,
+                                     char* ws, cudaStream_t st);
+
 // ----------------------------- re-compaction --------------------------------
 // Workspace of kv_recompact: the header, then one int32 per source row (the rows each head
 // keeps, listed at the head's own source offsets).

@@ -292,6 +292,29 @@ kv_status kv_compact(const kv_shape* shape, const void* k, const void* v, const 
                                     static_cast<cudaStream_t>(stream)));
 }
 
+kv_status kv_compact_streaming(const kv_shape* shape, const void* k, const void* v,
+                               int32_t sinks, const int32_t* head_budget, int32_t reserve,
+                               int32_t* kept_idx, int64_t* cu_off, int32_t* lens, void* k_flat,
+                               void* v_flat, int64_t flat_capacity_rows, void* ws,
+                               size_t ws_bytes, void* stream) {
+  Shape s;
+  if (!shape_ok(shape, &s)) return KV_ERR_INVALID_ARG;
+  if (sinks < 0) return KV_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned16(ws)) return KV_ERR_INVALID_ARG;
+  if (reserve < 0 || flat_capacity_rows < 0) return KV_ERR_INVALID_ARG;
+  if (s.units() == 0) return KV_OK;
+  // the checks of kv_compact; the scores are not read (any aligned pointer will do)
+  const kv_status st = kv_compact_check(s, k, v, reinterpret_cast<const float*>(head_budget),
+                                        nullptr, 1, 2, 0.0f, head_budget, reserve, kept_idx,
+                                        cu_off, lens, k_flat, v_flat, flat_capacity_rows, ws);
+  if (st != KV_OK) return st;
+  if (ws_bytes < kWsHeader) return KV_ERR_WORKSPACE;
+  return cuda_status(launch_compact_streaming(s, k, v, sinks, head_budget, reserve, kept_idx,
+                                              cu_off, lens, k_flat, v_flat, flat_capacity_rows,
+                                              static_cast<char*>(ws),
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 kv_status kv_compact_kappa(const kv_shape* shape, const void* k, const void* v,
                            const float* scores, const float* kappa, uint32_t crit_alpha_num,
                            uint32_t crit_alpha_den, const int32_t* head_budget, int32_t reserve,
