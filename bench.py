@@ -487,6 +487,177 @@ def time_crit_norm(kv, wl, shape, inp, crit, ws, dev, stream, reps=5):
             "how": "kv_crit_norm alone between CUDA events, median of %d" % reps}
 
 
+def time_call(fn, dev, stream, reps=3):
+    """Median device time (ms) of fn() between CUDA events on `stream`, after one warm-up."""
+    import torch
+    ts = []
+    for _ in range(reps + 1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts[1:])
+
+
+def measure_per_query_head(kv, wl, shape, inp, scores, dev, stream):
+    """GQA-exact CriticalKV and LaProx on the workload's inputs, with one W_O block per query
+    head ([L][Hq][d][D], N(0, 1/D)): per-query-head window terms (CUDA cores), the projected
+    score on tcgen05 (2 * C * d * D flops per query head and unit, the dominant cost), then
+    the selection each uses (two-stage with kappa given; model-wide TopK and per-head
+    compaction).  Each call timed alone (median of 3)."""
+    import torch
+    B, L = shape.batch, shape.layers
+    C = wl.n - wl.w
+    D = wl.model_dim
+    g = torch.Generator(device=dev).manual_seed(0x9A0)
+    w_oq = (torch.randn(L, wl.hq, wl.d, D, device=dev, generator=g) / math.sqrt(D)).to(
+        wl.torch_dtype)
+    terms = torch.empty(B, L, wl.hq, C, device=dev)
+    out = torch.empty(B, L, wl.hkv, C, device=dev)
+    ws_s = torch.zeros(max(kv.kv_workspace_size(kv.KV_OP_SCORE, shape), 256), dtype=torch.uint8,
+                       device=dev)
+    ws_a = torch.zeros(max(kv.kv_workspace_size(kv.KV_OP_ALLOCATE, shape), 256),
+                       dtype=torch.uint8, device=dev)
+    ws_c = torch.zeros(max(kv.kv_workspace_size(kv.KV_OP_COMPACT, shape), 256), dtype=torch.uint8,
+                       device=dev)
+    tpeak, tkind = read_tensor_peak()
+    flops = 2.0 * B * L * wl.hq * C * wl.d * D
+    cap = wl.flat_capacity_rows()
+    kept = torch.empty(cap, dtype=torch.int32, device=dev)
+    cu = torch.empty(B, L, wl.hkv + 1, dtype=torch.int64, device=dev)
+    lens = torch.empty(B, L, wl.hkv, dtype=torch.int32, device=dev)
+    kf = torch.empty(cap, wl.d, dtype=wl.torch_dtype, device=dev)
+    vf = torch.empty_like(kf)
+    hb = torch.empty(B, L, wl.hkv, dtype=torch.int32, device=dev)
+    lb = torch.empty(B, L, dtype=torch.int32, device=dev)
+    budgets = wl.budgets().to(dev)
+    res = {}
+    for name, tk, pk in (("crit_gqa", kv.KV_TERMS_MEAN_POOLED, kv.KV_PROJ_CRIT_GQA),
+                         ("laprox", kv.KV_TERMS_L2, kv.KV_PROJ_LAPROX)):
+        t_terms = time_call(lambda: kv.kv_window_terms(shape, tk, inp["q_win"], inp["k"], terms,
+                                                       ws_s, stream), dev, stream)
+        t_proj = time_call(lambda: kv.kv_proj_score(shape, pk, inp["v"], w_oq, D, terms,
+                                                    wl.crit_eps, out, ws_s, stream), dev, stream)
+        tf = flops / (t_proj / 1e3) / 1e12
+        r = {"terms_ms": t_terms, "proj_ms": t_proj, "proj_tflops": tf, "proj_frac": tf / tpeak,
+             "peak_kind": tkind, "proj_flops": flops,
+             "proj_kernel": "crit_tc_kernel, one W_O block per query head"}
+        if name == "crit_gqa":
+            kv.kv_allocate(shape, scores, budgets, 0, wl.alpha[0], wl.alpha[1], lb, hb, ws_a,
+                           stream)
+            r["select_ms"] = time_call(lambda: kv.kv_compact_kappa(
+                shape, inp["k"], inp["v"], scores, out, wl.crit_alpha[0], wl.crit_alpha[1], hb,
+                wl.reserve, kept, cu, lens, kf, vf, cap, ws_c, stream), dev, stream)
+            r["select"] = "kv_compact_kappa (two-stage, kappa given)"
+        else:
+            total = torch.full((B,), int(budgets[0].sum().item()), dtype=torch.int64, device=dev)
+            r["allocate_ms"] = time_call(lambda: kv.kv_allocate(
+                shape, out, total, 2, 0, 1, lb, hb, ws_a, stream), dev, stream)
+            r["select_ms"] = time_call(lambda: kv.kv_compact(
+                shape, inp["k"], inp["v"], out, None, 1, 2, 0.0, hb, wl.reserve, kept, cu, lens,
+                kf, vf, cap, ws_c, stream), dev, stream)
+            r["allocate"] = "kv_allocate layer_entropy_mode 2 (model-wide TopK, %d layers)" % L
+        for w_ in (ws_s, ws_a, ws_c):
+            if kv.kv_check_device_status(w_, stream):
+                raise RuntimeError("device check in the %s measurement" % name)
+        res[name] = r
+    del w_oq, terms, out, kf, vf, kept
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_cascade_and_presets(kv, wl, shape, inp, scores, hb_main, flat, dev, stream):
+    """The headline workload's other selection paths, timed alone on its inputs: LAVa's
+    online prefill cascade (stage t: kv_allocate_capped over layers 0..t-1, kv_recompact of
+    layers 0..t-2 from the previous flat cache, kv_recompact of layer t-1 from its K/V), the
+    StreamingLLM preset (kv_compact_streaming), and the re-eviction of the flat cache after
+    decode appends (kv_recompact); B = 1 for the cascade."""
+    import torch
+    B, L, hkv, n, w = shape.batch, shape.layers, wl.hkv, wl.n, wl.w
+    total = wl.total_budget_value()
+    reserve = wl.reserve
+    cap = total + L * hkv * reserve
+    flats = [{"kept": torch.empty(cap, dtype=torch.int32, device=dev),
+              "cu": torch.zeros(1, L, hkv + 1, dtype=torch.int64, device=dev),
+              "lens": torch.zeros(1, L, hkv, dtype=torch.int32, device=dev),
+              "kf": torch.empty(cap, wl.d, dtype=wl.torch_dtype, device=dev),
+              "vf": torch.empty(cap, wl.d, dtype=wl.torch_dtype, device=dev)} for _ in range(2)]
+    caps = [torch.full((1, L), n * hkv, dtype=torch.int32, device=dev) for _ in range(2)]
+    hbs = [torch.zeros(1, t, hkv, dtype=torch.int32, device=dev) for t in range(1, L + 1)]
+    budget = torch.tensor([total], dtype=torch.int64, device=dev)
+    sh = [kv.KvShape.from_workload(wl.with_(batch=1), layers=t) for t in range(0, L + 1)]
+    w_a = torch.zeros(max(kv.kv_workspace_size(kv.KV_OP_ALLOCATE, shape), 256),
+                      dtype=torch.uint8, device=dev)
+    w_r = torch.zeros(kv.kv_recompact_workspace_size(max(cap, hkv * n)), dtype=torch.uint8,
+                      device=dev)
+    sc1 = scores[:1]
+    k1, v1 = inp["k"][:1], inp["v"][:1]
+
+    def cascade():
+        for t in range(1, L + 1):
+            lb, hb = caps[t % 2], hbs[t - 1]
+            kv.kv_allocate_capped(sh[t], sc1[:, :t], budget, caps[(t - 1) % 2], 0, 1, lb, hb,
+                                  w_a, stream)
+            src, dst = flats[(t - 1) % 2], flats[t % 2]
+            if t >= 2:
+                kv.kv_recompact(sh[t - 1], sc1[:, :t - 1], hb[:, :t - 1], src["kept"],
+                                src["cu"][:, :t - 1], src["lens"][:, :t - 1], src["kf"],
+                                src["vf"], reserve, None, dst["kept"], dst["cu"], dst["lens"],
+                                dst["kf"], dst["vf"], w_r, stream)
+            row_base = dst["cu"][0, t - 2, hkv:hkv + 1] if t >= 2 else None
+            kv.kv_recompact(sh[1], sc1[:, t - 1:t], hb[:, t - 1:t], None, None, None,
+                            k1[:, t - 1:t], v1[:, t - 1:t], reserve, row_base, dst["kept"],
+                            dst["cu"][:, t - 1:t], dst["lens"][:, t - 1:t], dst["kf"], dst["vf"],
+                            w_r, stream)
+
+    # the slices above must be contiguous views (B = 1, or the first sequence)
+    t_cascade = time_call(cascade, dev, stream, reps=2)
+    for w_ in (w_a, w_r):
+        if kv.kv_check_device_status(w_, stream):
+            raise RuntimeError("device check in the cascade measurement")
+    rows_final = int(flats[L % 2]["lens"].sum().item())
+    peak_rows = total + n * hkv
+    res = {"cascade": {"ms": t_cascade, "stages": L, "ms_per_stage": t_cascade / L,
+                       "rows_final": rows_final, "peak_rows": peak_rows,
+                       "peak_rows_one_shot": L * n * hkv,
+                       "how": "32 stages of kv_allocate_capped + 2 kv_recompact, eager"}}
+    del flats
+    torch.cuda.empty_cache()
+    # StreamingLLM preset with the workload's own per-head budgets
+    row_bytes = wl.d * wl.elem_bytes
+    capm = wl.flat_capacity_rows()
+    out = {k_: torch.empty_like(x) for k_, x in flat.items()}
+    ws1 = torch.zeros(256, dtype=torch.uint8, device=dev)
+    t_st = time_call(lambda: kv.kv_compact_streaming(
+        shape, inp["k"], inp["v"], 4, hb_main, reserve, out["kept"], out["cu"], out["lens"],
+        out["kf"], out["vf"], capm, ws1, stream), dev, stream)
+    rows = int(hb_main.sum().item())
+    st_bytes = 4 * rows * row_bytes + 4 * rows
+    res["streaming"] = {"ms": t_st, "rows": rows, "gbs": st_bytes / (t_st / 1e3) / 1e9,
+                        "how": "kv_compact_streaming (4 sinks), the workload's head budgets"}
+    # re-eviction of the decoded flat cache: every head up to 16 prefill rows smaller (its
+    # window and appended rows stay)
+    new_hb = (flat["lens"] - torch.clamp(hb_main - wl.w, max=16)).to(torch.int32)
+    ws_r = torch.zeros(kv.kv_recompact_workspace_size(capm), dtype=torch.uint8, device=dev)
+    t_re = time_call(lambda: kv.kv_recompact(
+        shape, scores, new_hb, flat["kept"], flat["cu"], flat["lens"], flat["kf"], flat["vf"],
+        reserve, None, out["kept"], out["cu"], out["lens"], out["kf"], out["vf"], ws_r, stream),
+        dev, stream)
+    rows = int(new_hb.sum().item())
+    re_bytes = 4 * rows * row_bytes + 8 * rows + 4 * int(flat["lens"].sum().item())
+    res["reevict"] = {"ms": t_re, "rows": rows, "gbs": re_bytes / (t_re / 1e3) / 1e9,
+                      "how": "kv_recompact of the decoded flat cache, 16 prefill rows fewer "
+                             "per head (appended and window rows kept)"}
+    for w_ in (ws1, ws_r):
+        if kv.kv_check_device_status(w_, stream):
+            raise RuntimeError("device check in the preset measurements")
+    del out
+    torch.cuda.empty_cache()
+    return res
+
+
 def measure_workload(kv, W, wl, dev, stream, steps, warmup):
     """One more workload of the pages' configurations: the same step as the headline (eviction
     pass over every (sequence, layer), then one decode step over every layer), eager launches
@@ -579,6 +750,7 @@ def measure_workload(kv, W, wl, dev, stream, steps, warmup):
            "inputs larger than L2 (K+V %.1f GiB)" % (input_bytes / 2**30)}
     if wl.mode == "critical":
         res["crit_norm"] = time_crit_norm(kv, wl, shape, inp, crit, w_s, dev, stream)
+        res["per_query_head"] = measure_per_query_head(kv, wl, shape, inp, scores, dev, stream)
     del inp, scores, crit, kf, vf, kept, flush
     torch.cuda.empty_cache()
     return res
@@ -1038,6 +1210,14 @@ def run_ours(args):
                "steps": args.e2e_steps}
         del host
 
+    # -------------------- the headline workload's other selection paths --------------------
+    paths = None
+    if (rank == 0 and world == 1 and not args.no_other_workloads and args.layers <= 0 and
+            wl.mode == "lava" and B == 1):
+        paths = measure_cascade_and_presets(
+            kv, wl, shape, inp, scores, hb,
+            {"kept": kept, "cu": cu, "lens": lens, "kf": kf, "vf": vf}, dev, stream)
+
     # -------------------- the pages' other configurations --------------------
     others = None
     if rank == 0 and world == 1 and not args.no_other_workloads and args.layers <= 0:
@@ -1098,6 +1278,7 @@ def run_ours(args):
             "crit_norm": crit_norm,
             "cpu_baseline": cpu,
             "workloads": others,
+            "selection_paths": paths,
             "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clk,

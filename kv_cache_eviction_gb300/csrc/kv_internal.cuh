@@ -70,8 +70,8 @@ cudaError_t launch_proj_tc(const Shape& s, int mode, const void* v, const void* 
 // After the tcgen05 scoring kernel: LAVa's V-bar factor (vbar != nullptr) and the keys whose
 // pooling window crosses a range boundary (from the halo copies of both ranges).
 cudaError_t launch_score_fixup(const float* halo, const float* vbar, int64_t units, int Pg,
-                               int Tu, int C, int G, int r, int group_max, float* scores,
-                               cudaStream_t st);
+                               int Tu, int C, int G, int r, int group_max, int terms,
+                               float* scores, cudaStream_t st);
 
 // ----------------------------- allocation ----------------------------------
 struct AllocPlan {

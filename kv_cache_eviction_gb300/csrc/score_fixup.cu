@@ -18,10 +18,12 @@ constexpr int kFixU = 4;   // 16-byte vectors in flight per thread
 // boundary keys that fall inside the chunk (pooled from the halos, then scaled).
 __global__ void __launch_bounds__(kFixThreads)
 score_tc_fixup(const float* __restrict__ halo, const float* __restrict__ vbar, int Pg, int Tu,
-               int C, int G, int r, int group_max, int per, float* __restrict__ scores) {
+               int C, int G, int r, int group_max, int terms, int per,
+               float* __restrict__ scores) {
   const int64_t u = blockIdx.y;
   const int c0 = min(C, (int)blockIdx.x * per), c1 = min(C, c0 + per);
-  float* S = scores + u * C;
+  // terms: every query head's pooled mean, scores[u][G][C]
+  float* S = scores + u * (int64_t)C * (terms ? G : 1);
   float vb = 1.0f;
   if (vbar) {
     vb = vbar[u];
@@ -64,8 +66,10 @@ score_tc_fixup(const float* __restrict__ halo, const float* __restrict__ vbar, i
         const float x = jj < b ? Hl[q * R4 + 2 * r + (jj - (b - 2 * r))] : Hr[q * R4 + (jj - b)];
         pm = fmaxf(pm, x);
       }
+      if (terms) S[(int64_t)q * C + j] = pm;
       gv = group_max ? fmaxf(gv, pm) : gv + pm;
     }
+    if (terms) continue;
     if (!group_max) gv = gv / (float)G;
     if (vbar) gv = gv * vb;
     S[j] = gv;
@@ -73,8 +77,8 @@ score_tc_fixup(const float* __restrict__ halo, const float* __restrict__ vbar, i
 }
 
 cudaError_t launch_score_fixup(const float* halo, const float* vbar, int64_t units, int Pg,
-                               int Tu, int C, int G, int r, int group_max, float* scores,
-                               cudaStream_t st) {
+                               int Tu, int C, int G, int r, int group_max, int terms,
+                               float* scores, cudaStream_t st) {
   if (units <= 0 || C <= 0) return cudaSuccess;
   // scaling: about eight CTAs per SM, at least 4K keys each; boundary keys only: one CTA
   int64_t nch = 1;
@@ -87,7 +91,7 @@ cudaError_t launch_score_fixup(const float* halo, const float* vbar, int64_t uni
   const int per = (int)(cdiv(cdiv(C, nch), 4) * 4);
   nch = cdiv(C, per);
   score_tc_fixup<<<dim3((unsigned)nch, (unsigned)units), kFixThreads, 0, st>>>(
-      halo, vbar, Pg, Tu, C, G, r, group_max, per, scores);
+      halo, vbar, Pg, Tu, C, G, r, group_max, terms, per, scores);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -257,7 +257,7 @@ bool score_tc_supported(const Shape& s);
 size_t score_tc_ws(const Shape& s, int mode);
 cudaError_t launch_score_tc(const Shape& s, int mode, int group, const void* q_win,
                             const void* k, const void* v, float* scores, char* ws,
-                            cudaStream_t st);
+                            cudaStream_t st, int terms = 0);
 bool crit_tc_supported(const Shape& s, int D);
 cudaError_t launch_crit_tc(const Shape& s, const void* v, const void* w_o, int D, float* crit,
                            char* ws, cudaStream_t st);
@@ -367,6 +367,11 @@ static cudaError_t launch_terms_simt_t(const Shape& s, int kind, const T* q_win,
 
 cudaError_t launch_window_terms(const Shape& s, int kind, const void* q_win, const void* k,
                                 float* terms, char* ws, const ScorePlan& p, cudaStream_t st) {
+  // the tcgen05 kernel where the shape allows (its P2 epilogue forms every query head's
+  // window sums anyway), the CUDA-core kernels otherwise
+  if (p.path == 1 && !simt_forced())
+    return launch_score_tc(s, KV_SCORE_ADA, KV_GROUP_MEAN, q_win, k, nullptr, terms, ws, st,
+                           kind == KV_TERMS_L2 ? 2 : 1);
   if (s.dtype == KV_BF16)
     return launch_terms_simt_t<__nv_bfloat16>(s, kind, (const __nv_bfloat16*)q_win,
                                               (const __nv_bfloat16*)k, terms, ws, p, st);

@@ -85,6 +85,11 @@ static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 
 struct TcParams {
   int n, w, C, G, r, group_max;
+  // terms != 0: every query head's term instead of the KV head's score, into
+  // scores[units][G][C]: 1 = pooled window mean, 2 = sqrt(sum_t P^2) (r = 0, esc = 2: pass 2
+  // then exponentiates twice the log-probability, i.e. forms P^2, and inv_w is 1)
+  int terms;
+  float esc;
   int64_t units;
   int Pg, PgS, NG, Tu, Tc;
   int ncomb;            // CTAs that combine one unit's partials (power of two <= 16)
@@ -130,8 +135,8 @@ __device__ __forceinline__ float vrow_l1_row(const uint8_t* base, int row) {
 // index and the number of threads (a multiple of 32) that share the work.
 template <int LW>
 __device__ __forceinline__ void pool_range(const float* A, int RK, int sK, int eK, int C, int G,
-                                           int r, int group_max, float inv_w, float* S,
-                                           float* H, int tid, int nthr) {
+                                           int r, int group_max, float inv_w, int terms,
+                                           float* S, float* H, int tid, int nthr) {
   // window mean of query head q at key j (slots hold per-quarter sums for w = 64)
   auto aval = [&](int q, int j) -> float {
     if (LW <= 5) return A[q * RK + (j - sK)];
@@ -160,6 +165,18 @@ __device__ __forceinline__ void pool_range(const float* A, int RK, int sK, int e
 #pragma unroll
       for (int i = 0; i < RUN; ++i)
         out[i] = fmaxf(fmaxf(fmaxf(m2[i], m2[i + 2]), m2[i + 4]), v[i + 6]);
+      if (terms) {   // every query head's pooled mean, no group reduction
+        if (live) {
+#pragma unroll
+          for (int i = 0; i < RUN; ++i) {
+            const int j = j0 + i;
+            if (j >= eK) break;
+            const int lo = max(0, j - 3), hi = min(C - 1, j + 3);
+            if (lo >= sK && hi < eK) S[(int64_t)qh * C + j] = out[i];
+          }
+        }
+        continue;
+      }
 #pragma unroll
       for (int i = 0; i < RUN; ++i) {
         float gv = out[i];
@@ -177,6 +194,16 @@ __device__ __forceinline__ void pool_range(const float* A, int RK, int sK, int e
           const int lo = max(0, j - 3), hi = min(C - 1, j + 3);
           if (lo >= sK && hi < eK) S[j] = out[i];
         }
+      }
+    }
+  } else if (terms) {
+    for (int idx = tid; idx < G * (eK - sK); idx += nthr) {
+      const int q = idx / (eK - sK), j = sK + (idx - q * (eK - sK));
+      const int lo = max(0, j - r), hi = min(C - 1, j + r);
+      if (lo >= sK && hi < eK) {
+        float pm = -INFINITY;
+        for (int jj = lo; jj <= hi; ++jj) pm = fmaxf(pm, aval(q, jj));
+        S[(int64_t)q * C + j] = terms == 2 ? sqrtf(pm) : pm;
       }
     }
   } else {
@@ -514,7 +541,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         if (__any_sync(0xffffffffu, !filled)) { ok = false; break; }   // the whole warp
         ++np2;
         const int sK = t0 * 128, eK = min(te * 128, p.C);
-        pool_range<LW>(A, RK, sK, eK, p.C, p.G, p.r, p.group_max, p.inv_w, p.scores + u * p.C,
+        pool_range<LW>(A, RK, sK, eK, p.C, p.G, p.r, p.group_max, p.inv_w, p.terms,
+                       p.scores + u * (int64_t)p.C * (p.terms ? p.G : 1),
                        p.halo + (u * p.Pg + rank) * (int64_t)p.G * 4 * p.r, vt_, 32 * kVWarps);
         __syncwarp();
         if (lane == 0) mbar_arrive(&tl->aempty);
@@ -571,7 +599,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             }
           }
           named_bar(1, kEpiThreads);
-          if (et < 128) nlse[et] = -__ldcg(&p.lse[u * 128 + et]);
+          if (et < 128) nlse[et] = -__ldcg(&p.lse[u * 128 + et]) * p.esc;
         }
         named_bar(1, kEpiThreads);
       }
@@ -638,7 +666,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 #pragma unroll
           for (int j = 0; j < SL; ++j) acc[j] = 0.f;
           const float2* nl2 = reinterpret_cast<const float2*>(nlse + qc * 32);
-          const float2 sc = make_float2(c2, c2);
+          const float2 sc = make_float2(c2 * p.esc, c2 * p.esc);
 #pragma unroll
           for (int j = 0; j < SL; ++j) {
             float2 s0 = make_float2(0.f, 0.f), s1 = s0;
@@ -661,7 +689,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
           if (__shfl_sync(0xffffffffu, pf_flag, 0) >= (uint32_t)p.ncomb) {
             __threadfence();
             const float4 l4 = __ldcg(reinterpret_cast<const float4*>(p.lse + pf_u * 128) + lane);
-            reinterpret_cast<float4*>(nlse)[lane] = make_float4(-l4.x, -l4.y, -l4.z, -l4.w);
+            const float e = p.esc;
+            reinterpret_cast<float4*>(nlse)[lane] =
+                make_float4(-l4.x * e, -l4.y * e, -l4.z * e, -l4.w * e);
             __syncwarp();
             if (lane == 0) tl->pf_unit = pf_u;
             pf_u = -1;
@@ -841,7 +871,7 @@ size_t score_tc_ws(const Shape& s, int) {
 
 cudaError_t launch_score_tc(const Shape& s, int mode, int group, const void* q_win,
                             const void* k, const void* v, float* scores, char* ws,
-                            cudaStream_t st) {
+                            cudaStream_t st, int terms) {
   TcPlan tp;
   if (!tc_plan(s, &tp)) return cudaErrorNotSupported;
   const int64_t units = s.units();
@@ -860,8 +890,10 @@ cudaError_t launch_score_tc(const Shape& s, int mode, int group, const void* q_w
   prm.w = s.w;
   prm.C = s.C();
   prm.G = s.G();
-  prm.r = s.pool / 2;
+  prm.r = terms == 2 ? 0 : s.pool / 2;
   prm.group_max = group == KV_GROUP_MAX;
+  prm.terms = terms;
+  prm.esc = terms == 2 ? 2.0f : 1.0f;
   prm.units = units;
   prm.Pg = tp.Pg;
   prm.PgS = (tp.Pg + 1) & ~1;
@@ -871,7 +903,7 @@ cudaError_t launch_score_tc(const Shape& s, int mode, int group, const void* q_w
   prm.Tu = tp.Tu;
   prm.Tc = tp.Tc;
   prm.c2 = (1.0f / sqrtf((float)s.d)) * 1.4426950408889634f;
-  prm.inv_w = 1.0f / (float)s.w;
+  prm.inv_w = terms == 2 ? 1.0f : 1.0f / (float)s.w;
   prm.partial = reinterpret_cast<float2*>(ws + tp.off_partial);
   prm.lse = reinterpret_cast<float*>(ws + tp.off_lse);
   prm.done1 = reinterpret_cast<uint32_t*>(ws + tp.off_flags);
@@ -897,7 +929,7 @@ cudaError_t launch_score_tc(const Shape& s, int mode, int group, const void* q_w
   count_launches(1);
   if (prm.vbar != nullptr || (prm.r > 0 && tp.Pg > 1)) {
     e = launch_score_fixup(prm.halo, prm.vbar, units, tp.Pg, tp.Tu, prm.C, prm.G, prm.r,
-                           prm.group_max, scores, st);
+                           prm.group_max, terms, scores, st);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();

@@ -61,9 +61,24 @@ def gpu_proj(wl, shape, inp, w_o, terms, kind, eps):
     return out
 
 
+@pytest.fixture(params=["tc", "simt"])
+def score_path(request):
+    """Window terms through the tcgen05 scoring kernel (its pass-2 epilogue writes every
+    query head's window sums) and through the CUDA-core kernels."""
+    import os
+    old = os.environ.get("KVEVICT_SCORE_PATH")
+    os.environ["KVEVICT_SCORE_PATH"] = request.param
+    yield request.param
+    if old is None:
+        os.environ.pop("KVEVICT_SCORE_PATH", None)
+    else:
+        os.environ["KVEVICT_SCORE_PATH"] = old
+
+
 @pytest.mark.parametrize("kind", [kv.KV_TERMS_MEAN_POOLED, kv.KV_TERMS_L2])
-def test_window_terms_match_oracle(kind):
-    wl, shape, inp, _ = setup()
+@pytest.mark.parametrize("n", [1000, 5000])
+def test_window_terms_match_oracle(kind, n, score_path):
+    wl, shape, inp, _ = setup(n=n, L=1 if n > 2000 else 2)
     t = gpu_terms(wl, shape, inp, kind).cpu().numpy()
     okind = "mean_pool" if kind == kv.KV_TERMS_MEAN_POOLED else "l2"
     for l in range(wl.layers):
