@@ -38,10 +38,10 @@ constexpr uint32_t kNoBin = 0xFFFFFFFFu;
 // Offsets of every head in the flat buffer and the initial lengths.
 __global__ void __launch_bounds__(kScanThreads)
 compact_offsets(const int32_t* __restrict__ head_budget, int64_t H, int Hkv, int w, int n,
-                int reserve, int64_t cap, int64_t* __restrict__ cu, int32_t* __restrict__ lens,
-                WsHeader* hdr) {
+                int reserve, int64_t cap, const int64_t* __restrict__ row_base,
+                int64_t* __restrict__ cu, int32_t* __restrict__ lens, WsHeader* hdr) {
   __shared__ int64_t scratch[32];
-  int64_t carry = 0;
+  int64_t carry = row_base != nullptr ? *row_base : 0;   // the first row of the output
   for (int64_t t0 = 0; t0 < H; t0 += kScanThreads) {
     const int64_t h = t0 + threadIdx.x;
     int64_t val = 0;
@@ -615,11 +615,12 @@ cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const f
                            const float* crit, uint32_t can, uint32_t cad, float ceps,
                            bool kappa_given, const int32_t* head_budget, int reserve,
                            int32_t* kept, int64_t* cu, int32_t* lens, void* kf, void* vf,
-                           int64_t cap, char* ws, const CompactPlan& p, cudaStream_t st) {
+                           int64_t cap, char* ws, const CompactPlan& p, cudaStream_t st,
+                           const int64_t* row_base) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   const int64_t H = s.units();
-  compact_offsets<<<1, kScanThreads, 0, st>>>(head_budget, H, s.Hkv, s.w, s.n, reserve, cap, cu,
-                                               lens, hdr);
+  compact_offsets<<<1, kScanThreads, 0, st>>>(head_budget, H, s.Hkv, s.w, s.n, reserve, cap,
+                                               row_base, cu, lens, hdr);
   if (H > 0) {
     const int C = s.C();
     // the bulk copies need 16-byte aligned score (and norm) arrays
@@ -699,8 +700,8 @@ cudaError_t launch_compact_streaming(const Shape& s, const void* k, const void* 
                                      char* ws, cudaStream_t st) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   const int64_t H = s.units();
-  compact_offsets<<<1, kScanThreads, 0, st>>>(head_budget, H, s.Hkv, s.w, s.n, reserve, cap, cu,
-                                               lens, hdr);
+  compact_offsets<<<1, kScanThreads, 0, st>>>(head_budget, H, s.Hkv, s.w, s.n, reserve, cap,
+                                               nullptr, cu, lens, hdr);
   int gx = (int)cdiv((int64_t)num_sms() * 16, H);
   if (gx < 1) gx = 1;
   if (gx > 64) gx = 64;

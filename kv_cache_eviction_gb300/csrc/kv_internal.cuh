@@ -96,12 +96,14 @@ struct CompactPlan {
   int64_t flag_words;   // per head, when CriticalKV stage-1 flags are needed
 };
 CompactPlan compact_plan(const Shape& s, bool critical);
-// kappa_given: crit holds the stage-2 key itself instead of ||(V W_O)_j||_1.
+// kappa_given: crit holds the stage-2 key itself instead of ||(V W_O)_j||_1.  row_base
+// (nullable device pointer): the first output row (0 when null).
 cudaError_t launch_compact(const Shape& s, const void* k, const void* v, const float* scores,
                            const float* crit, uint32_t can, uint32_t cad, float ceps,
                            bool kappa_given, const int32_t* head_budget, int reserve,
                            int32_t* kept, int64_t* cu, int32_t* lens, void* kf, void* vf,
-                           int64_t cap, char* ws, const CompactPlan& p, cudaStream_t st);
+                           int64_t cap, char* ws, const CompactPlan& p, cudaStream_t st,
+                           const int64_t* row_base = nullptr);
 
 // StreamingLLM preset: sinks and the most recent candidates fill each head's budget.
 cudaError_t launch_compact_streaming(const Shape& s, const void* k, const void* v, int sinks,

@@ -30,7 +30,10 @@ constexpr int kRGatherThreads = 256;
 }  // namespace
 
 size_t recompact_ws_bytes(int64_t src_rows) {
-  return kWsHeader + align_up((size_t)(src_rows > 0 ? src_rows : 0) * sizeof(int32_t), 256);
+  // the row lists, or, for the uncompacted source, the candidate regions of kv_compact's
+  // selection (two 4-byte values per candidate)
+  const size_t r = (size_t)(src_rows > 0 ? src_rows : 0);
+  return kWsHeader + 2 * align_up(r * sizeof(int32_t), 256);
 }
 
 // Source extent of head h: its first source row and the rows it holds.
@@ -175,6 +178,13 @@ cudaError_t launch_recompact(const Shape& s, const float* scores, const int32_t*
                              int64_t src_rows, int reserve, const int64_t* row_base,
                              int32_t* kept, int64_t* cu, int32_t* lens, void* kf, void* vf,
                              int64_t cap, char* ws, cudaStream_t st) {
+  if (src_kept == nullptr) {
+    // every position held: kv_compact's selection (streamed per-head Top-B_g over the
+    // scores, the window kept) and gather, from the row base
+    return launch_compact(s, src_k, src_v, scores, nullptr, 1, 2, 0.0f, false, head_budget,
+                          reserve, kept, cu, lens, kf, vf, cap, ws, compact_plan(s, false), st,
+                          row_base);
+  }
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   int32_t* list = reinterpret_cast<int32_t*>(ws + kWsHeader);
   const int64_t H = s.units();
