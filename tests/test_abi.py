@@ -150,3 +150,53 @@ def test_binding_refuses_host_tensors(L):
     t = torch.zeros(16)
     with pytest.raises(ValueError):
         kv.kv_score(s, 0, 0, t, t, None, None, 0, t, None, t)
+
+
+def test_next_calls_reject_invalid_arguments_on_host(L):
+    """The calls of the cascade, the per-query-head scores and the presets refuse bad
+    arguments before anything is enqueued (no GPU is touched here)."""
+    s = shape()
+    p = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1004)
+    big = 1 << 30
+    # kv_allocate_capped: caps required, alpha a fraction
+    assert L.kv_allocate_capped(ctypes.byref(s), p, p, None, 0, 1, p, p, p, big, None) == 1
+    assert L.kv_allocate_capped(ctypes.byref(s), p, p, p, 2, 1, p, p, p, big, None) == 1
+    assert L.kv_allocate_capped(ctypes.byref(s), p, p, p, 0, 1, p, p, p,
+                                kv.kv_workspace_size(1, s) - 1, None) == kv.KV_ERR_WORKSPACE
+    # kv_recompact: the source is a flat cache (all three tables) or the K/V (none); the
+    # output is not the source; row tables and rows aligned; workspace large enough
+    vout = ctypes.c_void_p(0x3000)
+    args = lambda kept, cu, lens, sk, out, ws_bytes: (
+        ctypes.byref(s), p, p, kept, cu, lens, sk, p, 1 << 20, 0, None, p, p, p, out, vout,
+        1 << 20, p, ws_bytes, None)
+    assert L.kv_recompact(*args(p, None, p, p, ctypes.c_void_p(0x2000), big)) == 1
+    assert L.kv_recompact(*args(p, p, p, p, p, big)) == 1                    # k_flat is src_k
+    assert L.kv_recompact(*args(p, p, p, odd, ctypes.c_void_p(0x2000), big)) == 1
+    assert L.kv_recompact(*args(p, p, p, p, ctypes.c_void_p(0x2000),
+                                kv.kv_recompact_workspace_size(1 << 20) - 1)) == 3
+    assert kv.kv_recompact_workspace_size(-1) == 0
+    # kv_window_terms / kv_proj_score: kind, eps, model_dim
+    assert L.kv_window_terms(ctypes.byref(s), 2, p, p, p, p, big, None) == 1
+    assert L.kv_window_terms(ctypes.byref(s), 0, odd, p, p, p, big, None) == 1
+    assert L.kv_proj_score(ctypes.byref(s), 2, p, p, 4096, p, 0.0, p, p, big, None) == 1
+    assert L.kv_proj_score(ctypes.byref(s), 0, p, p, 4090, p, 0.0, p, p, big, None) == 1
+    assert L.kv_proj_score(ctypes.byref(s), 0, p, p, 4096, p, ctypes.c_float(-1.0), p, p, big,
+                           None) == 1
+    assert L.kv_proj_score(ctypes.byref(shape(dtype="f32", d=64)), 0, p, p, 4096, p, 0.0, p, p,
+                           big, None) == kv.KV_ERR_UNSUPPORTED
+    # kv_compact_kappa / kv_compact_streaming: kappa required, alpha a fraction, sinks >= 0
+    assert L.kv_compact_kappa(ctypes.byref(s), p, p, p, None, 1, 2, p, 0, p, p, p, p, p, 1 << 20,
+                              p, big, None) == 1
+    assert L.kv_compact_kappa(ctypes.byref(s), p, p, p, p, 3, 2, p, 0, p, p, p, p, p, 1 << 20,
+                              p, big, None) == 1
+    assert L.kv_compact_streaming(ctypes.byref(s), p, p, -1, p, 0, p, p, p, p, p, 1 << 20, p,
+                                  big, None) == 1
+    assert L.kv_compact_streaming(ctypes.byref(s), p, p, 4, p, 0, p, p, p, p, p, 10, p, big,
+                                  None) == kv.KV_ERR_CAPACITY
+    # the model-wide allocation needs L * Hkv <= 256
+    wide = shape(layers=64)
+    assert L.kv_allocate(ctypes.byref(wide), p, p, 2, 0, 1, p, p, p, big,
+                         None) == kv.KV_ERR_UNSUPPORTED
+    # kv_crit_norm: model_dim a multiple of 8
+    assert L.kv_crit_norm(ctypes.byref(s), p, p, 4090, p, p, big, None) == 1
