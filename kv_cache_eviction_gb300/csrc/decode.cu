@@ -698,14 +698,16 @@ static cudaError_t launch_attn_g(const Shape& s, const T* q, const void* kf, con
 }
 
 // KVEVICT_DECODE_PATH=rows forces the row-balanced split of this file for every shape,
-// =heads the one-CTA-per-head kernel and =split the one-launch split wherever their row size
-// and group allow, whatever the head lengths (tests compare the decode paths).
+// =heads the one-CTA-per-head kernel, =split the one-launch split and =parts the short heads
+// in parts wherever their row size, group and head count allow, whatever the head lengths
+// (tests compare the decode paths).
 static int decode_path_forced() {
   const char* e = std::getenv("KVEVICT_DECODE_PATH");
   if (e == nullptr) return 0;
   if (std::strcmp(e, "rows") == 0) return 1;
   if (std::strcmp(e, "heads") == 0) return 2;
   if (std::strcmp(e, "split") == 0) return 3;
+  if (std::strcmp(e, "parts") == 0) return 4;
   return 0;
 }
 
@@ -716,15 +718,23 @@ cudaError_t launch_decode(const Shape& s, const void* q, const void* kn, const v
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   const int64_t H = s.units();
   const int forced = decode_path_forced();
-  // Measured on GB300 (L2 flushed, log-normal head lengths): one CTA per head wins while
-  // the heads fit one wave and are short (every kernel is latency-bound there); the
-  // one-launch split wins from there to about 1.5K rows per head, and to about 8K when the
-  // heads are few; heads longer still stream best through the row-balanced split, except
-  // in calls of a few heads (one layer at a time), where the split spreads them over SMs.
+  // Measured on GB300 (log-normal head lengths, the cache cold in L2): while the heads fit
+  // one wave and are short (every kernel is latency-bound there), the heads in parts (one
+  // CTA per head, the rows of the longest spread over the CTAs left) match one CTA per head
+  // on even heads and stay flat on skewed ones, where one CTA per head waits on its longest
+  // head; the parts kernel also takes calls of a few heads (one layer at a time), whose
+  // lengths the capacity does not bound.  The one-launch split wins from there to about
+  // 1.5K rows per head, and to about 8K when the heads are few; heads longer still stream
+  // best through the row-balanced split.
   const int64_t rows_per_head = cap / H;
   const bool few_heads = H <= 2 * (int64_t)num_sms();
   const bool one_layer = H <= (int64_t)num_sms() / 4;
   if (forced == 0) {
+    if (((few_heads && rows_per_head <= kDecodeHeadShortRows) || one_layer) &&
+        decode_parts_supported(s, cap, p.part_slots))
+      return launch_decode_parts(s, q, kn, vn, kf, vf, cu, lens, cap, scale, out,
+                                 reinterpret_cast<float*>(ws + p.off_part), p.part_slots,
+                                 reinterpret_cast<uint32_t*>(ws + p.off_tick), hdr, st);
     if (few_heads && rows_per_head <= kDecodeHeadShortRows && decode_head_supported(s, cap))
       return launch_decode_head(s, q, kn, vn, kf, vf, cu, lens, cap, scale, out, hdr, st);
     if ((rows_per_head <= kDecodeSplitRowsMax ||
@@ -733,6 +743,10 @@ cudaError_t launch_decode(const Shape& s, const void* q, const void* kn, const v
       return launch_decode_split(s, q, kn, vn, kf, vf, cu, lens, cap, scale, out,
                                  reinterpret_cast<float*>(ws + p.off_part), p.part_slots,
                                  reinterpret_cast<uint32_t*>(ws + p.off_tick), hdr, st);
+  } else if (forced == 4 && decode_parts_supported(s, cap, p.part_slots)) {
+    return launch_decode_parts(s, q, kn, vn, kf, vf, cu, lens, cap, scale, out,
+                               reinterpret_cast<float*>(ws + p.off_part), p.part_slots,
+                               reinterpret_cast<uint32_t*>(ws + p.off_tick), hdr, st);
   } else if (forced == 3 && decode_split_supported(s, cap)) {
     return launch_decode_split(s, q, kn, vn, kf, vf, cu, lens, cap, scale, out,
                                reinterpret_cast<float*>(ws + p.off_part), p.part_slots,

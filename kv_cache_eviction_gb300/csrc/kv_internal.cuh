@@ -161,6 +161,18 @@ cudaError_t launch_decode_split(const Shape& s, const void* q, const void* kn, c
                                 int64_t part_slots, uint32_t* tick, WsHeader* hdr,
                                 cudaStream_t st);
 
+// Decode with one CTA per head and the rows of the longest heads spread over the CTAs left,
+// in parts of one ring fill (decode_parts.cu): rows of 256 bytes, G <= 4, at most
+// kDecodePartsHeadsMax heads, a flat capacity within int32 and a partial slot per head and
+// per extra part.
+constexpr int64_t kDecodePartsHeadsMax = 512;
+bool decode_parts_supported(const Shape& s, int64_t cap, int64_t part_slots);
+cudaError_t launch_decode_parts(const Shape& s, const void* q, const void* kn, const void* vn,
+                                void* kf, void* vf, const int64_t* cu, int32_t* lens,
+                                int64_t cap, float scale, void* out, float* part,
+                                int64_t part_slots, uint32_t* tick, WsHeader* hdr,
+                                cudaStream_t st);
+
 int num_sms();
 // Largest dynamic + static shared memory one CTA may opt in to.
 size_t max_smem_optin();

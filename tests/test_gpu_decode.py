@@ -4,9 +4,9 @@ The caches are built directly (no scoring or compaction) so that the per-head le
 be pushed to the cases the decode kernels have to get right: empty heads, one-row heads, heads
 longer than a whole row chunk (their partials are merged across CTAs), heads sharing a
 chunk, reserve rows exhausted, and every lane layout (16-byte slices per row of 1, 2, 4, 8,
-16 and 32) and group size 1, 2, 3, 4, 8.  Every case runs through both decode kernels (the
-one-CTA-per-head kernel takes the 256-byte-row cases; the others fall through to the
-row-balanced split either way).
+16 and 32) and group size 1, 2, 3, 4, 8.  Every case runs through each decode kernel that
+takes its shape (256-byte rows for all but the row-balanced split; the other shapes fall
+through to it).
 """
 from __future__ import annotations
 
@@ -25,12 +25,13 @@ from .kvpath import assert_decode_close, np64, workspace
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["split", "heads", "rows"], autouse=True)
+@pytest.fixture(params=["split", "heads", "rows", "parts"], autouse=True)
 def decode_path(request):
-    """Every case through the three decode kernels: the one-launch split of the used rows
+    """Every case through the four decode kernels: the one-launch split of the used rows
     across CTAs (256-byte rows, G <= 4, short heads), one CTA per KV head (256-byte rows, the
-    other groups) and the row-balanced split (the rest).  A shape a forced kernel does not
-    take goes to the next one that does."""
+    other groups), the row-balanced split (the rest) and the heads in parts (256-byte rows,
+    G <= 4, at most 512 heads).  A shape a forced kernel does not take goes to the
+    one-CTA-per-head kernel, else the row-balanced split."""
     old = os.environ.get("KVEVICT_DECODE_PATH")
     os.environ["KVEVICT_DECODE_PATH"] = request.param
     yield request.param
@@ -219,3 +220,50 @@ def test_decode_repeated_steps_match_single_oracle_run():
         got = np64(out[0, 0])
         assert_decode_close(got, ref, "bf16", what="decode step %d" % step)
     np.testing.assert_array_equal(lens_d.cpu().numpy(), ln)
+
+
+@pytest.mark.parametrize("dtype,d,G", [("bf16", 128, 4), ("f32", 64, 2), ("bf16", 128, 8),
+                                        ("bf16", 128, 1)])
+def test_decode_heads_at_part_boundaries(dtype, d, G):
+    """Head lengths around the part sizes of the kernel that cuts heads into parts (192 rows,
+    16 per ring stage): one row short of a part, a whole part, one row over, two parts and
+    one over, and one head of hundreds of parts, so that every CTA of the grid takes several
+    extra parts and the last part of a head merges more than one round of eight partials."""
+    B, L, hkv = 1, 2, 8
+    lens = np.array([191, 192, 193, 384, 385, 0, 1, 60000,
+                     127, 128, 129, 255, 256, 2000, 3, 12345])
+    c = build_cache(B, L, hkv, G, d, lens, reserve=2, dtype=dtype, seed=21)
+    check(c, B, L, hkv, G, d, dtype, append=True)
+
+
+def test_decode_most_heads_the_parts_kernel_takes():
+    """512 heads (the most the kernel that cuts heads into parts takes) of uneven lengths: more
+    heads than CTAs of one wave, so the heads' own CTAs take extra parts too."""
+    B, L, hkv, G, d = 2, 32, 8, 4, 128
+    rng = np.random.default_rng(23)
+    H = B * L * hkv
+    lens = np.minimum(rng.lognormal(5.0, 1.0, H).astype(np.int64), 5000)
+    c = build_cache(B, L, hkv, G, d, lens, reserve=1, dtype="bf16", seed=24)
+    check(c, B, L, hkv, G, d, "bf16", append=True)
+
+
+def test_decode_few_idle_ctas_long_first_parts():
+    """296 heads (a few CTAs of a two-per-SM launch left over) of skewed lengths: the kernel
+    that cuts heads into parts has to take longer first parts, streamed through its rings,
+    before the extra parts of the longest heads fit the idle CTAs."""
+    B, L, hkv, G, d = 1, 37, 8, 4, 128
+    rng = np.random.default_rng(29)
+    H = B * L * hkv
+    lens = np.minimum(rng.lognormal(np.log(200.0), 0.6, H).astype(np.int64), 3000)
+    c = build_cache(B, L, hkv, G, d, lens, reserve=2, dtype="bf16", seed=30)
+    check(c, B, L, hkv, G, d, "bf16", append=True)
+
+
+def test_decode_parts_lengths_bumped_at_the_end():
+    """A head of 480K rows: more extra parts than eight per CTA, so the kernel that cuts heads
+    into parts keeps every CTA's extra-part lengths unread until it needs them and bumps the
+    lengths after the last CTA is done (the other cases bump them right after the scan)."""
+    B, L, hkv, G, d = 1, 1, 2, 2, 64
+    lens = np.array([480000, 5])
+    c = build_cache(B, L, hkv, G, d, lens, reserve=2, dtype="f32", seed=31)
+    check(c, B, L, hkv, G, d, "f32", append=True)

@@ -77,7 +77,7 @@ def make_step(wl):
     ("llama8b_32k_b4", dict(layers=2, batch=2)),
     ("llama8b_64k_criticalkv", dict(layers=2, n=8192, model_dim=1024)),
 ])
-@pytest.mark.parametrize("path", [None, "split", "rows"])
+@pytest.mark.parametrize("path", [None, "split", "rows", "parts"])
 def test_graph_replay_matches_eager(name, kw, path):
     old = os.environ.get("KVEVICT_DECODE_PATH")
     if path is None:

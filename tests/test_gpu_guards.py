@@ -53,7 +53,7 @@ def guarded_ws(op, shape):
     return buf, n
 
 
-@pytest.mark.parametrize("path", [None, "split", "heads", "rows"])
+@pytest.mark.parametrize("path", [None, "split", "heads", "rows", "parts"])
 @pytest.mark.parametrize("name,kw", [
     ("mistral7b_128k_lava", dict(layers=2, n=16384)),
     ("llama8b_64k_criticalkv", dict(layers=2, n=8192, model_dim=1024)),

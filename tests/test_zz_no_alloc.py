@@ -29,11 +29,12 @@ def built():
     kv.lib()
 
 
-@pytest.fixture(params=["default", "split", "heads", "rows"])
+@pytest.fixture(params=["default", "split", "heads", "rows", "parts"])
 def decode_path(request):
     """Each decode kernel on the fixed scratch: the default choice, then the one-launch split
-    (tickets and partials in the scratch), one CTA per KV head (only the error word there) and
-    the row-balanced split (chunk map, work counter and partials there)."""
+    (tickets and partials in the scratch), one CTA per KV head (only the error word there), the
+    row-balanced split (chunk map, work counter and partials there) and the heads in parts
+    (per-head tickets, a done counter and partials there)."""
     old = os.environ.get("KVEVICT_DECODE_PATH")
     if request.param == "default":
         os.environ.pop("KVEVICT_DECODE_PATH", None)
