@@ -8,8 +8,8 @@ eviction-pass prefix tokens per second per layer, (batch * n * L) / step_time / 
 batch * n / step_time summed over ranks: the prompt tokens whose whole-model cache the path
 evicts (and then decodes over) per second.  `eviction_only` gives the same rate over the
 eviction stages alone (score + allocate + compact).  The second number, the flat varlen
-decode attention's HBM GB/s, is measured on its own, each decode step on a copy of the
-flat cache whose rows are not in L2 (the steps rotate through copies).  The other workloads of the pages' configurations are timed after the headline one
+decode attention's HBM GB/s, is measured on its own with L2 flushed before every decode
+step.  The other workloads of the pages' configurations are timed after the headline one
 (`workloads`), and the CPU oracle on the host cores (`cpu_baseline`: one core and all).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
@@ -40,23 +40,6 @@ METRIC = "eviction-pass prefix tokens/s per layer; flat varlen decode attn HBM G
 UNIT = "tokens/s/layer"
 DEFAULT_WORKLOAD = "mistral7b_128k_lava"
 L2_BYTES = 129 * 1024 * 1024
-
-
-def gpu_busy(stream) -> None:
-    """A spin kernel of about 50 us on `stream` (it touches no memory): the timed launch behind
-    it is enqueued while the GPU is still busy, so the events time the GPU, not the host's
-    launch path."""
-    import torch
-    with torch.cuda.stream(stream):
-        torch.cuda._sleep(100000)
-
-
-def rotation_count(bytes_per_step: int) -> int:
-    """Copies of a decode step's flat cache to rotate through so that every step reads K/V
-    rows that are not in L2: between two uses of one copy the other copies' steps read at
-    least 1.5 x L2.  (Flushing L2 instead also evicts the kernels' code and constants, which
-    then queue behind the step's own copies in DRAM, a cost a decode loop does not pay.)"""
-    return max(2, min(16, 1 + math.ceil(1.5 * L2_BYTES / max(int(bytes_per_step), 1))))
 
 
 def parse_args():
@@ -784,10 +767,9 @@ OTHER_WORKLOADS = (("llama8b_16k_layer", {"head_budget_frac": 0.2}),
 
 
 def run_decode_only(args, kv, W, dev):
-    """flat_decode_attn alone on flat caches of the workload's shape whose head lengths are
-    log-normal (--decode-sigma) around the workload's mean rows per head: the decode of the
-    eviction pass's output without its inputs on the device.  The steps rotate through copies
-    of the cache (rotation_count) so each one reads rows that are not in L2."""
+    """flat_decode_attn alone, L2 flushed before each step, on a flat cache of the workload's
+    shape whose head lengths are log-normal (--decode-sigma) around the workload's mean rows
+    per head: the decode of the eviction pass's output without its inputs on the device."""
     import torch
     wl = W.WORKLOADS[args.workload]
     if args.layers > 0:
@@ -803,24 +785,19 @@ def run_decode_only(args, kv, W, dev):
     wsd = torch.zeros(max(kv.kv_workspace_size(kv.KV_OP_DECODE, shape), 256), dtype=torch.uint8,
                       device=dev)
     out = torch.empty_like(fc["q"])
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     scale = 1.0 / math.sqrt(wl.d)
     B, L = wl.batch, wl.layers
-    n_rot = rotation_count(algorithmic_bytes(wl, B, L, 0, int(fc["lens"].sum().item()))["decode"])
-    copies = [(fc["k_flat"], fc["v_flat"], fc["lens"])] + [
-        (fc["k_flat"].clone(), fc["v_flat"].clone(), fc["lens"].clone())
-        for _ in range(n_rot - 1)]
-    steps = max(1, args.decode_steps if args.decode_steps > 0 else 32)
-    steps = min(steps, (reserve - 1) * n_rot - max(args.warmup, 0))
+    steps = max(1, min(args.decode_steps if args.decode_steps > 0 else 32, reserve - 1))
     dts, byts = [], []
     for i in range(max(args.warmup, 0) + steps):
-        kf_i, vf_i, lens_i = copies[i % n_rot]
-        rows = int(lens_i.sum().item()) + B * L * wl.hkv
-        gpu_busy(stream)
+        rows = int(fc["lens"].sum().item()) + B * L * wl.hkv
+        flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        kv.flat_decode_attn(shape, fc["q"], fc["k_new"], fc["v_new"], kf_i, vf_i, fc["cu"],
-                            lens_i, scale, out, wsd, stream)
+        kv.flat_decode_attn(shape, fc["q"], fc["k_new"], fc["v_new"], fc["k_flat"], fc["v_flat"],
+                            fc["cu"], fc["lens"], scale, out, wsd, stream)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         if i >= max(args.warmup, 0):
@@ -838,8 +815,7 @@ def run_decode_only(args, kv, W, dev):
         "data": "synthetic flat cache (log-normal head lengths, sigma %g, around %d rows, "
                 "longest %d)" % (args.decode_sigma, mean, int(fc["lens"].max().item())),
         "config": {"workload": wl.name, "batch": B, "layers": L, "hkv": wl.hkv, "hq": wl.hq,
-                   "d": wl.d, "reserve": reserve,
-                   "l2": "cold: %d copies of the flat cache, rotated step by step" % n_rot}}),
+                   "d": wl.d, "reserve": reserve, "l2": "flushed before each step"}}),
           flush=True)
     return 0
 
@@ -1023,71 +999,59 @@ def run_ours(args):
     t_local = max_over_ranks(ms_per_step, dev)
     value = aggregate_value(world, B, wl.n, L, t_local)
 
-    # -------------------- decode alone, the cache cold in L2 --------------------
+    # -------------------- decode alone, L2 flushed before each step --------------------
     hb_rows = int(hb.sum().item())
     lens0 = int(lens.sum().item())          # includes the timed region's last append
     nd = wl.decode_steps if args.decode_steps < 0 else args.decode_steps
     nd = max(1, min(nd, wl.reserve - 1))
-    # rebuild the flat cache so every decode step has a reserve row, then copies of it to
-    # rotate through (every step reads a copy last read 1.5 x L2 of traffic ago)
+    # rebuild the flat cache so every decode step has a reserve row
     kv.kv_compact(shape, inp["k"], inp["v"], scores, crit, wl.crit_alpha[0], wl.crit_alpha[1],
                   wl.crit_eps, hb, wl.reserve, kept, cu, lens, kf, vf, cap, w_c, stream)
     lens0 = int(lens.sum().item())
-    n_rot = rotation_count(algorithmic_bytes(wl, B, L, hb_rows, lens0)["decode"])
-    copies = [(kf, vf, lens)] + [(kf.clone(), vf.clone(), lens.clone())
-                                 for _ in range(n_rot - 1)]
-    uses = [0] * n_rot
-    # Even steps launch eagerly, odd steps replay one captured CUDA graph of the call per copy
-    # (what a serving loop does) with the step's inputs copied into the captured buffers
-    # first: both see the same growing caches.  Both are reported; the graph time is the
-    # value when the capture works.
+    # Even steps launch eagerly, odd steps replay one captured CUDA graph of the call (what a
+    # serving loop does) with the step's inputs copied into the captured buffers first: both
+    # see the same growing cache.  Both are reported; the graph time is the value when the
+    # capture works.
     d0 = W.make_decode_batch(wl, 1, inp["tau"], device=dev, seqs=seqs)
     xq, xk, xv = d0["q"].clone(), d0["k_new"].clone(), d0["v_new"].clone()
     dec_t = {"eager": ([], []), "graph": ([], [])}   # times, bytes
-    dec_graphs, dec_note = None, "not run (--no-graph)" if args.no_graph else None
+    dec_graph, dec_note = None, "not run (--no-graph)" if args.no_graph else None
     gsd = torch.cuda.Stream(dev)
     if not args.no_graph and nd >= 2:
         gsd.wait_stream(stream)
         torch.cuda.synchronize(dev)
         try:
-            dec_graphs = []
-            for (kf_i, vf_i, lens_i) in copies:
-                g_ = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g_, stream=gsd):
-                    kv.flat_decode_attn(shape, xq, xk, xv, kf_i, vf_i, cu, lens_i, scale, out,
-                                        w_d, gsd)
-                dec_graphs.append(g_)
+            dec_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(dec_graph, stream=gsd):
+                kv.flat_decode_attn(shape, xq, xk, xv, kf, vf, cu, lens, scale, out, w_d, gsd)
         except RuntimeError as e:
-            dec_graphs, dec_note = None, "capture failed: " + str(e).splitlines()[0][:160]
+            dec_graph, dec_note = None, "capture failed: " + str(e).splitlines()[0][:160]
             torch.cuda.synchronize(dev)
     for s_ in range(nd):
         d_in = W.make_decode_batch(wl, 1 + s_, inp["tau"], device=dev, seqs=seqs)
-        kind = "graph" if dec_graphs is not None and s_ % 2 == 1 else "eager"
-        i_ = s_ % n_rot
-        kf_i, vf_i, lens_i = copies[i_]
+        kind = "graph" if dec_graph is not None and s_ % 2 == 1 else "eager"
         st_ = gsd if kind == "graph" else stream
         with torch.cuda.stream(st_):
             if kind == "graph":
                 xq.copy_(d_in["q"])
                 xk.copy_(d_in["k_new"])
                 xv.copy_(d_in["v_new"])
-            gpu_busy(st_)
+            flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(st_)
             if kind == "graph":
-                dec_graphs[i_].replay()
+                dec_graph.replay()
             else:
-                kv.flat_decode_attn(shape, d_in["q"], d_in["k_new"], d_in["v_new"], kf_i, vf_i,
-                                    cu, lens_i, scale, out, w_d, st_)
+                kv.flat_decode_attn(shape, d_in["q"], d_in["k_new"], d_in["v_new"], kf, vf, cu,
+                                    lens, scale, out, w_d, st_)
             e1.record(st_)
         torch.cuda.synchronize(dev)
-        uses[i_] += 1
-        rows = lens0 + uses[i_] * B * L * wl.hkv
+        rows = lens0 + (s_ + 1) * B * L * wl.hkv
         dec_t[kind][0].append(e0.elapsed_time(e1))
         dec_t[kind][1].append(algorithmic_bytes(wl, B, L, hb_rows, rows)["decode"])
     if kv.kv_check_device_status(w_d, stream):
         raise RuntimeError("device check in decode")
-    del dec_graphs
+    del dec_graph
     peak, peak_kind = read_peaks()
     dec_kind = "graph" if dec_t["graph"][0] else "eager"
     dts, dbytes = dec_t[dec_kind]
@@ -1097,9 +1061,9 @@ def run_ours(args):
 
     # -------------------- decode alone, one launch per layer --------------------
     # The serving loop's own shape: each layer's decode is its own call (one sequence, the
-    # layer's Hkv heads).  The L calls of a step are captured once per cache copy as a CUDA
-    # graph and replayed (a launch loop in Python would time the host, not the GPU), with the
-    # step's inputs copied into the captured buffers; the steps rotate through the copies.
+    # layer's Hkv heads).  The L calls of a step are captured once as a CUDA graph and
+    # replayed (a launch loop in Python would time the host, not the GPU), with the step's
+    # inputs copied into the captured buffers and L2 flushed before each replay.
     dec_pl = None
     if B == 1 and L > 1 and not args.no_decode_per_layer:
         shape1 = kv.KvShape.from_workload(wl.with_(layers=1))
@@ -1107,37 +1071,28 @@ def run_ours(args):
                            dtype=torch.uint8, device=dev)
         kv.kv_compact(shape, inp["k"], inp["v"], scores, crit, wl.crit_alpha[0], wl.crit_alpha[1],
                       wl.crit_eps, hb, wl.reserve, kept, cu, lens, kf, vf, cap, w_c, stream)
-        for (kf_i, vf_i, lens_i) in copies[1:]:
-            kf_i.copy_(kf)
-            vf_i.copy_(vf)
-            lens_i.copy_(lens)
-        uses = [0] * n_rot
         # per-layer offset tables on 16-byte boundaries (the ABI's alignment rule)
         cu_pl = torch.zeros(L, 16, dtype=torch.int64, device=dev)
         cu_pl[:, :wl.hkv + 1] = cu[0]
         d0 = W.make_decode_batch(wl, 1, inp["tau"], device=dev, seqs=seqs)
         xq, xk, xv = d0["q"].clone(), d0["k_new"].clone(), d0["v_new"].clone()
 
-        def layer_calls(st, i_):
-            kf_i, vf_i, lens_i = copies[i_]
+        def layer_calls(st):
             for l in range(L):
-                kv.flat_decode_attn(shape1, xq[0, l], xk[0, l], xv[0, l], kf_i, vf_i, cu_pl[l],
-                                    lens_i[0, l], scale, out[0, l], w_d1, st,
+                kv.flat_decode_attn(shape1, xq[0, l], xk[0, l], xv[0, l], kf, vf, cu_pl[l],
+                                    lens[0, l], scale, out[0, l], w_d1, st,
                                     flat_capacity_rows=cap)
 
         gs = torch.cuda.Stream(dev)
         gs.wait_stream(stream)
         torch.cuda.synchronize(dev)
-        pl_graphs, pl_note = None, None
+        pl_graph, pl_note = None, None
         try:
-            pl_graphs = []
-            for i_ in range(n_rot):
-                g_ = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g_, stream=gs):
-                    layer_calls(gs, i_)
-                pl_graphs.append(g_)
+            pl_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(pl_graph, stream=gs):
+                layer_calls(gs)
         except RuntimeError as e:
-            pl_graphs, pl_note = None, "capture failed: " + str(e).splitlines()[0][:160]
+            pl_graph, pl_note = None, "capture failed: " + str(e).splitlines()[0][:160]
             torch.cuda.synchronize(dev)
         lens_pl0 = int(lens.sum().item())
         pl = {"graph": ([], []), "eager": ([], [])}   # times, bytes
@@ -1147,20 +1102,18 @@ def run_ours(args):
                 xq.copy_(d_in["q"])
                 xk.copy_(d_in["k_new"])
                 xv.copy_(d_in["v_new"])
-                i_ = s_ % n_rot
+                flush.zero_()
                 # the last step (or every step without a graph) launches eagerly
-                kind = "graph" if pl_graphs is not None and s_ < nd - 1 else "eager"
-                gpu_busy(gs)
+                kind = "graph" if pl_graph is not None and s_ < nd - 1 else "eager"
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(gs)
                 if kind == "graph":
-                    pl_graphs[i_].replay()
+                    pl_graph.replay()
                 else:
-                    layer_calls(gs, i_)
+                    layer_calls(gs)
                 e1.record(gs)
                 torch.cuda.synchronize(dev)
-                uses[i_] += 1
-                rows = lens_pl0 + uses[i_] * L * wl.hkv
+                rows = lens_pl0 + (s_ + 1) * L * wl.hkv
                 pl[kind][0].append(e0.elapsed_time(e1))
                 pl[kind][1].append(algorithmic_bytes(wl, B, L, hb_rows, rows)["decode"])
         if kv.kv_check_device_status(w_d1, stream):
@@ -1174,8 +1127,8 @@ def run_ours(args):
                   if kind == "graph" else "eager per-layer calls (graph: %s)" % pl_note,
                   "eager_us_per_call": statistics.mean(pl["eager"][0]) * 1e3 / L
                   if pl["eager"][0] else None,
-                  "l2": "cold: %d copies of the flat cache, rotated step by step" % n_rot}
-        del pl_graphs
+                  "l2": "flushed before each step of %d per-layer calls" % L}
+        del pl_graph
     dec_batches = None
     if args.decode_batches and rank == 0:
         kv.kv_compact(shape, inp["k"], inp["v"], scores, crit, wl.crit_alpha[0],
@@ -1310,14 +1263,13 @@ def run_ours(args):
             "decode_attn": {"value": dec_gbs, "unit": "GB/s", "frac": dec_gbs / peak,
                             "peak": peak, "steps": len(dts), "ms_per_step": statistics.mean(dts),
                             "bytes_per_step": statistics.mean(dbytes),
-                            "timing": "one captured CUDA graph of the call per cache copy, "
-                                      "replayed" if dec_kind == "graph" else
+                            "timing": "one captured CUDA graph of the call, replayed"
+                            if dec_kind == "graph" else
                             "eager launches (graph: %s)" % (dec_note or "not run"),
                             "eager_value": dec_eager_gbs,
                             "eager_ms_per_step": statistics.mean(dec_t["eager"][0])
                             if dec_t["eager"][0] else None,
-                            "l2": "cold: %d copies of the flat cache, rotated step by step "
-                                  "(each read again after 1.5 x L2 of other copies)" % n_rot},
+                            "l2": "flushed before each step"},
             "decode_attn_per_layer": dec_pl,
             "decode_attn_batches": dec_batches,
             "decode_attn_large": dict(dec_large, frac=dec_large["value"] / peak)
