@@ -883,13 +883,14 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
-    def step(ev=None, st=None):
+    def step(ev=None, st=None, score=True):
         st = stream if st is None else st
         if ev is not None:
             ev[0].record(st)
-        kv.kv_score(shape, mode, group, inp["q_win"], inp["k"],
-                    inp["v"] if wl.mode != "ada" else None, inp["w_o"], wl.model_dim, scores,
-                    crit, w_s, st)
+        if score:
+            kv.kv_score(shape, mode, group, inp["q_win"], inp["k"],
+                        inp["v"] if wl.mode != "ada" else None, inp["w_o"], wl.model_dim,
+                        scores, crit, w_s, st)
         if ev is not None:
             ev[1].record(st)
         kv.kv_allocate(shape, scores, budgets, entropy, wl.alpha[0], wl.alpha[1], lb, hb, w_a,
@@ -1184,18 +1185,51 @@ def run_ours(args):
                "lb": torch.empty(lb.shape, dtype=lb.dtype, pin_memory=True),
                "lens": torch.empty(lens.shape, dtype=lens.dtype, pin_memory=True)}
         d2h = sum(t.numel() * t.element_size() for t in res.values())
+        # The copies are bound by the host link (about 210 GB/s here, for copy engines and SM
+        # loads alike), so the scoring overlaps them: the layers go over in chunks on a copy
+        # stream, and each chunk is scored as soon as it is on the device.  Allocation (whose
+        # layer budgets need every layer), compaction and the decode step follow the last.
+        nch = 8 if (B == 1 and L % 8 == 0) else 1
+        Lc = L // nch
+        shape_c = kv.KvShape.from_workload(wl.with_(layers=Lc)) if nch > 1 else shape
+        cstream = torch.cuda.Stream(dev)
+
+        def layer_slice(name, t, l0, l1):
+            return t[l0:l1] if name == "w_o" else t[:, l0:l1]
+
         e2e_ms = []
         for it in range(args.e2e_steps + 1):     # the first pass is untimed (warm-up)
             torch.cuda.synchronize(dev)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for name in ("q_win", "k", "v", "w_o"):
-                if name in host:
-                    inp[name].copy_(host[name], non_blocking=True)
-            for name in ("q", "k_new", "v_new"):
-                dec[name].copy_(host["dec_" + name], non_blocking=True)
-            budgets.copy_(budgets_h, non_blocking=True)
-            step()
+            cstream.wait_event(e0)
+            chunk_ev = [torch.cuda.Event() for _ in range(nch + 1)]
+            with torch.cuda.stream(cstream):
+                for c in range(nch):
+                    l0, l1 = c * Lc, (c + 1) * Lc
+                    for name in ("q_win", "k", "v", "w_o"):
+                        if name in host:
+                            layer_slice(name, inp[name], l0, l1).copy_(
+                                layer_slice(name, host[name], l0, l1), non_blocking=True)
+                    chunk_ev[c].record(cstream)
+                for name in ("q", "k_new", "v_new"):
+                    dec[name].copy_(host["dec_" + name], non_blocking=True)
+                budgets.copy_(budgets_h, non_blocking=True)
+                chunk_ev[nch].record(cstream)
+            if nch > 1:
+                for c in range(nch):
+                    l0, l1 = c * Lc, (c + 1) * Lc
+                    stream.wait_event(chunk_ev[c])
+                    kv.kv_score(shape_c, mode, group, inp["q_win"][:, l0:l1], inp["k"][:, l0:l1],
+                                inp["v"][:, l0:l1] if wl.mode != "ada" else None,
+                                inp["w_o"][l0:l1] if inp.get("w_o") is not None else None,
+                                wl.model_dim, scores[:, l0:l1],
+                                crit[:, l0:l1] if crit is not None else None, w_s, stream)
+                stream.wait_event(chunk_ev[nch])
+                step(score=False)
+            else:
+                stream.wait_event(chunk_ev[nch])
+                step()
             res["out"].copy_(out, non_blocking=True)
             res["hb"].copy_(hb, non_blocking=True)
             res["lb"].copy_(lb, non_blocking=True)
@@ -1207,7 +1241,9 @@ def run_ours(args):
         t_e2e = max_over_ranks(statistics.median(e2e_ms), dev)
         e2e = {"value": aggregate_value(world, B, wl.n, L, t_e2e), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e,
-               "steps": args.e2e_steps}
+               "steps": args.e2e_steps,
+               "how": ("inputs copied in %d layer chunks on a copy stream, each chunk scored as "
+                       "it lands" % nch) if nch > 1 else "inputs copied, then the step"}
         del host
 
     # -------------------- the headline workload's other selection paths --------------------
