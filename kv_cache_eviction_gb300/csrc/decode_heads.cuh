@@ -38,4 +38,18 @@ __device__ __forceinline__ HeadRows head_rows(const int64_t* __restrict__ cu,
   return head_rows_of(base, end, lens[h], cap, has_new);
 }
 
+// Atomic add with release semantics (this thread's earlier memory accesses, and those
+// ordered before them by a CTA barrier, are ordered before it); returns the old value.  Like
+// any fence, it holds the thread until the bulk copies it issued have landed: use it only
+// where the thread has none in flight.
+__device__ __forceinline__ uint32_t atom_add_release_u32(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 }  // namespace kv

@@ -492,9 +492,9 @@ decode_parts(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
   // ---- 3. the lengths: bumped by the CTA that counted itself done with them last (early),
   // else by the last CTA to finish (every CTA has read them by then)
   if (tid == 0) {
-    if (!early_bump) done_before = ptx::atom_add_release_u32(&tick[0], 1u);
+    if (!early_bump) done_before = atom_add_release_u32(&tick[0], 1u);
     const int win = done_before == (uint32_t)(Nc - 1) ? 1 : 0;
-    if (win) ptx::fence_acq_rel_gpu();
+    if (win) fence_acq_rel_gpu();
     S.win = win;
   }
   __syncthreads();
