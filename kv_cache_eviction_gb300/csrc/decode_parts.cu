@@ -6,8 +6,9 @@
 // of the flat layout.
 //
 // With one CTA per head (decode_head.cu) a step waits on its longest head.  Here a head's
-// flat rows are cut into part 0 (its first P0 rows) and extra parts of kQPart = 192 rows
-// (4 warps x 3 ring stages of 16 rows: one fill of every warp's ring).  The head's own CTA
+// flat rows are cut into part 0 (its first P0 - 128 to P0 + 63 rows) and extra parts of
+// exactly kQPart = 192 rows from its end (4 warps x 3 ring stages of 16 rows: one fill of
+// every warp's ring).  The head's own CTA
 // takes part 0 and the new row; the extra parts go round-robin to the CTAs past the heads'
 // own (a launch of two CTAs per SM has more CTAs than heads), then to the heads' CTAs.  P0
 // is a multiple of kQPart chosen by every CTA from the head lengths: the smallest of
@@ -66,9 +67,14 @@ struct PartsSmem {
 };
 static_assert(kPartHead + 4 * 128 <= kRedFloats, "a warp's partial fits its buffer (G <= 4)");
 
-// Extra parts of a head of `flat` rows when part 0 holds p0 of them.
+// Extra parts of a head of `flat` rows past part 0's p0: whole parts of kQPart rows taken
+// from the head's end, part 0 keeping the rest (p0 - 128 to p0 + 63 rows).  A remainder of
+// fewer than kQSliver rows stays in part 0 (merging its partial would cost more than
+// reading it there), a longer one becomes an extra part (a third ring fill of the own CTA
+// would cost more than the merge).
+constexpr int kQSliver = 64;
 __device__ __forceinline__ int extra_parts(int flat, int p0) {
-  return flat > p0 ? (flat - p0 + kQPart - 1) / kQPart : 0;
+  return flat > p0 ? (flat - p0 + kQPart - kQSliver) / kQPart : 0;
 }
 }  // namespace
 
@@ -471,8 +477,12 @@ decode_parts(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
                         early_bump ? S.xlen[pidx - nown] : lens[h], cap, has_new);
     }
     // the part's rows (none where the layout, on the lengths, ran past the head's extent)
-    const int r0 = pi == 0 ? 0 : P0 + (pi - 1) * kQPart;
-    const int R = pi == 0 ? min(hr.flat, P0)
+    // (part 0 never holds fewer rows than the first fill requested before the scan, even
+    // where lengths past a head's extent make the layout disagree with its rows: every stage
+    // in flight is read before the CTA moves on)
+    const int R0 = hr.flat - kQPart * (nparts - 1);     // part 0's rows
+    const int r0 = pi == 0 ? 0 : R0 + (pi - 1) * kQPart;
+    const int R = pi == 0 ? max(R0, min(hr.flat, kQPart))
                           : (r0 >= 0 && r0 < hr.flat ? min(hr.flat - r0, kQPart) : 0);
     const int64_t row0 = hr.base + r0;
     const int cnt = my_stages(R);

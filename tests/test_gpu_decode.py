@@ -267,3 +267,14 @@ def test_decode_parts_lengths_bumped_at_the_end():
     lens = np.array([480000, 5])
     c = build_cache(B, L, hkv, G, d, lens, reserve=2, dtype="f32", seed=31)
     check(c, B, L, hkv, G, d, "f32", append=True)
+
+
+@pytest.mark.parametrize("append", [True, False])
+def test_decode_heads_around_whole_extra_parts(append):
+    """Lengths around part 0's smallest size (384 rows) plus whole extra parts of 192: a head
+    is split only where at least one whole extra part fits, part 0 keeping the remainder."""
+    B, L, hkv, G, d = 1, 2, 8, 4, 128
+    lens = np.array([383, 384, 385, 575, 576, 577, 767, 768,
+                     769, 959, 960, 961, 10, 0, 1000, 1151])
+    c = build_cache(B, L, hkv, G, d, lens, reserve=2, dtype="bf16", seed=41)
+    check(c, B, L, hkv, G, d, "bf16", append=append)
