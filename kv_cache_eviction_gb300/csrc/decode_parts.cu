@@ -8,22 +8,21 @@
 // With one CTA per head (decode_head.cu) a step waits on its longest head.  Here a head's
 // flat rows are cut into part 0 (its first P0 - 128 to P0 + 63 rows) and extra parts of
 // exactly kQPart = 192 rows from its end (4 warps x 3 ring stages of 16 rows: one fill of
-// every warp's ring).  The head's own CTA
-// takes part 0 and the new row; the extra parts go round-robin to the CTAs past the heads'
-// own (a launch of two CTAs per SM has more CTAs than heads), then to the heads' CTAs.  P0
-// is a multiple of kQPart chosen by every CTA from the head lengths: the smallest of
-// p0_mult(k) x kQPart whose extra parts all find an idle CTA (else the largest), so a cache of
-// even heads runs one CTA per head and a skewed one spreads its long heads.  A head of one
-// part is written out by its CTA; the parts of a longer head leave partials in global
-// memory and the last of them to finish (a per-head ticket) merges them.
+// every warp's ring).  The head's own CTA takes part 0 and the new row; the extra parts go
+// round-robin to the CTAs past the heads' own (a launch of two CTAs per SM has more CTAs than
+// heads), then to the heads' CTAs.  P0 is a multiple of kQPart chosen by every CTA from the
+// head lengths: the smallest candidate whose extra parts all find an idle CTA (else the
+// largest), so a cache of even heads runs one CTA per head and a skewed one spreads its long
+// heads.  A head of one part is written out by its CTA; the parts of a longer head leave
+// partials in global memory and the last of them to finish (a per-head ticket) merges them.
 //
-//   1. every CTA reads all heads' cu / lens, picks P0 and forms, in shared memory, the
-//      prefix of the heads' extra parts;
+//   1. the head's own CTA loads its q, new row, offsets and length and requests the first
+//      fill of part 0; every CTA then reads all heads' lengths, picks P0 and forms, in
+//      shared memory, the prefix of the heads' extra parts;
 //   2. it takes its parts one at a time.  Stage s (16 rows) of a part belongs to warp s % 4,
 //      which streams its stages through its ring of bulk copies (a stage is refilled as soon
-//      as it is read) and the tile loop of decode_rows16.cuh; the head's own CTA requests the
-//      first fill of part 0 before step 1.  The warps' partials are merged in shared memory
-//      (each warp's transpose buffer);
+//      as it is read) and the tile loop of decode_rows16.cuh.  The warps' partials are merged
+//      in shared memory (each warp's transpose buffer);
 //   3. the lengths of the heads that took the new row are bumped once no CTA reads them any
 //      more: by the last CTA to have read every length it needs (right after its scan, when
 //      no CTA has more than kQXMax extra parts), else by the last CTA to finish; that CTA
@@ -44,12 +43,10 @@ constexpr int kQPart = kQWarps * kQSlice;         // rows of one part
 constexpr int kQPer = (int)((kDecodePartsHeadsMax + kQThreads - 1) / kQThreads);
 static_assert(kQPer * kQThreads >= kDecodePartsHeadsMax, "scan covers every head");
 // candidate sizes of part 0, in parts of kQPart: 2, 3, 4, 6, 8, 12, 16 (arithmetic, not a
-// table: a constant-bank miss would wait behind the step's bulk copies in DRAM).  A head of
-// two fills or less is never split: a second fill of the own CTA's rings costs about what
-// merging partials across CTAs does.
+// table: a constant-bank miss would wait behind the step's bulk copies in DRAM)
 constexpr int kNP0 = 7;
 // extra parts per CTA up to which every CTA reads its extra parts' lengths right after the
-// scan, so the lengths can be bumped early (see step 1 below)
+// scan, so the lengths can be bumped early (step 3)
 constexpr int kQXMax = 8;
 __host__ __device__ constexpr int p0_mult(int k) {
   return k < 3 ? k + 2 : (k & 1 ? 6 : 8) << ((k - 3) >> 1);
