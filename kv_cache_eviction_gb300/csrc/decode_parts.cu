@@ -6,9 +6,10 @@
 // of the flat layout.
 //
 // With one CTA per head (decode_head.cu) a step waits on its longest head.  Here a head's
-// flat rows are cut into part 0 (its first P0 - 128 to P0 + 63 rows) and extra parts of
-// exactly kQPart = 192 rows from its end (4 warps x 3 ring stages of 16 rows: one fill of
-// every warp's ring).  The head's own CTA takes part 0 and the new row; the extra parts go
+// flat rows are cut into part 0 (its first P0 - 128 to P0 + 63 rows, and at least one fill)
+// and extra parts of kQPart = 192 rows (4 warps x 3 ring stages of 16 rows: one fill of every
+// warp's ring) from its end, the one next to part 0 shorter where part 0 keeps a whole first
+// fill.  The head's own CTA takes part 0 and the new row; the extra parts go
 // round-robin to the CTAs past the heads' own (a launch of two CTAs per SM has more CTAs than
 // heads), then to the heads' CTAs.  P0 is a multiple of kQPart chosen by every CTA from the
 // head lengths: the smallest candidate whose extra parts all find an idle CTA (else the
@@ -42,17 +43,17 @@ constexpr int kQSlice = kStages * kStageRows;     // rows of one warp's ring fil
 constexpr int kQPart = kQWarps * kQSlice;         // rows of one part
 constexpr int kQPer = (int)((kDecodePartsHeadsMax + kQThreads - 1) / kQThreads);
 static_assert(kQPer * kQThreads >= kDecodePartsHeadsMax, "scan covers every head");
-// candidate sizes of part 0, in parts of kQPart: 2, 3, 4, 6, 8, 12, 16 (arithmetic, not a
+// candidate sizes of part 0, in parts of kQPart: 1, 2, 3, 4, 6, 8, 12, 16 (arithmetic, not a
 // table: a constant-bank miss would wait behind the step's bulk copies in DRAM)
-constexpr int kNP0 = 7;
+constexpr int kNP0 = 8;
 // extra parts per CTA up to which every CTA reads its extra parts' lengths right after the
 // scan, so the lengths can be bumped early (step 3)
 constexpr int kQXMax = 8;
 __host__ __device__ constexpr int p0_mult(int k) {
-  return k < 3 ? k + 2 : (k & 1 ? 6 : 8) << ((k - 3) >> 1);
+  return k < 4 ? k + 1 : (k & 1 ? 8 : 6) << ((k - 4) >> 1);
 }
-static_assert(p0_mult(0) == 2 && p0_mult(2) == 4 && p0_mult(3) == 6 && p0_mult(4) == 8 &&
-                  p0_mult(5) == 12 && p0_mult(6) == 16, "candidate sizes");
+static_assert(p0_mult(0) == 1 && p0_mult(1) == 2 && p0_mult(3) == 4 && p0_mult(4) == 6 &&
+                  p0_mult(5) == 8 && p0_mult(6) == 12 && p0_mult(7) == 16, "candidate sizes");
 
 struct PartsSmem {
   WarpRing ring[kQWarps];   // a warp's partial goes to its transpose buffer (red)
@@ -65,10 +66,11 @@ struct PartsSmem {
 static_assert(kPartHead + 4 * 128 <= kRedFloats, "a warp's partial fits its buffer (G <= 4)");
 
 // Extra parts of a head of `flat` rows past part 0's p0: whole parts of kQPart rows taken
-// from the head's end, part 0 keeping the rest (p0 - 128 to p0 + 63 rows).  A remainder of
-// fewer than kQSliver rows stays in part 0 (merging its partial would cost more than
-// reading it there), a longer one becomes an extra part (a third ring fill of the own CTA
-// would cost more than the merge).
+// from the head's end, part 0 keeping the rest (p0 - 128 to p0 + 63 rows, and never less
+// than the first fill: with p0 = one fill, the extra part next to part 0 leaves it the rows
+// that fill already holds).  A remainder of fewer than kQSliver rows stays in part 0 (merging
+// its partial would cost more than reading it there), a longer one becomes an extra part (a
+// further ring fill of the own CTA would cost more than the merge).
 constexpr int kQSliver = 64;
 __device__ __forceinline__ int extra_parts(int flat, int p0) {
   return flat > p0 ? (flat - p0 + kQPart - kQSliver) / kQPart : 0;
@@ -477,10 +479,10 @@ decode_parts(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
     // (part 0 never holds fewer rows than the first fill requested before the scan, even
     // where lengths past a head's extent make the layout disagree with its rows: every stage
     // in flight is read before the CTA moves on)
-    const int R0 = hr.flat - kQPart * (nparts - 1);     // part 0's rows
-    const int r0 = pi == 0 ? 0 : R0 + (pi - 1) * kQPart;
-    const int R = pi == 0 ? max(R0, min(hr.flat, kQPart))
-                          : (r0 >= 0 && r0 < hr.flat ? min(hr.flat - r0, kQPart) : 0);
+    const int R0 = hr.flat - kQPart * (nparts - 1);     // rows left to part 0 by the layout
+    const int P0e = max(R0, min(hr.flat, kQPart));       // part 0's rows
+    const int r0 = pi == 0 ? 0 : max(R0 + (pi - 1) * kQPart, P0e);
+    const int R = pi == 0 ? P0e : max(min(R0 + pi * kQPart, hr.flat) - r0, 0);
     const int64_t row0 = hr.base + r0;
     const int cnt = my_stages(R);
     const int fill = min(kStages, cnt);      // stages in flight before the first is read

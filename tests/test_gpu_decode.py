@@ -236,6 +236,23 @@ def test_decode_heads_at_part_boundaries(dtype, d, G):
     check(c, B, L, hkv, G, d, dtype, append=True)
 
 
+@pytest.mark.parametrize("dtype,d,G", [("bf16", 128, 4), ("f32", 64, 2)])
+def test_decode_one_fill_first_parts(dtype, d, G):
+    """256 heads, most shorter than one ring fill (192 rows) and a few around one to three
+    fills, so that their extra parts all find an idle CTA with part 0 at a single fill: the
+    kernel that cuts heads into parts then keeps one fill in part 0 and shortens the extra part
+    next to it by the rows that fill already holds."""
+    B, L, hkv = 1, 32, 8
+    rng = np.random.default_rng(37)
+    H = B * L * hkv
+    lens = rng.integers(1, 190, H)
+    edge = [190, 191, 192, 193, 254, 255, 256, 257, 320, 382, 383, 384, 385, 446, 447, 448,
+            449, 574, 575, 576, 577, 640, 0]
+    lens[rng.choice(H, len(edge), replace=False)] = edge
+    c = build_cache(B, L, hkv, G, d, lens, reserve=2, dtype=dtype, seed=38)
+    check(c, B, L, hkv, G, d, dtype, append=True)
+
+
 def test_decode_most_heads_the_parts_kernel_takes():
     """512 heads (the most the kernel that cuts heads into parts takes) of uneven lengths: more
     heads than CTAs of one wave, so the heads' own CTAs take extra parts too."""
