@@ -396,7 +396,8 @@ KV_API kv_status flat_decode_attn(const kv_shape* shape, const void* q,
  *   device current) and caches it; make that first call before any stream capture.
  * - Every call on a device shares the one array and leaves its last contents there.  Each
  *   call first clears, on its own stream (cudaMemsetAsync, which allocates nothing), the
- *   parts the decode kernels need at zero: the error word and the split decode's tickets.
+ *   parts the decode kernels need at zero: the error word and the tickets and counter of the
+ *   one-launch decode kernels (rows split across CTAs, or heads in parts).
  *   The rest (partials, chunk map, work counter) is written before it is read.
  *   Calls whose kernels overlap on the GPU (different streams without ordering between
  *   them) race on the array and can return wrong outputs: order them on one stream, or use

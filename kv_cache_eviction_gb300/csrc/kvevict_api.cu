@@ -500,7 +500,8 @@ kv_status flat_decode_attn_noalloc(const kv_shape* shape, const void* q, const v
   // The array starts at zero when the library is loaded, but it is shared by every call and
   // no caller reads its error word back.  So each call clears, on its own stream, what the
   // decode kernels need at zero: the error word (a check that fired in an earlier call must
-  // not linger) and the one-launch split's tickets.  Those return to zero at the end of every
+  // not linger) and the tickets and counter of the one-launch kernels (the split and the
+  // heads in parts), which share one region.  Those return to zero at the end of every
   // complete launch; clearing them here also undoes a launch that was cut short or raced
   // with an overlapping call.  The partials, the chunk map and the work counter are written
   // before they are read in every launch.  A memset allocates nothing.
