@@ -129,12 +129,13 @@ decode_parts(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
                    bytes, &ws.full[st]);
   };
   // lane 0 waits for stage ls of the part, the warp runs its tiles, lane 0 refills the stage
-  // with stage ls + 3 when that is below `cnt`; on a wait that gives up, the copies issued and
-  // not yet read (below `issued`) are waited for (bounded) and `ok` turns false
+  // with stage ls + 3 when that is below `cnt`.  Every stage read so far was refilled, so at
+  // stage ls the copies in flight are stages [ls, min(cnt, ls + 3)); on a wait that gives up
+  // those are waited for (bounded) and `ok` turns false.
   Att att;
   bool ok = true;
-  auto consume = [&](int64_t row0, int R, int lo, int hi, int cnt, int issued) {
-    for (int ls = lo; ls < hi && ok; ++ls) {
+  auto consume = [&](int64_t row0, int R, int cnt) {
+    for (int ls = 0; ls < cnt && ok; ++ls) {
       const uint32_t k = seq + ls;
       const int st = (int)(k % kStages);
       const bool landed = ptx::mbar_wait(&ws.full[st], (k / kStages) & 1u);
@@ -142,7 +143,7 @@ decode_parts(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
         ok = false;
         if (lane == 0) {
           raise_dev(hdr, DEV_WAIT_TIMEOUT, 0x900u + (unsigned)st);
-          for (int l2 = ls; l2 < min(issued, ls + kStages); ++l2)
+          for (int l2 = ls; l2 < min(cnt, ls + kStages); ++l2)
             (void)ptx::mbar_wait(&ws.full[(seq + l2) % kStages], ((seq + l2) / kStages) & 1u,
                                  20000000ull);
         }
@@ -493,7 +494,7 @@ decode_parts(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
     if (lane == 0 && ok)
       for (int ls = sent; ls < fill; ++ls) issue(row0, R, ls);
     att.begin(pi == 0 ? qr0 : qr, c2);
-    consume(row0, R, 0, cnt, cnt, fill);
+    consume(row0, R, cnt);
     seq += (uint32_t)cnt;
     finish_part(h, pi, nparts, hr, newrow, nkr0, nvr0);   // the new row is the own head's
   }
