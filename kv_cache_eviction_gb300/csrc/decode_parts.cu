@@ -342,8 +342,8 @@ decode_parts(const T* __restrict__ q, const T* __restrict__ kn, const T* __restr
     hl[i] = h < H ? lens[h] : 0;
   }
   // The head's own CTA requests the first fill of part 0 before the scan, which runs while
-  // the copies are in flight.  Part 0 holds at least kQPart rows, so these are its first
-  // stages whatever P0 turns out to be.  (q and the new row are loaded first: behind the
+  // the copies are in flight.  Part 0 holds at least the head's first min(flat, kQPart) rows,
+  // so these are its first stages whatever P0 turns out to be.  (q and the new row are loaded first: behind the
   // copies they would wait for the step's traffic too.)
   HeadRows own{0, 0, 0, false};
   int pre = 0;   // stages of the own part 0 this warp has requested before the scan
